@@ -1,0 +1,142 @@
+/*
+ * tfqmm.h -- C ABI of the MLX-affine quantized row product for GB300 (sm_103a).
+ *
+ * The operation (TensorFold PR #788 "faster kernels in Zig engine", commit
+ * "every MLX affine width in the row kernel"; PR #774 "oQ support",
+ * Exactness, the Precision bullet):
+ *
+ *     y[r][n] = sum_k x[r][k] * (scale[n][k/G] * q[n][k] + bias[n][k/G])
+ *
+ * for 1..16 activation rows r.  q[n][k] is an unsigned code of `bits` bits
+ * (2, 3, 4, 5, 6 or 8), stored low code first in row n's little-endian
+ * bitstream (3- and 5-bit rows hold eight codes in three or five bytes; every
+ * row ends on a 32-bit word).  scale and bias are bf16, one per group of G = 32,
+ * 64 or 128 consecutive k.  x is bf16; y is fp32, accumulated in fp32.
+ *
+ * Results: every output lies within (K * 2^-24 + 2^-20) * sum_k |x_k * w_k| of
+ * the exact product; a row's bits depend on its own inputs only (the same in a
+ * window of 1..16 rows), and a strided or stacked output equals the contiguous
+ * one bit for bit (the canonical order below fixes the arithmetic).
+ *
+ * Canonical order of one output y[r][n]: K is cut into chunks of 512 k (the
+ * last may be shorter).  Inside a chunk, group by group in k order,
+ *     T = sum over the group of x*q     (tensor-core dot products, exact codes)
+ *     p = fma(scale, T, p); p = fma(bias, sum_group(x), p)     (p starts at 0)
+ * where sum_group(x) is the sequential fp32 sum of the group's x.  Then
+ * y = p_0, y = y + p_1, ... in chunk order.  Row count, N, output stride,
+ * split-K and stack membership never enter this order.
+ *
+ * Memory: every pointer of tf_qmm / tf_qmm_stack / tf_widen is DEVICE memory
+ * owned by the caller; the library never frees or retains it.  Calls are
+ * asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ * The library keeps, per device and stream, a small workspace for split-K
+ * partials and a device status word (allocated on first use, held until exit).
+ * Errors are returned as negative status codes; nothing throws across the ABI.
+ */
+#ifndef TFQMM_H
+#define TFQMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define TF_OK 0
+#define TF_EINVAL_BITS (-1)   /* bits not in {2,3,4,5,6,8} */
+#define TF_EINVAL_GROUP (-2)  /* group not in {32,64,128}, or K % group != 0, or K < 1 */
+#define TF_EINVAL_ROWS (-3)   /* rows not in [1, 16] */
+#define TF_EINVAL_STRIDE (-4) /* y_stride < N (a strided call writes rows at least a matrix wide) */
+#define TF_EINVAL_PTR (-5)    /* NULL pointer, or x / W not 16-byte aligned, y not 4-byte aligned */
+#define TF_EINVAL_SIZE (-6)   /* N < 1, or sizes too large for 32-bit indexing of one row */
+#define TF_ENARROW (-7)       /* tf_widen to fewer bits */
+#define TF_EGROUP (-8)        /* tf_widen to a group that does not divide the source group */
+#define TF_ESTACK (-9)        /* bad stack table: member range outside its run, overlapping
+                                 destinations, a destination past y_stride, mixed K */
+#define TF_ECUDA (-10)        /* a CUDA runtime call failed; see tf_last_error_string() */
+#define TF_EDEVICE (-11)      /* a kernel reported a bounded wait that ran out (device status) */
+
+/*
+ * tf_qmm -- one quantized product.
+ *   x        [rows][K] bf16 (uint16 bit patterns), contiguous, 16-byte aligned.
+ *   W        [N][K*bits/32] uint32, 16-byte aligned.
+ *   scales   [N][K/group] bf16; biases likewise.
+ *   y        fp32; row r, column n is y[r*y_stride + n] for n < N.  Columns
+ *            N..y_stride-1 of each row are not touched.
+ * Returns TF_OK or a negative status (checked on the host before any launch).
+ */
+int tf_qmm(const uint16_t *x, int rows, int K,
+           const uint32_t *W, const uint16_t *scales, const uint16_t *biases,
+           int N, int bits, int group,
+           float *y, int64_t y_stride, void *stream);
+
+/*
+ * Fused stack of members written through one strided output (PR #788, "a
+ * fused stack of 48-column members at mixed widths written through the
+ * stride"; PR #774, runs and members of the _stacked split rule and the
+ * column map that writes each member's columns in place).
+ *
+ * A run is one matrix at one width (usually widened by tf_widen).  A member
+ * takes n_cols consecutive columns of its run starting at src_col and writes
+ * them to y columns [dst_col, dst_col + n_cols).  Members of a run need not be
+ * adjacent in y.  Every member's columns equal the run's own tf_qmm result
+ * bit for bit.  The table is read on the host only.
+ */
+typedef struct tf_run {
+    const uint32_t *W;
+    const uint16_t *scales;
+    const uint16_t *biases;
+    int N;
+    int bits;
+    int group;
+} tf_run;
+
+typedef struct tf_member {
+    int run;
+    int src_col;
+    int n_cols;
+    int dst_col;
+} tf_member;
+
+int tf_qmm_stack(const uint16_t *x, int rows, int K,
+                 const tf_run *runs, int n_runs,
+                 const tf_member *members, int n_members,
+                 float *y, int64_t y_stride, void *stream);
+
+/*
+ * tf_widen -- exact widen / regroup on the device (PR #788, the widen commit:
+ * mixed-width members read as one matrix at their common width, the most bits
+ * and the smallest group; narrowing and groups that do not divide the source
+ * group are refused).  Every code keeps its integer value and is re-packed at
+ * bits_out; every finer group copies its parent group's scale and bias, so the
+ * dequantized fp64 weights are identical bit for bit.
+ *   W_out [N][K*bits_out/32], s_out/b_out [N][K/group_out]: caller-allocated
+ *   device memory (sizes from tf_qmm_bytes).  W and W_out 16-byte aligned.
+ */
+int tf_widen(const uint32_t *W, const uint16_t *scales, const uint16_t *biases,
+             int N, int K, int bits, int group,
+             uint32_t *W_out, uint16_t *s_out, uint16_t *b_out,
+             int bits_out, int group_out, void *stream);
+
+/* Common width of n members: (max bits, min group).  Host only. */
+int tf_common_width(const int *bits, const int *groups, int n, int *bits_out, int *group_out);
+
+/* Byte sizes of W and of one of scales/biases for an (N, K, bits, group) matrix. */
+int tf_qmm_bytes(int N, int K, int bits, int group, int64_t *w_bytes, int64_t *sb_bytes);
+
+/*
+ * Reads and clears the device status word of the current device (synchronizes
+ * the device).  TF_OK, or TF_EDEVICE if a kernel gave up a bounded wait.
+ */
+int tf_device_status(void);
+
+/* Message for the last failing call on this host thread ("" if none). */
+const char *tf_last_error_string(void);
+
+const char *tf_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,151 @@
+"""Python binding of libtfqmm, the MLX-affine quantized row product for GB300.
+
+Argument marshalling only: every step of the product runs in the library's
+CUDA kernels (``csrc/``).  The names and arguments follow ``include/tfqmm.h``.
+Tensors may be passed as torch tensors (their ``data_ptr()`` is used) or as
+raw integer addresses; ``stream`` is a ``torch.cuda.Stream``, a raw
+``cudaStream_t`` integer, or None for torch's current stream.
+
+The library must be built first (``mlx_affine_bit_gb300.build.build()``);
+loading fails loudly when it is missing.  There is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SO = os.path.join(HERE, "_build", "libtfqmm.so")
+
+TF_OK = 0
+STATUS = {
+    -1: "TF_EINVAL_BITS", -2: "TF_EINVAL_GROUP", -3: "TF_EINVAL_ROWS", -4: "TF_EINVAL_STRIDE",
+    -5: "TF_EINVAL_PTR", -6: "TF_EINVAL_SIZE", -7: "TF_ENARROW", -8: "TF_EGROUP",
+    -9: "TF_ESTACK", -10: "TF_ECUDA", -11: "TF_EDEVICE",
+}
+SYMBOLS = ("tf_qmm", "tf_qmm_stack", "tf_widen", "tf_common_width", "tf_qmm_bytes",
+           "tf_device_status", "tf_last_error_string", "tf_version")
+
+
+class TfError(RuntimeError):
+    def __init__(self, rc: int, msg: str):
+        super().__init__("%s (%d): %s" % (STATUS.get(rc, "?"), rc, msg))
+        self.rc = rc
+
+
+class TfRun(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("biases", ctypes.c_void_p),
+                ("N", ctypes.c_int), ("bits", ctypes.c_int), ("group", ctypes.c_int)]
+
+
+class TfMember(ctypes.Structure):
+    _fields_ = [("run", ctypes.c_int), ("src_col", ctypes.c_int), ("n_cols", ctypes.c_int),
+                ("dst_col", ctypes.c_int)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libtfqmm (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(SO):
+            raise ImportError("libtfqmm.so is not built (%s); run mlx_affine_bit_gb300.build.build()" % SO)
+        L = ctypes.CDLL(SO)
+        P, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        L.tf_qmm.argtypes = [P, i32, i32, P, P, P, i32, i32, i32, P, i64, P]
+        L.tf_qmm_stack.argtypes = [P, i32, i32, ctypes.POINTER(TfRun), i32,
+                                   ctypes.POINTER(TfMember), i32, P, i64, P]
+        L.tf_widen.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, i32, i32, P]
+        L.tf_common_width.argtypes = [P, P, i32, P, P]
+        L.tf_qmm_bytes.argtypes = [i32, i32, i32, i32, P, P]
+        L.tf_device_status.argtypes = []
+        L.tf_last_error_string.restype = ctypes.c_char_p
+        L.tf_version.restype = ctypes.c_char_p
+        for name in ("tf_qmm", "tf_qmm_stack", "tf_widen", "tf_common_width", "tf_qmm_bytes",
+                     "tf_device_status"):
+            getattr(L, name).restype = i32
+        _lib = L
+    return _lib
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int) -> None:
+    if rc != TF_OK:
+        raise TfError(rc, lib().tf_last_error_string().decode())
+
+
+def tf_qmm(x, rows, K, W, scales, biases, N, bits, group, y, y_stride, stream=None) -> None:
+    _check(lib().tf_qmm(_ptr(x), rows, K, _ptr(W), _ptr(scales), _ptr(biases), N, bits, group,
+                        _ptr(y), y_stride, _stream(stream)))
+
+
+def tf_qmm_stack(x, rows, K, runs, members, y, y_stride, stream=None) -> None:
+    """runs: [(W, scales, biases, N, bits, group)]; members: [(run, src_col, n_cols, dst_col)]."""
+    rr = (TfRun * len(runs))(*[TfRun(_ptr(W), _ptr(s), _ptr(b), N, bits, g)
+                               for (W, s, b, N, bits, g) in runs])
+    mm = (TfMember * len(members))(*[TfMember(*m) for m in members])
+    _check(lib().tf_qmm_stack(_ptr(x), rows, K, rr, len(runs), mm, len(members), _ptr(y),
+                              y_stride, _stream(stream)))
+
+
+def tf_widen(W, scales, biases, N, K, bits, group, W_out, s_out, b_out, bits_out, group_out,
+             stream=None) -> None:
+    _check(lib().tf_widen(_ptr(W), _ptr(scales), _ptr(biases), N, K, bits, group, _ptr(W_out),
+                          _ptr(s_out), _ptr(b_out), bits_out, group_out, _stream(stream)))
+
+
+def tf_common_width(bits_list, groups_list) -> tuple[int, int]:
+    n = len(bits_list)
+    b = (ctypes.c_int * n)(*bits_list)
+    g = (ctypes.c_int * n)(*groups_list)
+    bo, go = ctypes.c_int(), ctypes.c_int()
+    _check(lib().tf_common_width(b, g, n, ctypes.byref(bo), ctypes.byref(go)))
+    return bo.value, go.value
+
+
+def tf_qmm_bytes(N, K, bits, group) -> tuple[int, int]:
+    wb, sb = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().tf_qmm_bytes(N, K, bits, group, ctypes.byref(wb), ctypes.byref(sb)))
+    return wb.value, sb.value
+
+
+def tf_device_status() -> None:
+    _check(lib().tf_device_status())
+
+
+def tf_version() -> str:
+    return lib().tf_version().decode()
+
+
+def qmm(x, W, scales, biases, bits, group, y=None, y_stride=None, stream=None):
+    """Convenience wrapper on torch tensors: x [rows][K] bf16, W [N][K*bits/32] int32.
+
+    Allocates y [rows][N] fp32 when not given, then calls tf_qmm.
+    """
+    import torch
+    rows, K = x.shape
+    N = W.shape[0]
+    if y is None:
+        y = torch.empty((rows, N), dtype=torch.float32, device=x.device)
+        y_stride = N
+    tf_qmm(x, rows, K, W, scales, biases, N, bits, group, y,
+           y_stride if y_stride is not None else y.stride(0), stream)
+    return y

@@ -1,0 +1,405 @@
+// api.cu -- C ABI of libtfqmm (declared in include/tfqmm.h).
+//
+// Host-side argument checks, the launch planner (column tiles x K slices),
+// the per-(device, stream) split-K workspace, the stack dispatcher and the
+// device widen / regroup kernels.  All arithmetic of the product runs in the
+// kernels of qmm_kernel.cuh.
+#include <cuda_runtime.h>
+
+#include <map>
+#include <mutex>
+#include <string>
+#include <utility>
+
+#include "../../include/tfqmm.h"
+#include "internal.h"
+
+using namespace tfq;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const std::string &msg) {
+    g_err = msg;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *where) {
+    g_err = std::string(where) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+    return TF_ECUDA;
+}
+
+bool valid_bits(int b) { return b == 2 || b == 3 || b == 4 || b == 5 || b == 6 || b == 8; }
+bool valid_group(int g) { return g == 32 || g == 64 || g == 128; }
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_matrix(int K, const uint32_t *W, const uint16_t *s, const uint16_t *b, int N, int bits,
+                 int group) {
+    if (!valid_bits(bits)) return fail(TF_EINVAL_BITS, "bits must be 2, 3, 4, 5, 6 or 8");
+    if (!valid_group(group) || K < group || K % group != 0)
+        return fail(TF_EINVAL_GROUP, "group must be 32, 64 or 128 and divide K");
+    if (N < 1 || K > (1 << 26)) return fail(TF_EINVAL_SIZE, "N must be >= 1 and K <= 2^26");
+    if (!W || !s || !b) return fail(TF_EINVAL_PTR, "NULL weight, scale or bias pointer");
+    if (!aligned(W, 16)) return fail(TF_EINVAL_PTR, "W must be 16-byte aligned");
+    if (!aligned(s, 2) || !aligned(b, 2)) return fail(TF_EINVAL_PTR, "scales/biases must be 2-byte aligned");
+    return TF_OK;
+}
+
+int check_io(const uint16_t *x, int rows, const float *y) {
+    if (rows < 1 || rows > 16) return fail(TF_EINVAL_ROWS, "rows must be in [1, 16]");
+    if (!x || !y) return fail(TF_EINVAL_PTR, "NULL x or y");
+    if (!aligned(x, 16)) return fail(TF_EINVAL_PTR, "x must be 16-byte aligned");
+    if (!aligned(y, 4)) return fail(TF_EINVAL_PTR, "y must be 4-byte aligned");
+    return TF_OK;
+}
+
+// ---------------------------------------------------------------- planner --
+
+struct Plan {
+    int nct, nsl, sl, nchunks, stages, smem, grid, wpitch, sbpitch, stage_bytes, x_off, sx_off,
+        st_off, rows_even;
+};
+
+int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+Plan make_plan(int N, int K, int bits, int group, int rows, int nsm) {
+    Plan p{};
+    p.nct = ceil_div(N, TN);
+    p.nchunks = ceil_div(K, CHUNK);
+    const int max_cps = std::max(1, XS_MAX / (rows * 2 * CHUNK));   // chunks of x a CTA holds
+    double best = 1e30;
+    int best_cps = p.nchunks;
+    for (int nsl = 1; nsl <= p.nchunks; ++nsl) {
+        const int cps = ceil_div(p.nchunks, nsl);
+        if (cps > max_cps || (nsl - 1) * cps >= p.nchunks) continue;
+        const long long items = (long long)p.nct * nsl;
+        const double waves = (double)ceil_div(items, nsm);
+        const double cost = waves * (cps + 0.25);
+        if (cost < best) {
+            best = cost;
+            best_cps = cps;
+        }
+    }
+    p.sl = best_cps * CHUNK;
+    p.nsl = ceil_div(p.nchunks, best_cps);
+    const int len = std::min(p.sl, K);
+    const int SK = stage_k(bits);
+    p.rows_even = (rows + 1) & ~1;
+    p.wpitch = SK * bits / 8 + 16;
+    p.sbpitch = std::max(16, (SK / group) * 2);
+    p.stage_bytes = TN * p.wpitch + 2 * TN * p.sbpitch;
+    const int x_bytes = (rows * len * 2 + 127) & ~127;
+    const int sx_bytes = ((len / group) * p.rows_even * 4 + 127) & ~127;
+    p.x_off = HDR_BYTES;
+    p.sx_off = p.x_off + x_bytes;
+    p.st_off = (p.sx_off + sx_bytes + 127) & ~127;
+    p.stages = std::min(MAX_STAGES, (SMEM_MAX - p.st_off) / p.stage_bytes);
+    p.smem = p.st_off + p.stages * p.stage_bytes;
+    p.grid = (int)std::min<long long>((long long)p.nct * p.nsl, nsm);
+    return p;
+}
+
+// ----------------------------------------------------- per-stream storage --
+
+struct StreamWs {
+    float *ws = nullptr;
+    size_t ws_floats = 0;
+    int *cnt = nullptr;
+    size_t n_cnt = 0;
+};
+
+struct DevState {
+    int nsm = 0;
+    int *status = nullptr;
+};
+
+std::mutex g_mu;
+std::map<int, DevState> g_dev;
+std::map<std::pair<int, cudaStream_t>, StreamWs> g_ws;
+
+int dev_state(DevState **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    DevState &d = g_dev[dev];
+    if (!d.nsm) {
+        e = cudaDeviceGetAttribute(&d.nsm, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        e = cudaMalloc(&d.status, 256);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(status)");
+        e = cudaMemset(d.status, 0, 256);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
+    }
+    *out = &d;
+    return TF_OK;
+}
+
+int stream_ws(cudaStream_t st, size_t floats, size_t counters, StreamWs **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    StreamWs &w = g_ws[{dev, st}];
+    if (w.ws_floats < floats) {
+        if (w.ws) cudaFree(w.ws);
+        w.ws = nullptr;
+        w.ws_floats = 0;
+        e = cudaMalloc(&w.ws, floats * sizeof(float));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+        w.ws_floats = floats;
+    }
+    if (w.n_cnt < counters) {
+        if (w.cnt) cudaFree(w.cnt);
+        w.cnt = nullptr;
+        w.n_cnt = 0;
+        e = cudaMalloc(&w.cnt, counters * sizeof(int));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(counters)");
+        e = cudaMemsetAsync(w.cnt, 0, counters * sizeof(int), st);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(counters)");
+        w.n_cnt = counters;
+    }
+    *out = &w;
+    return TF_OK;
+}
+
+cudaError_t launch(int bits, int group, int nt, const QmmParams &P, int grid, int smem,
+                   cudaStream_t st) {
+    switch (bits) {
+        case 2: return launch_b2(group, nt, P, grid, smem, st);
+        case 3: return launch_b3(group, nt, P, grid, smem, st);
+        case 4: return launch_b4(group, nt, P, grid, smem, st);
+        case 5: return launch_b5(group, nt, P, grid, smem, st);
+        case 6: return launch_b6(group, nt, P, grid, smem, st);
+        case 8: return launch_b8(group, nt, P, grid, smem, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// One run (matrix) written through `nseg` column segments.
+int run_product(const uint16_t *x, int rows, int K, const uint32_t *W, const uint16_t *s,
+                const uint16_t *b, int N, int bits, int group, float *y, int64_t y_stride,
+                int nseg, const int *seg_src, const int *seg_len, const int *seg_dst,
+                cudaStream_t st) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevState *d = nullptr;
+    int rc = dev_state(&d);
+    if (rc) return rc;
+    const Plan pl = make_plan(N, K, bits, group, rows, d->nsm);
+    QmmParams P{};
+    P.x = x;
+    P.W = W;
+    P.s = s;
+    P.b = b;
+    P.y = y;
+    P.status = d->status;
+    P.y_stride = y_stride;
+    P.rows = rows;
+    P.K = K;
+    P.N = N;
+    P.nct = pl.nct;
+    P.nsl = pl.nsl;
+    P.sl = pl.sl;
+    P.nchunks = pl.nchunks;
+    P.n_items = pl.nct * pl.nsl;
+    P.stages = pl.stages;
+    P.bulk = aligned(s, 16) && aligned(b, 16) && (K % (8 * group) == 0);
+    P.wpitch = pl.wpitch;
+    P.sbpitch = pl.sbpitch;
+    P.stage_bytes = pl.stage_bytes;
+    P.x_off = pl.x_off;
+    P.sx_off = pl.sx_off;
+    P.st_off = pl.st_off;
+    P.rows_even = pl.rows_even;
+    P.nseg = nseg;
+    for (int i = 0; i < nseg; ++i) {
+        P.seg_src[i] = seg_src[i];
+        P.seg_len[i] = seg_len[i];
+        P.seg_dst[i] = seg_dst[i];
+    }
+    if (pl.nsl > 1) {
+        StreamWs *w = nullptr;
+        rc = stream_ws(st, (size_t)pl.nchunks * rows * N, (size_t)pl.nct, &w);
+        if (rc) return rc;
+        P.ws = w->ws;
+        P.counters = w->cnt;
+    }
+    const cudaError_t e = launch(bits, group, rows > 8 ? 2 : 1, P, pl.grid, pl.smem, st);
+    if (e != cudaSuccess) return cuda_fail(e, "qmm kernel launch");
+    return TF_OK;
+}
+
+// ------------------------------------------------------------------ widen --
+
+// One thread re-packs 32 consecutive codes of one row (bits_in words in,
+// bits_out words out); every code keeps its integer value.
+__global__ void widen_codes(const uint32_t *W, uint32_t *Wo, long long N, int K, int bi, int bo) {
+    const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    const long long runs = K / 32;
+    if (t >= N * runs) return;
+    const long long n = t / runs, j = t - n * runs;
+    const uint32_t *src = W + n * ((long long)K * bi / 32) + j * bi;
+    uint32_t *dst = Wo + n * ((long long)K * bo / 32) + j * bo;
+    uint32_t out[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    const uint32_t mask = (1u << bi) - 1u;
+    for (int i = 0; i < 32; ++i) {
+        const int ib = i * bi, w = ib >> 5, sh = ib & 31;
+        const uint64_t v = ((uint64_t)(w + 1 < bi ? src[w + 1] : 0u) << 32) | src[w];
+        const uint32_t c = (uint32_t)(v >> sh) & mask;
+        const int ob = i * bo, ow = ob >> 5, osh = ob & 31;
+        out[ow] |= c << osh;
+        if (osh + bo > 32) out[ow + 1] |= c >> (32 - osh);
+    }
+    for (int w = 0; w < bo; ++w) dst[w] = out[w];
+}
+
+// Each finer group copies its parent group's scale and bias.
+__global__ void widen_groups(const uint16_t *s, const uint16_t *b, uint16_t *so, uint16_t *bo,
+                             long long N, int ngi, int ngo, int ratio) {
+    const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    if (t >= N * ngo) return;
+    const long long n = t / ngo, g = t - n * ngo;
+    so[t] = s[n * ngi + g / ratio];
+    bo[t] = b[n * ngi + g / ratio];
+}
+
+}  // namespace
+
+// ============================================================== C ABI ====
+
+extern "C" {
+
+int tf_qmm(const uint16_t *x, int rows, int K, const uint32_t *W, const uint16_t *scales,
+           const uint16_t *biases, int N, int bits, int group, float *y, int64_t y_stride,
+           void *stream) {
+    g_err.clear();
+    int rc = check_matrix(K, W, scales, biases, N, bits, group);
+    if (rc) return rc;
+    rc = check_io(x, rows, y);
+    if (rc) return rc;
+    if (y_stride < N) return fail(TF_EINVAL_STRIDE, "y_stride below N is refused");
+    const int src = 0, len = N, dst = 0;
+    return run_product(x, rows, K, W, scales, biases, N, bits, group, y, y_stride, 1, &src, &len,
+                       &dst, static_cast<cudaStream_t>(stream));
+}
+
+int tf_qmm_stack(const uint16_t *x, int rows, int K, const tf_run *runs, int n_runs,
+                 const tf_member *members, int n_members, float *y, int64_t y_stride,
+                 void *stream) {
+    g_err.clear();
+    int rc = check_io(x, rows, y);
+    if (rc) return rc;
+    if (!runs || !members || n_runs < 1 || n_members < 1)
+        return fail(TF_ESTACK, "empty run or member table");
+    for (int i = 0; i < n_runs; ++i) {
+        rc = check_matrix(K, runs[i].W, runs[i].scales, runs[i].biases, runs[i].N, runs[i].bits,
+                          runs[i].group);
+        if (rc) return rc;
+    }
+    for (int i = 0; i < n_members; ++i) {
+        const tf_member &m = members[i];
+        if (m.run < 0 || m.run >= n_runs) return fail(TF_ESTACK, "member names a missing run");
+        if (m.n_cols < 1 || m.src_col < 0 || m.src_col + m.n_cols > runs[m.run].N)
+            return fail(TF_ESTACK, "member columns outside its run");
+        if (m.dst_col < 0 || (int64_t)m.dst_col + m.n_cols > y_stride)
+            return fail(TF_ESTACK, "member destination past y_stride");
+        for (int j = 0; j < i; ++j) {
+            const tf_member &o = members[j];
+            if (m.dst_col < o.dst_col + o.n_cols && o.dst_col < m.dst_col + m.n_cols)
+                return fail(TF_ESTACK, "member destinations overlap");
+            if (m.run == o.run && m.src_col < o.src_col + o.n_cols && o.src_col < m.src_col + m.n_cols)
+                return fail(TF_ESTACK, "members take overlapping columns of one run");
+        }
+    }
+    for (int r = 0; r < n_runs; ++r) {
+        int src[MAXSEG], len[MAXSEG], dst[MAXSEG], n = 0;
+        for (int i = 0; i < n_members; ++i) {
+            if (members[i].run != r) continue;
+            if (n == MAXSEG) return fail(TF_ESTACK, "more than 16 members in one run");
+            src[n] = members[i].src_col;
+            len[n] = members[i].n_cols;
+            dst[n] = members[i].dst_col;
+            ++n;
+        }
+        if (n == 0) continue;
+        rc = run_product(x, rows, K, runs[r].W, runs[r].scales, runs[r].biases, runs[r].N,
+                         runs[r].bits, runs[r].group, y, y_stride, n, src, len, dst,
+                         static_cast<cudaStream_t>(stream));
+        if (rc) return rc;
+    }
+    return TF_OK;
+}
+
+int tf_widen(const uint32_t *W, const uint16_t *scales, const uint16_t *biases, int N, int K,
+             int bits, int group, uint32_t *W_out, uint16_t *s_out, uint16_t *b_out, int bits_out,
+             int group_out, void *stream) {
+    g_err.clear();
+    int rc = check_matrix(K, W, scales, biases, N, bits, group);
+    if (rc) return rc;
+    if (!valid_bits(bits_out)) return fail(TF_EINVAL_BITS, "bits_out must be 2, 3, 4, 5, 6 or 8");
+    if (!valid_group(group_out)) return fail(TF_EINVAL_GROUP, "group_out must be 32, 64 or 128");
+    if (bits_out < bits) return fail(TF_ENARROW, "narrowing bits is refused");
+    if (group_out > group || group % group_out != 0)
+        return fail(TF_EGROUP, "a group that does not divide the source group is refused");
+    if (!W_out || !s_out || !b_out) return fail(TF_EINVAL_PTR, "NULL output pointer");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const long long nrun = (long long)N * (K / 32);
+    widen_codes<<<(unsigned)((nrun + 255) / 256), 256, 0, st>>>(W, W_out, N, K, bits, bits_out);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "widen_codes launch");
+    const long long ng = (long long)N * (K / group_out);
+    widen_groups<<<(unsigned)((ng + 255) / 256), 256, 0, st>>>(scales, biases, s_out, b_out, N,
+                                                               K / group, K / group_out,
+                                                               group / group_out);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "widen_groups launch");
+    return TF_OK;
+}
+
+int tf_common_width(const int *bits, const int *groups, int n, int *bits_out, int *group_out) {
+    g_err.clear();
+    if (!bits || !groups || !bits_out || !group_out || n < 1)
+        return fail(TF_EINVAL_PTR, "empty member list");
+    int b = 0, g = 1 << 30;
+    for (int i = 0; i < n; ++i) {
+        if (!valid_bits(bits[i])) return fail(TF_EINVAL_BITS, "unsupported member bits");
+        if (!valid_group(groups[i])) return fail(TF_EINVAL_GROUP, "unsupported member group");
+        b = std::max(b, bits[i]);
+        g = std::min(g, groups[i]);
+    }
+    *bits_out = b;
+    *group_out = g;
+    return TF_OK;
+}
+
+int tf_qmm_bytes(int N, int K, int bits, int group, int64_t *w_bytes, int64_t *sb_bytes) {
+    g_err.clear();
+    if (!valid_bits(bits)) return fail(TF_EINVAL_BITS, "bits must be 2, 3, 4, 5, 6 or 8");
+    if (!valid_group(group) || K < group || K % group) return fail(TF_EINVAL_GROUP, "bad group");
+    if (N < 1) return fail(TF_EINVAL_SIZE, "N must be >= 1");
+    if (w_bytes) *w_bytes = (int64_t)N * K * bits / 8;
+    if (sb_bytes) *sb_bytes = (int64_t)N * (K / group) * 2;
+    return TF_OK;
+}
+
+int tf_device_status(void) {
+    g_err.clear();
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevState *d = nullptr;
+    int rc = dev_state(&d);
+    if (rc) return rc;
+    int v = 0;
+    cudaError_t e = cudaMemcpy(&v, d->status, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status)");
+    if (v) {
+        e = cudaMemset(d->status, 0, sizeof v);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
+        return fail(TF_EDEVICE, "a kernel gave up a bounded wait");
+    }
+    return TF_OK;
+}
+
+const char *tf_last_error_string(void) { return g_err.c_str(); }
+
+const char *tf_version(void) { return "tfqmm 0.1.0 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,200 @@
+// unpack.cuh -- MLX-affine codes -> exact bf16 pairs for the tensor-core A operand.
+//
+// Codes are stored low code first in a row's little-endian bitstream
+// (TensorFold PR #788, commit "every MLX affine width in the row kernel":
+// 3- and 5-bit rows hold eight codes in three or five bytes).  The kernel
+// reads a "run" of 8 consecutive codes (8*BITS bits) of one row and forms four
+// bf16x2 registers holding the code pairs (c_i, c_{i+4}), i = 0..3, each code
+// entering as its own exact integer value (PR #788, the 2-bit affine_mm commit:
+// codes enter "as itself, with no offset").
+//
+// Method: a code sitting at bit p of a 16-bit half (p + BITS <= 7) is OR-ed
+// into the mantissa of bf16 128.0 (0x4300), giving 128 + c*2^p exactly; one
+// bf16x2 FMA with (2^-p, -128*2^-p) then yields c exactly.  8-bit codes do not
+// fit the 7 mantissa bits: the low 7 bits enter that way and the top bit picks
+// an addend of -128 or 0.
+//
+// The header compiles as CUDA device code and as plain host C++ (for the CPU
+// unit test of the extraction); host builds emulate the three device
+// primitives (byte permute, funnel shift, bf16x2 fma).
+#pragma once
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define TF_HD __host__ __device__ __forceinline__
+#else
+#define TF_HD inline
+#endif
+
+namespace tfq {
+
+// Byte permute: result byte i = byte (s >> 4i) & 7 of the 8-byte value {b:a};
+// bit 3 of a selector nibble replicates that byte's top bit instead.
+TF_HD uint32_t prmt(uint32_t a, uint32_t b, uint32_t s) {
+#if defined(__CUDA_ARCH__)
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(s));
+    return d;
+#else
+    uint64_t v = ((uint64_t)b << 32) | a;
+    uint32_t d = 0;
+    for (int i = 0; i < 4; ++i) {
+        uint32_t sel = (s >> (4 * i)) & 0xF;
+        uint32_t byte = (uint32_t)(v >> (8 * (sel & 7))) & 0xFF;
+        if (sel & 8) byte = (byte & 0x80) ? 0xFF : 0x00;
+        d |= byte << (8 * i);
+    }
+    return d;
+#endif
+}
+
+// Low 32 bits of ({hi:lo} >> sh), 0 <= sh < 32.
+TF_HD uint32_t funnel(uint32_t lo, uint32_t hi, uint32_t sh) {
+#if defined(__CUDA_ARCH__)
+    return __funnelshift_r(lo, hi, sh);
+#else
+    return (uint32_t)((((uint64_t)hi << 32) | lo) >> (sh & 31));
+#endif
+}
+
+// (a & m) | o  -- one LOP3 on the device.
+TF_HD uint32_t mask_or(uint32_t a, uint32_t m, uint32_t o) { return (a & m) | o; }
+
+// Low half from a, high half from b -- one LOP3 on the device.
+TF_HD uint32_t halves(uint32_t a, uint32_t b) { return (a & 0x0000FFFFu) | (b & 0xFFFF0000u); }
+
+#if !defined(__CUDA_ARCH__)
+inline float bf16_to_float_host(uint16_t h) {
+    union { uint32_t u; float f; } c;
+    c.u = (uint32_t)h << 16;
+    return c.f;
+}
+inline uint16_t float_to_bf16_host_exact(float f) {
+    // Only used on exactly representable values (small integers).
+    union { uint32_t u; float f; } c;
+    c.f = f;
+    return (uint16_t)(c.u >> 16);
+}
+#endif
+
+// d = a * b + c on two bf16 lanes (round to nearest even); exact in every use here.
+TF_HD uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+#if defined(__CUDA_ARCH__)
+    uint32_t d;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+#else
+    uint32_t d = 0;
+    for (int h = 0; h < 2; ++h) {
+        float x = bf16_to_float_host((uint16_t)(a >> (16 * h)));
+        float y = bf16_to_float_host((uint16_t)(b >> (16 * h)));
+        float z = bf16_to_float_host((uint16_t)(c >> (16 * h)));
+        d |= (uint32_t)float_to_bf16_host_exact(x * y + z) << (16 * h);
+    }
+    return d;
+#endif
+}
+
+// bf16x2 constants: 128.0 magic, and (scale, addend) per mantissa position p.
+constexpr uint32_t MAGIC = 0x43004300u;            // 128.0 | 128.0
+constexpr uint32_t ONE2 = 0x3F803F80u;             // 1.0
+constexpr uint32_t NEG128 = 0xC300C300u;           // -128
+constexpr uint32_t Q2 = 0x3E803E80u, NEG32 = 0xC200C200u;   // p=2: 1/4, -32
+constexpr uint32_t Q3 = 0x3E003E00u, NEG16 = 0xC180C180u;   // p=3: 1/8, -16
+constexpr uint32_t Q4 = 0x3D803D80u, NEG8 = 0xC100C100u;    // p=4: 1/16, -8
+
+// Run of 8 codes -> pairs p[i] = (c_i | c_{i+4} << 16) as exact bf16 values.
+// `w` points at the 32-bit word holding the run's first bit; `sh` is that
+// bit's position in the word.  Reads at most w[0], w[1].
+template <int BITS>
+struct Unpack;
+
+template <>
+struct Unpack<2> {  // 16 bits; sh in {0, 16}
+    static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t p[4]) {
+        uint32_t v = w[0] >> sh;
+        uint32_t u = halves(v, v << 8);              // c0..c3 @0,2,4,6 | c4..c7 @16,18,20,22
+        p[0] = hfma2(mask_or(u, 0x00030003u, MAGIC), ONE2, NEG128);
+        p[1] = hfma2(mask_or(u, 0x000C000Cu, MAGIC), Q2, NEG32);
+        p[2] = hfma2(mask_or(u, 0x00300030u, MAGIC), Q4, NEG8);
+        p[3] = hfma2(mask_or(u >> 2, 0x00300030u, MAGIC), Q4, NEG8);
+    }
+};
+
+template <>
+struct Unpack<4> {  // 32 bits; sh == 0
+    static TF_HD void run(const uint32_t *w, uint32_t, uint32_t p[4]) {
+        uint32_t v = w[0];
+        p[0] = hfma2(mask_or(v, 0x000F000Fu, MAGIC), ONE2, NEG128);
+        p[1] = hfma2(mask_or(v >> 4, 0x000F000Fu, MAGIC), ONE2, NEG128);
+        p[2] = hfma2(mask_or(v >> 8, 0x000F000Fu, MAGIC), ONE2, NEG128);
+        p[3] = hfma2(mask_or(v >> 12, 0x000F000Fu, MAGIC), ONE2, NEG128);
+    }
+};
+
+template <>
+struct Unpack<8> {  // 64 bits; sh == 0
+    static TF_HD uint32_t one(uint32_t t) {
+        // t: code a in byte 0, code b in byte 2.
+        uint32_t mant = mask_or(t, 0x007F007Fu, MAGIC);     // 128 + (c & 127)
+        uint32_t sgn = prmt(t, 0u, 0xA484u);                // 0xFF00 per half if c >= 128
+        uint32_t add = ~sgn & NEG128;                       // -128 if c < 128, else 0
+        return hfma2(mant, ONE2, add);
+    }
+    static TF_HD void run(const uint32_t *w, uint32_t, uint32_t p[4]) {
+        uint32_t lo = w[0], hi = w[1];
+        p[0] = one(prmt(lo, hi, 0x0400u));   // byte i of lo -> 0, byte i of hi -> 2
+        p[1] = one(prmt(lo, hi, 0x0501u));
+        p[2] = one(prmt(lo, hi, 0x0602u));
+        p[3] = one(prmt(lo, hi, 0x0703u));
+    }
+};
+
+template <>
+struct Unpack<3> {  // 24 bits; sh in {0, 8, 16, 24}
+    static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t p[4]) {
+        uint32_t v = sh ? funnel(w[0], w[1], sh) : w[0];
+        uint32_t u = halves(v, v << 4);   // c0..c3 @0,3,6,9 | c4..c7 @16,19,22,25
+        p[0] = hfma2(mask_or(u, 0x00070007u, MAGIC), ONE2, NEG128);
+        p[1] = hfma2(mask_or(u, 0x00380038u, MAGIC), Q3, NEG16);
+        uint32_t u2 = u >> 6;             // c2 @0, c3 @3 | c6 @16, c7 @19
+        p[2] = hfma2(mask_or(u2, 0x00070007u, MAGIC), ONE2, NEG128);
+        p[3] = hfma2(mask_or(u2, 0x00380038u, MAGIC), Q3, NEG16);
+    }
+};
+
+template <>
+struct Unpack<5> {  // 40 bits; sh in {0, 8, 16, 24}
+    static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t p[4]) {
+        uint32_t lo = sh ? funnel(w[0], w[1], sh) : w[0];   // run bits 0..31
+        uint32_t hi = w[1] >> sh;                           // run bits 32..39 at 0..7
+        uint32_t u = halves(lo, funnel(lo, hi, 4));         // c0,c1,c2 @0,5,10 | c4,c5,c6 @16,21,26
+        p[0] = hfma2(mask_or(u, 0x001F001Fu, MAGIC), ONE2, NEG128);
+        p[1] = hfma2(mask_or(u >> 5, 0x001F001Fu, MAGIC), ONE2, NEG128);
+        p[2] = hfma2(mask_or(u >> 10, 0x001F001Fu, MAGIC), ONE2, NEG128);
+        uint32_t u3 = halves(lo >> 15, funnel(lo, hi, 19)); // c3 @0 | c7 @16
+        p[3] = hfma2(mask_or(u3, 0x001F001Fu, MAGIC), ONE2, NEG128);
+    }
+};
+
+template <>
+struct Unpack<6> {  // 48 bits; sh in {0, 16}
+    static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t p[4]) {
+        // Run bytes {0,1,3,4} and {1,2,4,5}; raw byte = run byte + sh/8.
+        uint32_t s0 = sh ? 0x6532u : 0x4310u;
+        uint32_t s2 = sh ? 0x7643u : 0x5421u;
+        uint32_t P0 = prmt(w[0], w[1], s0);   // c0 @0, c1 @6 | c4 @16, c5 @22
+        uint32_t P2 = prmt(w[0], w[1], s2);   // c2 @4, c3 @10 | c6 @20, c7 @26
+        p[0] = hfma2(mask_or(P0, 0x003F003Fu, MAGIC), ONE2, NEG128);
+        p[1] = hfma2(mask_or(P0 >> 6, 0x003F003Fu, MAGIC), ONE2, NEG128);
+        p[2] = hfma2(mask_or(P2 >> 4, 0x003F003Fu, MAGIC), ONE2, NEG128);
+        p[3] = hfma2(mask_or(P2 >> 10, 0x003F003Fu, MAGIC), ONE2, NEG128);
+    }
+};
+
+// Position of code (step j, slot e) inside a thread's quarter of a group:
+// step j takes pairs 2*(j%2) and 2*(j%2)+1 of run j/2; slot e = 0,1 are the
+// low/high code of the first pair (A/B register 0), e = 2,3 of the second.
+TF_HD int slot_code(int j, int e) { return 8 * (j >> 1) + 2 * (j & 1) + (e >> 1) + 4 * (e & 1); }
+
+}  // namespace tfq

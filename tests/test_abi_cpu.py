@@ -1,0 +1,84 @@
+"""CPU-only checks of the C ABI: the library builds and loads, exports every
+symbol include/tfqmm.h declares, and refuses bad arguments on the host before
+any CUDA call.  Also runs the host build of the kernel's code unpack."""
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def tf():
+    from mlx_affine_bit_gb300.build import build
+    build()
+    import mlx_affine_bit_gb300 as tf
+    tf.lib()
+    return tf
+
+
+def test_exports_every_declared_symbol(tf):
+    hdr = open(os.path.join(ROOT, "include", "tfqmm.h")).read()
+    declared = set(re.findall(r"^(?:int|const char \*)\s*(tf_\w+)\s*\(", hdr, re.M))
+    assert {"tf_qmm", "tf_qmm_stack", "tf_widen"} <= declared
+    out = subprocess.check_output(["nm", "-D", "--defined-only", tf.SO]).decode()
+    exported = set(re.findall(r"\sT\s(tf_\w+)$", out, re.M))
+    assert declared <= exported, declared - exported
+    for name in declared:
+        getattr(tf.lib(), name)
+
+
+A = 4096  # a 16-byte aligned stand-in address; no call below reaches the device
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bits=7), -1), (dict(bits=1), -1),
+    (dict(group=48), -2), (dict(group=64, K=96), -2), (dict(K=16, group=32), -2),
+    (dict(rows=0), -3), (dict(rows=17), -3),
+    (dict(y_stride=255), -4),
+    (dict(x=0), -5), (dict(W=0), -5), (dict(x=A + 8), -5), (dict(W=A + 4), -5), (dict(y=A + 2), -5),
+    (dict(N=0, y_stride=0), -6),
+])
+def test_tf_qmm_refusals(tf, kw, code):
+    args = dict(x=A, rows=1, K=1024, W=A, s=A, b=A, N=256, bits=4, group=64, y=A, y_stride=256)
+    args.update(kw)
+    rc = tf.lib().tf_qmm(args["x"], args["rows"], args["K"], args["W"], args["s"], args["b"],
+                         args["N"], args["bits"], args["group"], args["y"], args["y_stride"], None)
+    assert rc == code, tf.lib().tf_last_error_string()
+    assert tf.lib().tf_last_error_string()
+
+
+def test_widen_refusals_on_host(tf):
+    L = tf.lib()
+    assert L.tf_widen(A, A, A, 4, 256, 5, 64, A, A, A, 4, 64, None) == -7
+    assert L.tf_widen(A, A, A, 4, 256, 5, 64, A, A, A, 5, 128, None) == -8
+    assert L.tf_widen(A, A, A, 4, 256, 5, 32, A, A, A, 5, 64, None) == -8
+    assert L.tf_widen(A, A, A, 4, 256, 5, 64, A, A, A, 7, 64, None) == -1
+
+
+def test_stack_refusals_on_host(tf):
+    runs = [(A, A, A, 64, 4, 64)]
+    for members in ([(0, 0, 65, 0)], [(1, 0, 8, 0)], [(0, 0, 32, 0), (0, 32, 32, 16)],
+                    [(0, 0, 32, 190)]):
+        with pytest.raises(tf.TfError) as e:
+            tf.tf_qmm_stack(A, 1, 256, runs, members, A, 200, stream=0)
+        assert e.value.rc == -9
+
+
+def test_bytes_and_common_width(tf):
+    assert tf.tf_qmm_bytes(248320, 2048, 6, 32) == (248320 * 2048 * 6 // 8, 248320 * 64 * 2)
+    assert tf.tf_common_width([4, 5, 5, 6], [64, 128, 128, 64]) == (6, 64)
+    assert tf.tf_common_width([4, 5, 5], [64, 128, 128]) == (5, 64)
+    with pytest.raises(tf.TfError):
+        tf.tf_common_width([4, 7], [64, 64])
+    assert "sm_103a" in tf.tf_version()
+
+
+def test_unpack_host_build(tmp_path):
+    exe = str(tmp_path / "unpack_test")
+    subprocess.check_call(["g++", "-O1", "-std=c++17", os.path.join(ROOT, "tests", "unpack_host_test.cpp"),
+                           "-o", exe])
+    out = subprocess.check_output([exe]).decode()
+    assert "PASS" in out

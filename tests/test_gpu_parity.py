@@ -1,0 +1,248 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Bars (TensorFold PR #788 row-kernel and tf-affine-ref commits):
+  (i)   every output within (K*2^-24 + 2^-20) * sum|x*w| of the fp64 product;
+  (ii)  each row alone equals the same row in 2-, 3-, 8- and 16-row windows,
+        bit for bit, at every window position;
+  (iii) strided and stacked outputs equal the contiguous result bit for bit,
+        with the gap columns untouched.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import mlx_affine_bit_gb300 as tf
+from tests.gpu_util import DEV, DevMatrix, control_ratio, dev, oracle_check, run_qmm, sample_cols
+
+pytestmark = pytest.mark.gpu
+
+BITS = (2, 3, 4, 5, 6, 8)
+GROUPS = (32, 64, 128)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    yield
+    torch.cuda.synchronize()
+    tf.tf_device_status()
+
+
+def test_single_matrix_full():
+    m, x = synth.single_matrix()
+    y = run_qmm(DevMatrix(m), dev(x)).cpu().numpy()
+    worst = oracle_check(m, x, y)
+    assert control_ratio(m, x, y) > 1.0          # scales 1% off must exceed the bound
+    print("single matrix worst err/bound %.4f" % worst)
+
+
+@pytest.mark.parametrize("bits", BITS)
+@pytest.mark.parametrize("group", GROUPS)
+@pytest.mark.parametrize("N,K,rows", [(300, 1536, 3), (257, 2048, 11), (33, 1024, 16)])
+def test_widths_small_full(bits, group, N, K, rows):
+    # several column tiles, a ragged column tail, 2-4 K chunks; G=128 at K=1536
+    # takes the producer-copy path (K not a multiple of 8*G).
+    m = synth.make_matrix(N, K, bits, group, 500 + bits * 7 + group, 0.001, 0.03)
+    x = synth.make_x(rows, K, 77 + rows)
+    y = run_qmm(DevMatrix(m), dev(x)).cpu().numpy()
+    oracle_check(m, x, y)
+
+
+@pytest.mark.parametrize("bits,group,seed", synth.width_sweep_cases())
+def test_width_sweep_4096_sampled(bits, group, seed):
+    m = synth.width_sweep_matrix(bits, group, seed)
+    x = synth.make_x(1, m.K, seed)
+    y = run_qmm(DevMatrix(m), dev(x)).cpu().numpy()
+    cols = sample_cols(m.N, 96, seed)
+    oracle_check(m, x, y, cols)
+    control_ratio(m, x, y, cols)   # reported by the bench; here only computed
+
+
+@pytest.mark.parametrize("N,K,seed", synth.DECODE_SHAPES)
+def test_decode_windows_bit_exact(N, K, seed):
+    m = synth.decode_matrix(N, K, seed)
+    dm = DevMatrix(m)
+    x = synth.make_x(16, K, seed)
+    xd = dev(x)
+    alone = [run_qmm(dm, xd[r:r + 1].contiguous()) for r in range(16)]
+    for w in (2, 3, 8, 16):
+        for p0 in range(0, 16 - w + 1):
+            yw = run_qmm(dm, xd[p0:p0 + w].contiguous())
+            for i in range(w):
+                assert torch.equal(yw[i].view(torch.int32), alone[p0 + i][0].view(torch.int32)), (w, p0, i)
+    y16 = run_qmm(dm, xd).cpu().numpy()
+    oracle_check(m, x, y16, sample_cols(N, 48, seed))
+
+
+@pytest.mark.parametrize("rows", list(range(1, 17)))
+def test_every_row_count_matches_alone(rows):
+    m = synth.make_matrix(200, 2048, 5, 64, 9, 0.001, 0.03)
+    dm = DevMatrix(m)
+    x = synth.make_x(rows, m.K, 900 + rows)
+    xd = dev(x)
+    y = run_qmm(dm, xd)
+    for r in range(rows):
+        assert torch.equal(y[r].view(torch.int32), run_qmm(dm, xd[r:r + 1].contiguous())[0].view(torch.int32))
+    oracle_check(m, x, y.cpu().numpy())
+
+
+@pytest.mark.parametrize("bits,group", [(6, 32), (3, 128), (8, 64)])
+def test_strided_equals_contiguous(bits, group):
+    N, K, rows = 500, 2048, 5
+    m = synth.make_matrix(N, K, bits, group, 31, 0.001, 0.03)
+    dm = DevMatrix(m)
+    xd = dev(synth.make_x(rows, K, 31))
+    yc = run_qmm(dm, xd)
+    stride = N + 37
+    ys = run_qmm(dm, xd, y_stride=stride, fill=-1234.5)
+    assert torch.equal(ys[:, :N].view(torch.int32), yc.view(torch.int32))
+    assert torch.all(ys[:, N:] == -1234.5)
+
+
+@pytest.mark.parametrize("N,K,rows", [(1, 32, 1), (17, 96, 2), (16, 64, 16), (129, 4096, 1)])
+def test_edge_shapes(N, K, rows):
+    for bits in (3, 8):
+        m = synth.make_matrix(N, K, bits, 32, 3 * N + K, 0.001, 0.03)
+        x = synth.make_x(rows, K, N)
+        oracle_check(m, x, run_qmm(DevMatrix(m), dev(x)).cpu().numpy())
+
+
+def test_extreme_codes_and_zero_x():
+    from tests.packing import pack
+    N, K = 40, 512
+    for bits in BITS:
+        codes = np.full((N, K), (1 << bits) - 1)
+        codes[::3] = 0
+        m = synth.make_matrix(N, K, bits, 64, 1, 0.001, 0.03)
+        m.W = pack(codes, bits)
+        x = synth.make_x(2, K, 5)
+        oracle_check(m, x, run_qmm(DevMatrix(m), dev(x)).cpu().numpy())
+        y0 = run_qmm(DevMatrix(m), dev(np.zeros((1, K), np.uint16))).cpu().numpy()
+        assert np.all(y0 == 0.0)
+
+
+def test_integer_dot_exact():
+    # s=1, b=0, small integer x: every partial sum is an integer below 2^24, so
+    # the GPU result is exactly the integer dot product.
+    from tests.packing import pack
+    rng = np.random.default_rng(3)
+    N, K = 64, 1024
+    for bits in BITS:
+        codes = rng.integers(0, 1 << bits, size=(N, K))
+        xi = rng.integers(-3, 4, size=(4, K))
+        m = synth.make_matrix(N, K, bits, 32, 2, 0.001, 0.03)
+        m.W = pack(codes, bits)
+        m.scales = synth.to_bf16(np.ones((N, K // 32)))
+        m.biases = synth.to_bf16(np.zeros((N, K // 32)))
+        y = run_qmm(DevMatrix(m), dev(synth.to_bf16(xi.astype(np.float64)))).cpu().numpy()
+        assert np.array_equal(y.astype(np.int64), xi @ codes.T)
+
+
+# ------------------------------------------------------------ widen & stack --
+
+@pytest.mark.parametrize("b0,g0,b1,g1", [(4, 64, 5, 64), (5, 128, 5, 64), (2, 128, 8, 32),
+                                         (3, 32, 6, 32), (6, 64, 6, 64), (5, 64, 8, 32)])
+def test_widen_matches_oracle(b0, g0, b1, g1):
+    N, K = 70, 1024
+    m = synth.make_matrix(N, K, b0, g0, 40 + b0 + g0, 0.001, 0.03)
+    dm = DevMatrix(m)
+    Wo = torch.zeros((N, K * b1 // 32), dtype=torch.int32, device=DEV)
+    so = torch.zeros((N, K // g1), dtype=torch.int16, device=DEV)
+    bo = torch.zeros_like(so)
+    tf.tf_widen(dm.W, dm.s, dm.b, N, K, b0, g0, Wo, so, bo, b1, g1)
+    rW, rs, rb = oracle.widen(m.W, m.scales, m.biases, N, K, b0, g0, b1, g1)
+    assert np.array_equal(Wo.cpu().numpy().view(np.uint32), rW)
+    assert np.array_equal(so.cpu().numpy().view(np.uint16), rs)
+    assert np.array_equal(bo.cpu().numpy().view(np.uint16), rb)
+
+
+def test_widen_refusals():
+    m = synth.make_matrix(4, 256, 5, 64, 1, 0.001, 0.03)
+    dm = DevMatrix(m)
+    out = torch.zeros(4096, dtype=torch.int32, device=DEV)
+    for (b1, g1, code) in ((4, 64, -7), (5, 128, -8), (7, 64, -1)):
+        with pytest.raises(tf.TfError) as e:
+            tf.tf_widen(dm.W, dm.s, dm.b, 4, 256, 5, 64, out, out, out, b1, g1)
+        assert e.value.rc == code
+
+
+def _widen_dev(m, bits, group):
+    Wo = torch.zeros((m.N, m.K * bits // 32), dtype=torch.int32, device=DEV)
+    so = torch.zeros((m.N, m.K // group), dtype=torch.int16, device=DEV)
+    bo = torch.zeros_like(so)
+    dm = DevMatrix(m)
+    tf.tf_widen(dm.W, dm.s, dm.b, m.N, m.K, m.bits, m.group, Wo, so, bo, bits, group)
+    return Wo, so, bo
+
+
+@pytest.mark.parametrize("rows", synth.STACK_ROWS)
+def test_fused_stack(rows):
+    K = synth.STACK_K
+    mats = synth.stack_member_matrices()
+    # runs: members 0-2 widen to 5-bit g64 (6192 columns), member 3 is 6-bit g64 (48)
+    parts = [_widen_dev(m, 5, 64) for m in mats[:3]]
+    W5 = torch.cat([p[0] for p in parts]).contiguous()
+    s5 = torch.cat([p[1] for p in parts]).contiguous()
+    b5 = torch.cat([p[2] for p in parts]).contiguous()
+    m6 = DevMatrix(mats[3])
+    runs = [(W5, s5, b5, 6192, 5, 64), (m6.W, m6.s, m6.b, 48, 6, 64)]
+    stride = 6240
+    x = synth.make_x(rows, K, 60 + rows)
+    xd = dev(x)
+    members = [(0, 0, 4096, 0), (0, 4096, 2048, 4096), (0, 6144, 48, 6144), (1, 0, 48, 6192)]
+    y = torch.full((rows, stride), float("nan"), dtype=torch.float32, device=DEV)
+    tf.tf_qmm_stack(xd, rows, K, runs, members, y, stride)
+    # each run equals its own contiguous product bit for bit
+    y5 = torch.empty((rows, 6192), dtype=torch.float32, device=DEV)
+    tf.tf_qmm(xd, rows, K, W5, s5, b5, 6192, 5, 64, y5, 6192)
+    y6 = torch.empty((rows, 48), dtype=torch.float32, device=DEV)
+    tf.tf_qmm(xd, rows, K, m6.W, m6.s, m6.b, 48, 6, 64, y6, 48)
+    assert torch.equal(y[:, :6192].view(torch.int32), y5.view(torch.int32))
+    assert torch.equal(y[:, 6192:].view(torch.int32), y6.view(torch.int32))
+    # and every member is within the bound of the oracle on its unwidened matrix
+    yn = y.cpu().numpy()
+    off = 0
+    for m in mats:
+        cols = sample_cols(m.N, 40, m.seed)
+        oracle_check(m, x, yn[:, off:off + m.N], cols)
+        off += m.N
+    # non-adjacent destinations through the column map
+    members2 = [(0, 4096, 2048, 0), (1, 0, 48, 2048), (0, 0, 4096, 2096), (0, 6144, 48, 6192)]
+    y2 = torch.full((rows, stride), float("nan"), dtype=torch.float32, device=DEV)
+    tf.tf_qmm_stack(xd, rows, K, runs, members2, y2, stride)
+    assert torch.equal(y2[:, 0:2048].view(torch.int32), y5[:, 4096:6144].view(torch.int32))
+    assert torch.equal(y2[:, 2048:2096].view(torch.int32), y6.view(torch.int32))
+    assert torch.equal(y2[:, 2096:6192].view(torch.int32), y5[:, :4096].view(torch.int32))
+    assert torch.equal(y2[:, 6192:].view(torch.int32), y5[:, 6144:].view(torch.int32))
+
+
+def test_stack_refusals():
+    m = synth.make_matrix(64, 256, 4, 64, 1, 0.001, 0.03)
+    dm = DevMatrix(m)
+    xd = dev(synth.make_x(1, 256, 1))
+    y = torch.zeros((1, 200), dtype=torch.float32, device=DEV)
+    runs = [(dm.W, dm.s, dm.b, 64, 4, 64)]
+    for members in ([(0, 0, 65, 0)], [(1, 0, 8, 0)], [(0, 0, 32, 0), (0, 32, 32, 16)],
+                    [(0, 0, 32, 190)], [(0, 0, 32, 0), (0, 16, 8, 100)]):
+        with pytest.raises(tf.TfError) as e:
+            tf.tf_qmm_stack(xd, 1, 256, runs, members, y, 200)
+        assert e.value.rc == -9
+
+
+# ------------------------------------------------------------------- LM head --
+
+@pytest.mark.parametrize("bits,group,seed", synth.LMHEAD_CASES)
+def test_lmhead_sampled(bits, group, seed):
+    m = synth.lmhead_matrix(bits, group, seed)
+    dm = DevMatrix(m)
+    x = synth.make_x(16, m.K, seed)
+    xd = dev(x)
+    y1 = run_qmm(dm, xd[0:1].contiguous())
+    y16 = run_qmm(dm, xd)
+    assert torch.equal(y16[0].view(torch.int32), y1[0].view(torch.int32))
+    cols = sample_cols(m.N, 64, seed)
+    oracle_check(m, x[0:1], y1.cpu().numpy(), cols)
+    oracle_check(m, x, y16.cpu().numpy(), cols)
