@@ -1,0 +1,330 @@
+#!/usr/bin/env python
+"""Throughput bench of the MLX-affine quantized row product (GB/s of HBM).
+
+A step is one pass of the hot path over its workload; the default workload is
+the one-row 4096 x 4096 width sweep (every bits in {2,3,4,5,6,8} x group in
+{32,64,128}: 18 products a step).  Inputs are resident in HBM when the timed
+region starts; every product reads a different copy of its weights in turn so
+that a buffer is reused only after several L2 sizes of other traffic.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+on a bounded column sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "achieved HBM GB/s (and % of GB300 peak) of quantized GEMV per bits/group/rows"
+L2_BYTES = 129 * 2 ** 20
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def workload_cases(name: str):
+    """[(label, N, K, bits, group, seed, rows)] of a workload."""
+    if name == "sweep":
+        return [("%d/%d" % (b, g), 4096, 4096, b, g, s, 1) for (b, g, s) in synth.width_sweep_cases()]
+    if name == "lmhead":
+        return [("lmhead %d/%d r%d" % (b, g, r), synth.LMHEAD_N, synth.LMHEAD_K, b, g, s, r)
+                for (b, g, s) in synth.LMHEAD_CASES for r in (1,)]
+    if name == "lmhead16":
+        return [("lmhead %d/%d r16" % (b, g), synth.LMHEAD_N, synth.LMHEAD_K, b, g, s, 16)
+                for (b, g, s) in synth.LMHEAD_CASES]
+    if name == "decode":
+        return [("decode %dx%d r%d" % (N, K, r), N, K, 6, 32, s, r)
+                for (N, K, s) in synth.DECODE_SHAPES for r in synth.DECODE_ROWS]
+    raise SystemExit("unknown workload " + name)
+
+
+WORKLOAD_TEXT = {
+    "sweep": "width sweep: N=K=4096, 1 bf16 row, bits {2,3,4,5,6,8} x group {32,64,128} (18 GEMVs a step)",
+    "lmhead": "LM head: N=248320, K=2048, 1 row, 6-bit g32 and 4-bit g64 (2 GEMVs a step)",
+    "lmhead16": "LM head: N=248320, K=2048, 16 rows, 6-bit g32 and 4-bit g64 (2 GEMVs a step)",
+    "decode": "decode windows: 6-bit g32, 12288x2048 and 2048x12288, rows {1,2,3,8,16} (10 GEMVs a step)",
+}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.path = index, None, None
+
+    def start(self):
+        try:
+            out = os.path.join(ROOT, "gpurun_out")
+            os.makedirs(out, exist_ok=True)
+            self.path = os.path.join(out, "clocks_%d.csv" % os.getpid())
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def cpu_sample(cases, cols_per_case: int, nthreads: int):
+    """Time the oracle on `cols_per_case` columns of every case; (GB/s, seconds, desc)."""
+    import oracle
+    total_bytes, t_total = 0, 0.0
+    for (label, N, K, bits, group, seed, rows) in cases:
+        m = synth.make_matrix(min(N, 4096), K, bits, group, seed, 0.001, 0.03)
+        x = synth.make_x(rows, K, seed)
+        cols = np.arange(min(cols_per_case, m.N), dtype=np.int64)
+        t0 = time.perf_counter()
+        oracle.qmm(x, m.W, m.scales, m.biases, m.N, K, bits, group, cols=cols, nthreads=nthreads)
+        t_total += time.perf_counter() - t0
+        total_bytes += len(cols) * (K * bits // 8 + (K // group) * 4 + rows * 4) + rows * K * 2
+    return total_bytes / t_total / 1e9, t_total, total_bytes
+
+
+def run_reference(args, cases):
+    import oracle
+    oracle.build()
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    cores = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        cpu_sample(cases, 1, cores)
+    gbs_list, secs, nbytes = [], 0.0, 0
+    for _ in range(args.steps):
+        g, t, b = cpu_sample(cases, 1, cores)
+        gbs_list.append(g)
+        secs += t
+        nbytes += b
+    value = nbytes / secs / 1e9
+    sample = "fp64 oracle, one output column of each of the %d products per step" % len(cases)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD_TEXT[args.workload], "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def run_gpu(args, cases):
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    import mlx_affine_bit_gb300 as tf
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    tf.lib()
+    stream = torch.cuda.current_stream()
+
+    # Device-resident inputs; enough weight copies that a buffer is reused only
+    # after >= 4 L2 sizes of other traffic.
+    per_step = sum(synth.algorithmic_bytes(N, K, b, g, r) for (_, N, K, b, g, _, r) in cases)
+    copies = max(1, -(-4 * L2_BYTES // per_step))
+    items = []
+    for (label, N, K, bits, group, seed, rows) in cases:
+        m = synth.make_matrix(N, K, bits, group, seed, 0.001, 0.03 if N < 100000 else 0.02)
+        W = torch.from_numpy(m.W.view(np.int32)).to(dev)
+        s = torch.from_numpy(m.scales.view(np.int16)).to(dev)
+        b = torch.from_numpy(m.biases.view(np.int16)).to(dev)
+        reps = [(W, s, b)] + [(W.clone(), s.clone(), b.clone()) for _ in range(copies - 1)]
+        x_h = synth.make_x(rows, K, seed)
+        x = torch.from_numpy(x_h.view(np.int16)).to(dev)
+        y = torch.empty((rows, N), dtype=torch.float32, device=dev)
+        x_pin = torch.from_numpy(x_h.view(np.int16)).pin_memory()
+        y_pin = torch.empty((rows, N), dtype=torch.float32).pin_memory()
+        items.append(dict(label=label, N=N, K=K, bits=bits, group=group, rows=rows, reps=reps, x=x, y=y,
+                          x_pin=x_pin, y_pin=y_pin, bytes=synth.algorithmic_bytes(N, K, bits, group, rows)))
+    torch.cuda.synchronize()
+
+    def launch(it, c):
+        W, s, b = it["reps"][c % len(it["reps"])]
+        tf.tf_qmm(it["x"], it["rows"], it["K"], W, s, b, it["N"], it["bits"], it["group"], it["y"],
+                  it["N"], stream)
+
+    for w in range(args.warmup):
+        for it in items:
+            launch(it, w)
+    torch.cuda.synchronize()
+
+    # ---- timed region: device-resident inputs, events around every launch ----
+    n = len(items)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+          for _ in range(args.steps)]
+    clk = ClockSampler(local)
+    clk.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        for i, it in enumerate(items):
+            ev[k][i][0].record(stream)
+            launch(it, args.warmup + k)
+            ev[k][i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = clk.stop()
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    tf.tf_device_status()
+    per_launch = [[ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps)] for i in range(n)]
+
+    # ---- end to end: pinned host x in, host y out, through the C ABI ----
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, min(args.steps, 200))
+    e0.record(stream)
+    for k in range(e2e_steps):
+        for it in items:
+            it["x"].copy_(it["x_pin"], non_blocking=True)
+            launch(it, k)
+            it["y_pin"].copy_(it["y"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    peak, peak_kind = _peaks()
+    total_bytes = per_step * args.steps * world
+    value = total_bytes / (ms * 1e-3) / 1e9
+    kern_ms = sum(statistics.mean(p) for p in per_launch)   # mean step time inside the kernels
+    achieved = per_step / (kern_ms * 1e-3) / 1e9
+    case_rows = []
+    for i, it in enumerate(items):
+        med = statistics.median(per_launch[i])
+        case_rows.append({"case": it["label"], "bytes": it["bytes"], "median_us": round(med * 1e3, 3),
+                          "gbs": round(it["bytes"] / (med * 1e-3) / 1e9, 1),
+                          "frac_of_peak": round(it["bytes"] / (med * 1e-3) / 1e9 / peak, 4)})
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic_%s.json" % args.workload)
+    if os.path.exists(tpath):
+        try:
+            traffic = json.load(open(tpath)).get("dram_bytes_per_step")
+        except Exception:
+            traffic = None
+    if rank == 0:
+        h2d = sum(it["x_pin"].numel() * 2 for it in items)
+        d2h = sum(it["y_pin"].numel() * 4 for it in items)
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            cores = os.cpu_count() or 1
+            gbs, secs, nb = cpu_sample(cases, 1, cores)          # probe
+            cols = max(1, min(4096, int(12.0 / max(secs, 1e-3))))
+            gbs, secs, nb = cpu_sample(cases, cols, cores)
+            cpu = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                   "sample": "fp64 oracle on the first %d output columns of each product (%.1f s)" % (cols, secs)}
+        print(json.dumps({
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT[args.workload], "parallelism": "replicas" if world > 1 else "1 GPU",
+                       "l2": "weights rotate over %d copies (%.0f MB a step, >= 4x L2 between reuses)"
+                             % (copies, per_step / 1e6)},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_kind": peak_kind,
+                         "traffic": traffic,
+                         "kernel": "tfq::qmm_kernel (all products of the step, bytes / summed launch time)"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": per_step * e2e_steps / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": n * args.steps,
+            "clocks": clocks,
+            "cases": case_rows,
+        }))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="sweep", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    cases = workload_cases(args.workload)
+    if args.impl == "reference":
+        run_reference(args, cases)
+    else:
+        run_gpu(args, cases)
+
+
+if __name__ == "__main__":
+    main()
