@@ -4,6 +4,7 @@
 // the per-(device, stream) split-K workspace, the stack dispatcher and the
 // device widen / regroup kernels.  All arithmetic of the product runs in the
 // kernels of qmm_kernel.cuh.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <map>
@@ -98,6 +99,41 @@ Plan make_plan(int N, int K, int bits, int group, int rows, int nsm) {
     p.smem = p.st_off + p.stages * p.stage_bytes;
     p.grid = (int)std::min<long long>((long long)p.nct * p.nsl, nsm);
     return p;
+}
+
+// ------------------------------------------------------------ TMA maps --
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn g_encode = nullptr;
+
+int get_encoder() {
+    if (g_encode) return TF_OK;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return fail(TF_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    return TF_OK;
+}
+
+// 2D row-major tensor [rows][cols] of `esize`-byte elements, box [box_rows][box_cols].
+int encode_2d(CUtensorMap *m, const void *base, CUtensorMapDataType t, int esize, long long cols,
+              long long rows, int box_cols, int box_rows) {
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(cols * esize)};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, t, 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(TF_ECUDA, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
+    return TF_OK;
 }
 
 // ----------------------------------------------------- per-stream storage --
@@ -203,6 +239,19 @@ int run_product(const uint16_t *x, int rows, int K, const uint32_t *W, const uin
     P.n_items = pl.nct * pl.nsl;
     P.stages = pl.stages;
     P.bulk = aligned(s, 16) && aligned(b, 16) && (K % (8 * group) == 0);
+    if (P.bulk) {
+        rc = get_encoder();
+        if (rc) return rc;
+        const int SK = stage_k(bits);
+        // W box: one stage of codes plus 16 bytes (pitch = 16 mod 128 in shared memory).
+        rc = encode_2d(&P.tmW, W, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, (long long)K * bits / 32, N,
+                       pl.wpitch / 4, TN);
+        if (!rc) rc = encode_2d(&P.tmS, s, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / group, N,
+                                pl.sbpitch / 2, TN);
+        if (!rc) rc = encode_2d(&P.tmB, b, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / group, N,
+                                pl.sbpitch / 2, TN);
+        if (rc) return rc;
+    }
     P.wpitch = pl.wpitch;
     P.sbpitch = pl.sbpitch;
     P.stage_bytes = pl.stage_bytes;

@@ -1,6 +1,7 @@
 // qmm_common.h -- launch parameters shared by the host planner (api.cu) and
 // the kernel template (qmm_kernel.cuh).  Internal to libtfqmm.
 #pragma once
+#include <cuda.h>   // CUtensorMap (type only; the encoder is fetched at run time)
 #include <stdint.h>
 
 #if defined(__CUDACC__)
@@ -25,6 +26,10 @@ constexpr int HDR_BYTES = 256;             // mbarriers + flags at the start of 
 TFQ_HD constexpr int stage_k(int bits) { return bits <= 4 ? 512 : 256; }
 
 struct QmmParams {
+    // 2D TMA descriptors (bulk mode): W as u32 [N][K*bits/32] with a box of
+    // 128 rows x (stage bytes + 16); scales and biases as u16 [N][K/G] with a
+    // box of 128 rows x max(8, stage groups).
+    CUtensorMap tmW, tmS, tmB;
     const uint16_t *x;
     const uint32_t *W;
     const uint16_t *s;
@@ -40,7 +45,7 @@ struct QmmParams {
     int nchunks;
     int n_items;        // nct * nsl, slice-major
     int stages;         // pipeline depth
-    int bulk;           // 1: cp.async.bulk copies; 0: copies by the producer warp
+    int bulk;           // 1: tensor-map TMA copies; 0: copies by the producer warp
     int wpitch;         // bytes per W row in a stage
     int sbpitch;        // bytes per scale (or bias) row in a stage
     int stage_bytes;

@@ -85,11 +85,11 @@ __device__ __forceinline__ void mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+__device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
     asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
             smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
 }
 
@@ -140,6 +140,11 @@ __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
     const int S = P.stages;
     const long long row_bytes = (long long)P.K * BITS / 8;
     const int ngK = P.K / G;
+    if (P.bulk && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&P.tmW) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&P.tmS) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&P.tmB) : "memory");
+    }
     uint32_t it = 0;
     for (int item = blockIdx.x; item < P.n_items; item += gridDim.x) {
         const Item I = item_of(P, item);
@@ -156,18 +161,13 @@ __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
             const int g0 = k0 / G, ng = (k1 - k0) / G;
             const int sboff = sb_offset<G>(P, g0, ng);
             if (P.bulk) {
-                const int sbbytes = ng * 2 < 16 ? 16 : ng * 2;
-                if (lane == 0) mbar_arrive_tx(&full[slot], (uint32_t)(nrows * (wbytes + 2 * sbbytes)));
-                __syncwarp();
-                for (int r = lane; r < nrows; r += 32) {
-                    const long long n = n0 + r;
-                    bulk_g2s(st + r * P.wpitch,
-                             reinterpret_cast<const uint8_t *>(P.W) + n * row_bytes + (long long)k0 * BITS / 8,
-                             (uint32_t)wbytes, &full[slot]);
-                    bulk_g2s(sst + r * P.sbpitch, P.s + n * ngK + g0 - sboff, (uint32_t)sbbytes,
-                             &full[slot]);
-                    bulk_g2s(bst + r * P.sbpitch, P.b + n * ngK + g0 - sboff, (uint32_t)sbbytes,
-                             &full[slot]);
+                // One 2D tensor copy each for codes, scales and biases; rows past N
+                // arrive zero-filled, and the full boxes count toward the bytes.
+                if (lane == 0) {
+                    mbar_arrive_tx(&full[slot], (uint32_t)P.stage_bytes);
+                    tma_2d(st, &P.tmW, k0 * BITS / 32, n0, &full[slot]);
+                    tma_2d(sst, &P.tmS, g0 - sboff, n0, &full[slot]);
+                    tma_2d(bst, &P.tmB, g0 - sboff, n0, &full[slot]);
                 }
             } else {
                 // Odd shapes or alignments: plain 4-byte / 2-byte copies by the warp.
