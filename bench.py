@@ -199,20 +199,37 @@ def run_gpu(args, cases):
                           x_pin=x_pin, y_pin=y_pin, bytes=synth.algorithmic_bytes(N, K, bits, group, rows)))
     torch.cuda.synchronize()
 
-    def launch(it, c):
+    def launch(it, c, st):
         W, s, b = it["reps"][c % len(it["reps"])]
         tf.tf_qmm(it["x"], it["rows"], it["K"], W, s, b, it["N"], it["bits"], it["group"], it["y"],
-                  it["N"], stream)
+                  it["N"], st)
 
-    for w in range(args.warmup):
-        for it in items:
-            launch(it, w)
+    # The timed region replays a CUDA graph of `copies` consecutive steps (each
+    # step = every product of the workload once, on the next weight copy), so
+    # host launch overhead does not enter the device timing.  Event-record
+    # nodes between launches give every launch's device time.
+    n = len(items)
+    cap = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(cap):
+        for w in range(args.warmup):
+            for it in items:
+                launch(it, w, cap)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(copies)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        for c in range(copies):
+            ev[c][0].record(cap)
+            for i, it in enumerate(items):
+                launch(it, c, cap)
+                ev[c][i + 1].record(cap)
+    torch.cuda.synchronize()
+    for _ in range(max(1, args.warmup // copies)):
+        graph.replay()
     torch.cuda.synchronize()
 
-    # ---- timed region: device-resident inputs, events around every launch ----
-    n = len(items)
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-          for _ in range(args.steps)]
+    replays = max(1, -(-args.steps // copies))
+    steps = replays * copies
     clk = ClockSampler(local)
     clk.start()
     if world > 1:
@@ -220,13 +237,10 @@ def run_gpu(args, cases):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for k in range(args.steps):
-        for i, it in enumerate(items):
-            ev[k][i][0].record(stream)
-            launch(it, args.warmup + k)
-            ev[k][i][1].record(stream)
-    t1.record(stream)
+    t0.record(cap)
+    for _ in range(replays):
+        graph.replay()
+    t1.record(cap)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -237,7 +251,9 @@ def run_gpu(args, cases):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms = float(tt.item())
     tf.tf_device_status()
-    per_launch = [[ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps)] for i in range(n)]
+    # per-launch device times of the last replay inside the timed region
+    per_launch = [[ev[c][i].elapsed_time(ev[c][i + 1]) for c in range(copies)] for i in range(n)]
+    args.steps = steps
 
     # ---- end to end: pinned host x in, host y out, through the C ABI ----
     torch.cuda.synchronize()
@@ -248,7 +264,7 @@ def run_gpu(args, cases):
     for k in range(e2e_steps):
         for it in items:
             it["x"].copy_(it["x_pin"], non_blocking=True)
-            launch(it, k)
+            launch(it, k, stream)
             it["y_pin"].copy_(it["y"], non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -261,7 +277,7 @@ def run_gpu(args, cases):
     peak, peak_kind = _peaks()
     total_bytes = per_step * args.steps * world
     value = total_bytes / (ms * 1e-3) / 1e9
-    kern_ms = sum(statistics.mean(p) for p in per_launch)   # mean step time inside the kernels
+    kern_ms = sum(statistics.mean(p) for p in per_launch)   # a step's summed launch times
     achieved = per_step / (kern_ms * 1e-3) / 1e9
     case_rows = []
     for i, it in enumerate(items):
@@ -302,6 +318,8 @@ def run_gpu(args, cases):
             "e2e": {"value": per_step * e2e_steps / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": n * args.steps,
+            "timing": "CUDA graph of %d steps replayed %d times; launch times from event nodes of the last replay"
+                      % (copies, replays),
             "clocks": clocks,
             "cases": case_rows,
         }))

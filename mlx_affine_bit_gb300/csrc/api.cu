@@ -64,19 +64,22 @@ struct Plan {
 
 int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
-Plan make_plan(int N, int K, int bits, int group, int rows, int nsm) {
+Plan layout(int N, int K, int bits, int group, int rows, int nsm, int ctas) {
     Plan p{};
+    const int R = rows > 8 ? 16 : 8;                        // padded B-fragment rows
+    const int xs_max = ctas == 2 ? XS_MAX / 2 : XS_MAX;
+    const int budget = ctas == 2 ? SMEM_PER_SM / 2 - 1024 : SMEM_MAX;
     p.nct = ceil_div(N, TN);
     p.nchunks = ceil_div(K, CHUNK);
-    const int max_cps = std::max(1, XS_MAX / (rows * 2 * CHUNK));   // chunks of x a CTA holds
+    const int max_cps = std::max(1, xs_max / (R * 2 * CHUNK));   // chunks of x a CTA holds
+    const long long slots = (long long)ctas * nsm;
     double best = 1e30;
     int best_cps = p.nchunks;
     for (int nsl = 1; nsl <= p.nchunks; ++nsl) {
         const int cps = ceil_div(p.nchunks, nsl);
         if (cps > max_cps || (nsl - 1) * cps >= p.nchunks) continue;
         const long long items = (long long)p.nct * nsl;
-        const double waves = (double)ceil_div(items, nsm);
-        const double cost = waves * (cps + 0.25);
+        const double cost = (double)ceil_div(items, slots) * (cps + 0.25) * ctas;
         if (cost < best) {
             best = cost;
             best_cps = cps;
@@ -86,19 +89,27 @@ Plan make_plan(int N, int K, int bits, int group, int rows, int nsm) {
     p.nsl = ceil_div(p.nchunks, best_cps);
     const int len = std::min(p.sl, K);
     const int SK = stage_k(bits);
-    p.rows_even = (rows + 1) & ~1;
+    p.rows_even = R;
     p.wpitch = SK * bits / 8 + 16;
     p.sbpitch = std::max(16, (SK / group) * 2);
     p.stage_bytes = TN * p.wpitch + 2 * TN * p.sbpitch;
-    const int x_bytes = (rows * len * 2 + 127) & ~127;
-    const int sx_bytes = ((len / group) * p.rows_even * 4 + 127) & ~127;
+    const int x_bytes = (R * len * 2 + 127) & ~127;
+    const int sx_bytes = ((len / group) * R * 4 + 127) & ~127;
     p.x_off = HDR_BYTES;
     p.sx_off = p.x_off + x_bytes;
     p.st_off = (p.sx_off + sx_bytes + 127) & ~127;
-    p.stages = std::min(MAX_STAGES, (SMEM_MAX - p.st_off) / p.stage_bytes);
+    p.stages = std::min(MAX_STAGES, (budget - p.st_off) / p.stage_bytes);
     p.smem = p.st_off + p.stages * p.stage_bytes;
-    p.grid = (int)std::min<long long>((long long)p.nct * p.nsl, nsm);
+    p.grid = (int)std::min<long long>((long long)p.nct * p.nsl, slots);
     return p;
+}
+
+// Two CTAs per SM (16 consumer warps) when two stages of each still fit;
+// otherwise one CTA per SM with a deeper ring.
+Plan make_plan(int N, int K, int bits, int group, int rows, int nsm) {
+    const Plan two = layout(N, K, bits, group, rows, nsm, 2);
+    if (two.stages >= 2) return two;
+    return layout(N, K, bits, group, rows, nsm, 1);
 }
 
 // ------------------------------------------------------------ TMA maps --
@@ -133,6 +144,51 @@ int encode_2d(CUtensorMap *m, const void *base, CUtensorMapDataType t, int esize
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(TF_ECUDA, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
+    return TF_OK;
+}
+
+// Encoded maps of recently used matrices (a map holds only address and shape).
+struct MapKey {
+    const void *W, *s, *b;
+    int N, K, bits, group;
+    bool operator<(const MapKey &o) const {
+        if (W != o.W) return W < o.W;
+        if (s != o.s) return s < o.s;
+        if (b != o.b) return b < o.b;
+        if (N != o.N) return N < o.N;
+        if (K != o.K) return K < o.K;
+        if (bits != o.bits) return bits < o.bits;
+        return group < o.group;
+    }
+};
+struct MapSet {
+    CUtensorMap W, s, b;
+};
+std::map<MapKey, MapSet> g_maps;
+constexpr size_t MAP_CACHE_MAX = 512;
+
+int tensor_maps(const uint32_t *W, const uint16_t *s, const uint16_t *b, int N, int K, int bits,
+                int group, const Plan &pl, QmmParams &P) {
+    const MapKey key{W, s, b, N, K, bits, group};
+    auto it = g_maps.find(key);
+    if (it == g_maps.end()) {
+        int rc = get_encoder();
+        if (rc) return rc;
+        MapSet ms;
+        // W box: one stage of codes plus 16 bytes (pitch = 16 mod 128 in shared memory).
+        rc = encode_2d(&ms.W, W, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, (long long)K * bits / 32, N,
+                       pl.wpitch / 4, TN);
+        if (!rc) rc = encode_2d(&ms.s, s, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / group, N,
+                                pl.sbpitch / 2, TN);
+        if (!rc) rc = encode_2d(&ms.b, b, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / group, N,
+                                pl.sbpitch / 2, TN);
+        if (rc) return rc;
+        if (g_maps.size() >= MAP_CACHE_MAX) g_maps.clear();
+        it = g_maps.emplace(key, ms).first;
+    }
+    P.tmW = it->second.W;
+    P.tmS = it->second.s;
+    P.tmB = it->second.b;
     return TF_OK;
 }
 
@@ -240,16 +296,7 @@ int run_product(const uint16_t *x, int rows, int K, const uint32_t *W, const uin
     P.stages = pl.stages;
     P.bulk = aligned(s, 16) && aligned(b, 16) && (K % (8 * group) == 0);
     if (P.bulk) {
-        rc = get_encoder();
-        if (rc) return rc;
-        const int SK = stage_k(bits);
-        // W box: one stage of codes plus 16 bytes (pitch = 16 mod 128 in shared memory).
-        rc = encode_2d(&P.tmW, W, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, (long long)K * bits / 32, N,
-                       pl.wpitch / 4, TN);
-        if (!rc) rc = encode_2d(&P.tmS, s, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / group, N,
-                                pl.sbpitch / 2, TN);
-        if (!rc) rc = encode_2d(&P.tmB, b, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / group, N,
-                                pl.sbpitch / 2, TN);
+        rc = tensor_maps(W, s, b, N, K, bits, group, pl, P);
         if (rc) return rc;
     }
     P.wpitch = pl.wpitch;

@@ -20,6 +20,7 @@ constexpr int MAXSEG = 16;     // column segments (stack members) per run
 constexpr int MAX_STAGES = 8;
 constexpr int XS_MAX = 64 * 1024;          // bytes of permuted x a CTA keeps resident
 constexpr int SMEM_MAX = 227 * 1024;       // dynamic shared memory per CTA on sm_103a
+constexpr int SMEM_PER_SM = 228 * 1024;    // shared memory per SM (each CTA reserves 1 KB)
 constexpr int HDR_BYTES = 256;             // mbarriers + flags at the start of smem
 
 // K length of one pipeline stage: 512 k for <= 4 bits, 256 k above (bytes balance).
@@ -50,7 +51,7 @@ struct QmmParams {
     int sbpitch;        // bytes per scale (or bias) row in a stage
     int stage_bytes;
     int x_off, sx_off, st_off;   // smem offsets
-    int rows_even;
+    int rows_even;      // padded rows of the B-fragment and sum_group(x) layouts (8*NT)
     int nseg;
     int seg_src[MAXSEG], seg_len[MAXSEG], seg_dst[MAXSEG];
 };

@@ -202,39 +202,80 @@ __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
 // ------------------------------------------------------------- consumers --
 
 // Activations of one K slice, permuted into mma B-fragment order, and the
-// per-(group,row) sums of x.  B entry (k-step ks, row r, quad lane q) holds
-// the four x values that pair with quad lane q's four codes in that step:
+// per-(group,row) sums of x.  Layout [k-step][R rows][4 quad lanes] of uint2
+// with R = 8*NT (rows >= `rows` are zero), so every B load of a warp is one
+// 8-byte access at a compile-time offset.  Entry (k-step, row, quad lane q)
+// holds the four x values that meet quad lane q's four codes in that step:
 // code i of an 8-code run is paired with code i+4, so a run x0..x7 feeds
 // step 2m as {(x0,x4),(x1,x5)} and step 2m+1 as {(x2,x6),(x3,x7)}.
 // sum_group(x) is the sequential fp32 sum of the group's x in k order.
-template <int G>
+template <int G, int NT>
 __device__ void load_x_slice(const QmmParams &P, const Item &I, uint2 *Bf, float *sx, int tid) {
-    const int rows = P.rows, re = P.rows_even;
+    constexpr int R = 8 * NT;
+    const int rows = P.rows;
     const int ngs = (I.k_hi - I.k_lo) / G;
-    for (int u = tid; u < re * ngs; u += NCW * 32) {
+    for (int u = tid; u < R * ngs; u += NCW * 32) {
         const int r = u / ngs, gs = u - r * ngs;
         float acc = 0.f;
-        if (r < rows) {
-            const uint16_t *src = P.x + (long long)r * P.K + I.k_lo + gs * G;
+        const uint16_t *src = P.x + (long long)r * P.K + I.k_lo + gs * G;
 #pragma unroll 4
-            for (int t = 0; t < G / 8; ++t) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(src + 8 * t);
-                const int qq = (8 * t) / (G / 4), m = ((8 * t) % (G / 4)) / 8;
-                const int ks = gs * (G / 16) + 2 * m;
-                Bf[(ks * rows + r) * 4 + qq] = make_uint2(prmt(v.x, v.z, 0x5410u), prmt(v.x, v.z, 0x7632u));
-                Bf[((ks + 1) * rows + r) * 4 + qq] =
-                    make_uint2(prmt(v.y, v.w, 0x5410u), prmt(v.y, v.w, 0x7632u));
-                acc += bf16f((uint16_t)(v.x & 0xFFFF));
-                acc += bf16f((uint16_t)(v.x >> 16));
-                acc += bf16f((uint16_t)(v.y & 0xFFFF));
-                acc += bf16f((uint16_t)(v.y >> 16));
-                acc += bf16f((uint16_t)(v.z & 0xFFFF));
-                acc += bf16f((uint16_t)(v.z >> 16));
-                acc += bf16f((uint16_t)(v.w & 0xFFFF));
-                acc += bf16f((uint16_t)(v.w >> 16));
-            }
+        for (int t = 0; t < G / 8; ++t) {
+            const int qq = (8 * t) / (G / 4), m = ((8 * t) % (G / 4)) / 8;
+            const int ks = gs * (G / 16) + 2 * m;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (r < rows) v = *reinterpret_cast<const uint4 *>(src + 8 * t);
+            Bf[(ks * R + r) * 4 + qq] = make_uint2(prmt(v.x, v.z, 0x5410u), prmt(v.x, v.z, 0x7632u));
+            Bf[((ks + 1) * R + r) * 4 + qq] = make_uint2(prmt(v.y, v.w, 0x5410u), prmt(v.y, v.w, 0x7632u));
+            acc += bf16f((uint16_t)(v.x & 0xFFFF));
+            acc += bf16f((uint16_t)(v.x >> 16));
+            acc += bf16f((uint16_t)(v.y & 0xFFFF));
+            acc += bf16f((uint16_t)(v.y >> 16));
+            acc += bf16f((uint16_t)(v.z & 0xFFFF));
+            acc += bf16f((uint16_t)(v.z >> 16));
+            acc += bf16f((uint16_t)(v.w & 0xFFFF));
+            acc += bf16f((uint16_t)(v.w >> 16));
         }
-        sx[gs * re + r] = acc;
+        sx[gs * R + r] = acc;
+    }
+}
+
+// One group of this thread's two columns: T = tensor-core dot products of the
+// group's exact codes with x, then p = fma(s,T,p); p = fma(b,sum_group(x),p).
+// pr0/pr1[m]: run m of the thread's quarter in column rows g and g+8 (words);
+// woff: the group's word offset in the stage row; bq: this lane's B entry of
+// the group's first k-step; sxq: the group's sum_group(x) at rows 2q, 2q+1.
+template <int BITS, int G, int NT>
+__device__ __forceinline__ void group_body(const uint32_t *const (&pr0)[G / 32],
+                                           const uint32_t *const (&pr1)[G / 32],
+                                           const uint32_t (&sh)[G / 32], int woff, const uint2 *bq,
+                                           const uint16_t *s0, const uint16_t *s1,
+                                           const uint16_t *b0, const uint16_t *b1,
+                                           const float *sxq, float (&p)[NT][4]) {
+    constexpr int RUNS = G / 32, R = 8 * NT;
+    float c[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
+#pragma unroll
+    for (int m = 0; m < RUNS; ++m) {
+        uint32_t pa[4], pb[4];
+        Unpack<BITS>::run(pr0[m] + woff, sh[m], pa);
+        Unpack<BITS>::run(pr1[m] + woff, sh[m], pb);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const uint2 bb = bq[((2 * m + h) * R + nt * 8) * 4];
+                mma_bf16(c[nt], pa[2 * h], pb[2 * h], pa[2 * h + 1], pb[2 * h + 1], bb.x, bb.y);
+            }
+    }
+    const float sg0 = bf16f(*s0), bg0 = bf16f(*b0), sg1 = bf16f(*s1), bg1 = bf16f(*b1);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const float2 v = *reinterpret_cast<const float2 *>(sxq + nt * 8);
+        p[nt][0] = fmaf(bg0, v.x, fmaf(sg0, c[nt][0], p[nt][0]));
+        p[nt][1] = fmaf(bg0, v.y, fmaf(sg0, c[nt][1], p[nt][1]));
+        p[nt][2] = fmaf(bg1, v.x, fmaf(sg1, c[nt][2], p[nt][2]));
+        p[nt][3] = fmaf(bg1, v.y, fmaf(sg1, c[nt][3], p[nt][3]));
     }
 }
 
@@ -257,26 +298,38 @@ template <int BITS, int G, int NT>
 __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint64_t *empty,
                          volatile int *abort, volatile int *flag) {
     constexpr int SK = stage_k(BITS);
-    constexpr int QG = G / 4;      // codes of a group per quad lane
-    constexpr int RUNS = G / 32;   // 8-code runs per quad lane per group
-    constexpr int STEPS = G / 16;  // mma k-steps per group
+    constexpr int NG = SK / G;               // groups in a full stage
+    constexpr int QG = G / 4;                // codes of a group per quad lane
+    constexpr int RUNS = G / 32;             // 8-code runs per quad lane per group
+    constexpr int STEPS = G / 16;            // mma k-steps per group
+    constexpr int GW = G * BITS / 32;        // words per group of one row
+    constexpr int R = 8 * NT;
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, q = lane & 3;
-    const int S = P.stages, rows = P.rows, re = P.rows_even;
+    const int S = P.stages, rows = P.rows;
     uint2 *Bf = reinterpret_cast<uint2 *>(smem + P.x_off);
     float *sx = reinterpret_cast<float *>(smem + P.sx_off);
+    // This lane's runs inside any group: word offset and bit shift of run m.
+    uint32_t wo[RUNS], sh[RUNS];
+#pragma unroll
+    for (int m = 0; m < RUNS; ++m) {
+        const uint32_t bit = (uint32_t)(q * QG + 8 * m) * BITS;
+        wo[m] = bit >> 5;
+        sh[m] = bit & 31u;
+    }
+    const int row0 = warp * 16 + g;          // stage row of A row g (A row g+8 is row0+8)
     int cur_slice = -1;
     uint32_t it = 0;
     for (int item = blockIdx.x; item < P.n_items; item += gridDim.x) {
         const Item I = item_of(P, item);
         if (I.slice != cur_slice) {
             named_bar_consumers();
-            load_x_slice<G>(P, I, Bf, sx, tid);
+            load_x_slice<G, NT>(P, I, Bf, sx, tid);
             named_bar_consumers();
             cur_slice = I.slice;
         }
-        const int col0 = I.ct * TN + warp * 16 + g;   // A row g -> column col0, row g+8 -> col0+8
+        const int col0 = I.ct * TN + row0;
         float p[NT][4], yv[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -288,80 +341,58 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
             const int slot = it % S;
             mbar_wait(&full[slot], (it / S) & 1u, abort, P.status);
             const uint8_t *st = smem + P.st_off + slot * P.stage_bytes;
-            const int row0 = warp * 16 + g;
             const uint32_t *wr0 = reinterpret_cast<const uint32_t *>(st + row0 * P.wpitch);
             const uint32_t *wr1 = reinterpret_cast<const uint32_t *>(st + (row0 + 8) * P.wpitch);
-            const uint8_t *sbase = st + TN * P.wpitch;
-            const uint16_t *s0 = reinterpret_cast<const uint16_t *>(sbase + row0 * P.sbpitch);
-            const uint16_t *s1 = reinterpret_cast<const uint16_t *>(sbase + (row0 + 8) * P.sbpitch);
-            const uint16_t *b0 = reinterpret_cast<const uint16_t *>(sbase + (TN + row0) * P.sbpitch);
-            const uint16_t *b1 = reinterpret_cast<const uint16_t *>(sbase + (TN + row0 + 8) * P.sbpitch);
+            const uint32_t *pr0[RUNS], *pr1[RUNS];
+#pragma unroll
+            for (int m = 0; m < RUNS; ++m) {
+                pr0[m] = wr0 + wo[m];
+                pr1[m] = wr1 + wo[m];
+            }
             const int ng = (k1 - k0) / G;
             const int sboff = sb_offset<G>(P, k0 / G, ng);
-            for (int gl = 0; gl < ng; ++gl) {
-                const int kg = k0 + gl * G;
-                const int gs = (kg - I.k_lo) / G;
-                float c[NT][4];
+            const uint8_t *sbase = st + TN * P.wpitch;
+            const uint16_t *s0 = reinterpret_cast<const uint16_t *>(sbase + row0 * P.sbpitch) + sboff;
+            const uint16_t *s1 = reinterpret_cast<const uint16_t *>(sbase + (row0 + 8) * P.sbpitch) + sboff;
+            const uint16_t *b0 = reinterpret_cast<const uint16_t *>(sbase + (TN + row0) * P.sbpitch) + sboff;
+            const uint16_t *b1 = reinterpret_cast<const uint16_t *>(sbase + (TN + row0 + 8) * P.sbpitch) + sboff;
+            const int gs0 = (k0 - I.k_lo) / G;
+            const uint2 *bq = Bf + (gs0 * STEPS * R + g) * 4 + q;
+            const float *sxq = sx + gs0 * R + 2 * q;
+            if (ng == NG) {
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
-#pragma unroll
-                for (int m = 0; m < RUNS; ++m) {
-                    const int bo = (gl * G + q * QG + 8 * m) * BITS;   // bit offset in the stage row
-                    uint32_t pa[4], pb[4];
-                    Unpack<BITS>::run(wr0 + (bo >> 5), (uint32_t)(bo & 31), pa);
-                    Unpack<BITS>::run(wr1 + (bo >> 5), (uint32_t)(bo & 31), pb);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int ks = gs * STEPS + 2 * m + h;
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            const int r = nt * 8 + g;
-                            uint2 bb = make_uint2(0u, 0u);
-                            if (r < rows) bb = Bf[(ks * rows + r) * 4 + q];
-                            mma_bf16(c[nt], pa[2 * h], pb[2 * h], pa[2 * h + 1], pb[2 * h + 1], bb.x, bb.y);
-                        }
-                    }
-                }
-                // Group epilogue: p = fma(scale, T, p); p = fma(bias, sum_group(x), p).
-                const float sg0 = bf16f(s0[sboff + gl]), bg0 = bf16f(b0[sboff + gl]);
-                const float sg1 = bf16f(s1[sboff + gl]), bg1 = bf16f(b1[sboff + gl]);
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const int r0 = nt * 8 + 2 * q;
-                    float x0 = 0.f, x1 = 0.f;
-                    if (r0 < re) {
-                        const float2 v = *reinterpret_cast<const float2 *>(sx + gs * re + r0);
-                        x0 = v.x;
-                        x1 = v.y;
-                    }
-                    p[nt][0] = fmaf(bg0, x0, fmaf(sg0, c[nt][0], p[nt][0]));
-                    p[nt][1] = fmaf(bg0, x1, fmaf(sg0, c[nt][1], p[nt][1]));
-                    p[nt][2] = fmaf(bg1, x0, fmaf(sg1, c[nt][2], p[nt][2]));
-                    p[nt][3] = fmaf(bg1, x1, fmaf(sg1, c[nt][3], p[nt][3]));
-                }
-                if ((kg + G) % CHUNK == 0 || kg + G == P.K) {   // end of a canonical chunk
-                    const int chunk = kg / CHUNK;
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        if (P.nsl == 1) {
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) yv[nt][e] = chunk == 0 ? p[nt][e] : yv[nt][e] + p[nt][e];
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int r = nt * 8 + 2 * q + (e & 1);
-                                const int n = col0 + 8 * (e >> 1);
-                                if (r < rows && n < P.N)
-                                    P.ws[((long long)chunk * rows + r) * P.N + n] = p[nt][e];
-                            }
-                        }
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) p[nt][e] = 0.f;
-                    }
-                }
+                for (int gl = 0; gl < NG; ++gl)
+                    group_body<BITS, G, NT>(pr0, pr1, sh, gl * GW, bq + gl * STEPS * R * 4, s0 + gl,
+                                            s1 + gl, b0 + gl, b1 + gl, sxq + gl * R, p);
+            } else {
+#pragma unroll 1
+                for (int gl = 0; gl < ng; ++gl)
+                    group_body<BITS, G, NT>(pr0, pr1, sh, gl * GW, bq + gl * STEPS * R * 4, s0 + gl,
+                                            s1 + gl, b0 + gl, b1 + gl, sxq + gl * R, p);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
+
+            if (k1 % CHUNK == 0 || k1 == P.K) {   // end of a canonical chunk
+                const int chunk = (k1 - 1) / CHUNK;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    if (P.nsl == 1) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) yv[nt][e] = chunk == 0 ? p[nt][e] : yv[nt][e] + p[nt][e];
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int r = nt * 8 + 2 * q + (e & 1);
+                            const int n = col0 + 8 * (e >> 1);
+                            if (r < rows && n < P.N)
+                                P.ws[((long long)chunk * rows + r) * P.N + n] = p[nt][e];
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) p[nt][e] = 0.f;
+                }
+            }
         }
 
         if (P.nsl == 1) {
@@ -402,7 +433,7 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
 // ------------------------------------------------------------------ kernel --
 
 template <int BITS, int G, int NT>
-__global__ void __launch_bounds__(NTHREADS, 1) qmm_kernel(const __grid_constant__ QmmParams P) {
+__global__ void __launch_bounds__(NTHREADS, 2) qmm_kernel(const __grid_constant__ QmmParams P) {
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + MAX_STAGES;
@@ -427,14 +458,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) qmm_kernel(const __grid_constant_
 // Host-side launcher for one width: every group and row-tile count.
 template <int BITS>
 cudaError_t launch_width(int group, int nt, const QmmParams &P, int grid, int smem, cudaStream_t st) {
-#define TFQ_CASE(G_, NT_)                                                                  \
-    if (group == G_ && nt == NT_) {                                                        \
-        auto k = qmm_kernel<BITS, G_, NT_>;                                                \
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                             SMEM_MAX);                                    \
-        if (e != cudaSuccess) return e;                                                    \
-        k<<<grid, NTHREADS, smem, st>>>(P);                                                \
-        return cudaGetLastError();                                                         \
+#define TFQ_CASE(G_, NT_)                                                                     \
+    if (group == G_ && nt == NT_) {                                                           \
+        auto k = qmm_kernel<BITS, G_, NT_>;                                                   \
+        static unsigned attr_set = 0; /* one bit per device: smem limit raised */             \
+        int dev = 0;                                                                          \
+        cudaError_t e = cudaGetDevice(&dev);                                                  \
+        if (e != cudaSuccess) return e;                                                       \
+        const unsigned bit = 1u << (dev & 31);                                                \
+        if (!(__atomic_load_n(&attr_set, __ATOMIC_ACQUIRE) & bit)) {                          \
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_MAX); \
+            if (e != cudaSuccess) return e;                                                   \
+            __atomic_fetch_or(&attr_set, bit, __ATOMIC_RELEASE);                              \
+        }                                                                                     \
+        k<<<grid, NTHREADS, smem, st>>>(P);                                                   \
+        return cudaGetLastError();                                                            \
     }
     TFQ_CASE(32, 1) TFQ_CASE(32, 2) TFQ_CASE(64, 1) TFQ_CASE(64, 2) TFQ_CASE(128, 1) TFQ_CASE(128, 2)
 #undef TFQ_CASE

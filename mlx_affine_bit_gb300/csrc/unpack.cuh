@@ -153,7 +153,7 @@ struct Unpack<8> {  // 64 bits; sh == 0
 template <>
 struct Unpack<3> {  // 24 bits; sh in {0, 8, 16, 24}
     static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t p[4]) {
-        uint32_t v = sh ? funnel(w[0], w[1], sh) : w[0];
+        uint32_t v = funnel(w[0], w[1], sh);
         uint32_t u = halves(v, v << 4);   // c0..c3 @0,3,6,9 | c4..c7 @16,19,22,25
         p[0] = hfma2(mask_or(u, 0x00070007u, MAGIC), ONE2, NEG128);
         p[1] = hfma2(mask_or(u, 0x00380038u, MAGIC), Q3, NEG16);
@@ -166,7 +166,7 @@ struct Unpack<3> {  // 24 bits; sh in {0, 8, 16, 24}
 template <>
 struct Unpack<5> {  // 40 bits; sh in {0, 8, 16, 24}
     static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t p[4]) {
-        uint32_t lo = sh ? funnel(w[0], w[1], sh) : w[0];   // run bits 0..31
+        uint32_t lo = funnel(w[0], w[1], sh);               // run bits 0..31
         uint32_t hi = w[1] >> sh;                           // run bits 32..39 at 0..7
         uint32_t u = halves(lo, funnel(lo, hi, 4));         // c0,c1,c2 @0,5,10 | c4,c5,c6 @16,21,26
         p[0] = hfma2(mask_or(u, 0x001F001Fu, MAGIC), ONE2, NEG128);
