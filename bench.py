@@ -189,7 +189,8 @@ def run_gpu(args, cases):
         W = torch.from_numpy(m.W.view(np.int32)).to(dev)
         s = torch.from_numpy(m.scales.view(np.int16)).to(dev)
         b = torch.from_numpy(m.biases.view(np.int16)).to(dev)
-        reps = [(W, s, b)] + [(W.clone(), s.clone(), b.clone()) for _ in range(copies - 1)]
+        pc = max(copies, -(-4 * L2_BYTES // synth.algorithmic_bytes(N, K, bits, group, rows)))
+        reps = [(W, s, b)] + [(W.clone(), s.clone(), b.clone()) for _ in range(pc - 1)]
         x_h = synth.make_x(rows, K, seed)
         x = torch.from_numpy(x_h.view(np.int16)).to(dev)
         y = torch.empty((rows, N), dtype=torch.float32, device=dev)
@@ -204,10 +205,11 @@ def run_gpu(args, cases):
         tf.tf_qmm(it["x"], it["rows"], it["K"], W, s, b, it["N"], it["bits"], it["group"], it["y"],
                   it["N"], st)
 
-    # The timed region replays a CUDA graph of `copies` consecutive steps (each
-    # step = every product of the workload once, on the next weight copy), so
-    # host launch overhead does not enter the device timing.  Event-record
-    # nodes between launches give every launch's device time.
+    # The timed region replays CUDA graphs, so host launch overhead does not
+    # enter the device timing.  The step graph holds `copies` consecutive steps
+    # (every product once per step, each step on the next weight copy); each
+    # product also has its own graph over its copies (>= 4 L2 sizes of weights)
+    # for its per-launch device time.
     n = len(items)
     cap = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(cap):
@@ -215,17 +217,23 @@ def run_gpu(args, cases):
             for it in items:
                 launch(it, w, cap)
     torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(copies)]
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=cap):
         for c in range(copies):
-            ev[c][0].record(cap)
-            for i, it in enumerate(items):
+            for it in items:
                 launch(it, c, cap)
-                ev[c][i + 1].record(cap)
+    case_graphs = []
+    for it in items:
+        gph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gph, stream=cap):
+            for c in range(len(it["reps"])):
+                launch(it, c, cap)
+        case_graphs.append(gph)
     torch.cuda.synchronize()
     for _ in range(max(1, args.warmup // copies)):
         graph.replay()
+    for gph in case_graphs:
+        gph.replay()
     torch.cuda.synchronize()
 
     replays = max(1, -(-args.steps // copies))
@@ -241,6 +249,16 @@ def run_gpu(args, cases):
     for _ in range(replays):
         graph.replay()
     t1.record(cap)
+    per_launch = []
+    for it, gph in zip(items, case_graphs):
+        reps = max(1, -(-args.steps // len(it["reps"])))
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(cap)
+        for _ in range(reps):
+            gph.replay()
+        c1.record(cap)
+        per_launch.append((c0, c1, reps * len(it["reps"])))
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -251,8 +269,7 @@ def run_gpu(args, cases):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms = float(tt.item())
     tf.tf_device_status()
-    # per-launch device times of the last replay inside the timed region
-    per_launch = [[ev[c][i].elapsed_time(ev[c][i + 1]) for c in range(copies)] for i in range(n)]
+    per_launch = [[c0.elapsed_time(c1) / nl] for (c0, c1, nl) in per_launch]
     args.steps = steps
 
     # ---- end to end: pinned host x in, host y out, through the C ABI ----
@@ -318,8 +335,8 @@ def run_gpu(args, cases):
             "e2e": {"value": per_step * e2e_steps / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": n * args.steps,
-            "timing": "CUDA graph of %d steps replayed %d times; launch times from event nodes of the last replay"
-                      % (copies, replays),
+            "timing": "CUDA graph of %d steps replayed %d times; per-product launch time from its own graph "
+                      "over >= 4 L2 sizes of weight copies" % (copies, replays),
             "clocks": clocks,
             "cases": case_rows,
         }))
