@@ -230,10 +230,11 @@ def run_gpu(args, cases):
                 launch(it, c, cap)
         case_graphs.append(gph)
     torch.cuda.synchronize()
-    for _ in range(max(1, args.warmup // copies)):
-        graph.replay()
-    for gph in case_graphs:
-        gph.replay()
+    with torch.cuda.stream(cap):
+        for _ in range(max(1, args.warmup // copies)):
+            graph.replay()
+        for gph in case_graphs:
+            gph.replay()
     torch.cuda.synchronize()
 
     replays = max(1, -(-args.steps // copies))
@@ -245,20 +246,21 @@ def run_gpu(args, cases):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(cap)
-    for _ in range(replays):
-        graph.replay()
-    t1.record(cap)
     per_launch = []
-    for it, gph in zip(items, case_graphs):
-        reps = max(1, -(-args.steps // len(it["reps"])))
-        c0 = torch.cuda.Event(enable_timing=True)
-        c1 = torch.cuda.Event(enable_timing=True)
-        c0.record(cap)
-        for _ in range(reps):
-            gph.replay()
-        c1.record(cap)
-        per_launch.append((c0, c1, reps * len(it["reps"])))
+    with torch.cuda.stream(cap):          # graph replays run on the current stream
+        t0.record(cap)
+        for _ in range(replays):
+            graph.replay()
+        t1.record(cap)
+        for it, gph in zip(items, case_graphs):
+            reps = max(1, -(-args.steps // len(it["reps"])))
+            c0 = torch.cuda.Event(enable_timing=True)
+            c1 = torch.cuda.Event(enable_timing=True)
+            c0.record(cap)
+            for _ in range(reps):
+                gph.replay()
+            c1.record(cap)
+            per_launch.append((c0, c1, reps * len(it["reps"])))
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
