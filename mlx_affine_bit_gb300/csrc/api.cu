@@ -58,28 +58,31 @@ int check_io(const uint16_t *x, int rows, const float *y) {
 // ---------------------------------------------------------------- planner --
 
 struct Plan {
-    int nct, nsl, sl, nchunks, stages, smem, grid, wpitch, sbpitch, stage_bytes, x_off, sx_off,
-        st_off, rows_even;
+    int nmt, nsl, sl, nchunks, stages, smem, grid, segpitch, sbpitch, stage_bytes, x_off, sx_off,
+        pb_off, st_off, rb, ctas;
+    bool sb3d;
 };
 
 int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
-Plan layout(int N, int K, int bits, int group, int rows, int nsm, int ctas) {
+Plan layout(int N, int K, int bits, int group, int rows, int nsm, int ctas, bool sb3d) {
     Plan p{};
-    const int R = rows > 8 ? 16 : 8;                        // padded B-fragment rows
+    p.rb = row_bucket(rows);
+    p.ctas = ctas;
+    p.sb3d = sb3d;
     const int xs_max = ctas == 2 ? XS_MAX / 2 : XS_MAX;
     const int budget = ctas == 2 ? SMEM_PER_SM / 2 - 1024 : SMEM_MAX;
-    p.nct = ceil_div(N, TN);
+    p.nmt = ceil_div(N, TN);
     p.nchunks = ceil_div(K, CHUNK);
-    const int max_cps = std::max(1, xs_max / (R * 2 * CHUNK));   // chunks of x a CTA holds
+    const int max_cps = std::max(1, xs_max / (p.rb * 2 * CHUNK));   // chunks of x a CTA holds
     const long long slots = (long long)ctas * nsm;
     double best = 1e30;
     int best_cps = p.nchunks;
     for (int nsl = 1; nsl <= p.nchunks; ++nsl) {
         const int cps = ceil_div(p.nchunks, nsl);
         if (cps > max_cps || (nsl - 1) * cps >= p.nchunks) continue;
-        const long long items = (long long)p.nct * nsl;
-        const double cost = (double)ceil_div(items, slots) * (cps + 0.25) * ctas;
+        const long long items = (long long)p.nmt * nsl;
+        const double cost = (double)ceil_div(items, slots) * (cps + (nsl > 1 ? 0.5 : 0.25)) * ctas;
         if (cost < best) {
             best = cost;
             best_cps = cps;
@@ -88,28 +91,29 @@ Plan layout(int N, int K, int bits, int group, int rows, int nsm, int ctas) {
     p.sl = best_cps * CHUNK;
     p.nsl = ceil_div(p.nchunks, best_cps);
     const int len = std::min(p.sl, K);
-    const int SK = stage_k(bits);
-    p.rows_even = R;
-    p.wpitch = SK * bits / 8 + 16;
-    p.sbpitch = std::max(16, (SK / group) * 2);
-    p.stage_bytes = TN * p.wpitch + 2 * TN * p.sbpitch;
-    const int x_bytes = (R * len * 2 + 127) & ~127;
-    const int sx_bytes = ((len / group) * R * 4 + 127) & ~127;
+    const int sbg = CHUNK / group;                          // groups of one stage
+    p.segpitch = SEG * bits / 8 + 16;
+    p.sbpitch = sb3d ? (sbg + 8) * 2 : sbg * 2;
+    p.stage_bytes = SEGS * TN * p.segpitch + 2 * TN * p.sbpitch;
+    const int x_bytes = (p.rb * len * 2 + 127) & ~127;
+    const int sx_bytes = ((len / group) * p.rb * 4 + 127) & ~127;
+    const int pb_bytes = 2 * SEGS * TN * p.rb * 4;
     p.x_off = HDR_BYTES;
     p.sx_off = p.x_off + x_bytes;
-    p.st_off = (p.sx_off + sx_bytes + 127) & ~127;
+    p.pb_off = p.sx_off + sx_bytes;
+    p.st_off = (p.pb_off + pb_bytes + 127) & ~127;
     p.stages = std::min(MAX_STAGES, (budget - p.st_off) / p.stage_bytes);
     p.smem = p.st_off + p.stages * p.stage_bytes;
-    p.grid = (int)std::min<long long>((long long)p.nct * p.nsl, slots);
+    p.grid = (int)std::min<long long>((long long)p.nmt * p.nsl, slots);
     return p;
 }
 
-// Two CTAs per SM (16 consumer warps) when two stages of each still fit;
+// Two CTAs per SM (16 consumer warps) when three stages of each still fit;
 // otherwise one CTA per SM with a deeper ring.
-Plan make_plan(int N, int K, int bits, int group, int rows, int nsm) {
-    const Plan two = layout(N, K, bits, group, rows, nsm, 2);
-    if (two.stages >= 2) return two;
-    return layout(N, K, bits, group, rows, nsm, 1);
+Plan make_plan(int N, int K, int bits, int group, int rows, int nsm, bool sb3d) {
+    const Plan two = layout(N, K, bits, group, rows, nsm, 2, sb3d);
+    if (two.stages >= 3) return two;
+    return layout(N, K, bits, group, rows, nsm, 1, sb3d);
 }
 
 // ------------------------------------------------------------ TMA maps --
@@ -142,8 +146,23 @@ int encode_2d(CUtensorMap *m, const void *base, CUtensorMapDataType t, int esize
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(m, t, 2, const_cast<void *>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(TF_ECUDA, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
+    return TF_OK;
+}
+
+// A 3D view {d0, d1, d2} (d0 innermost, stride 4 or 2 bytes) with byte
+// strides s1, s2 and box {b0, b1, b2}.
+int encode_3d(CUtensorMap *m, const void *base, CUtensorMapDataType t, long long d0, long long d1,
+              long long d2, long long s1, long long s2, int b0, int b1, int b2) {
+    cuuint64_t dims[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
+    cuuint64_t strides[2] = {(cuuint64_t)s1, (cuuint64_t)s2};
+    cuuint32_t box[3] = {(cuuint32_t)b0, (cuuint32_t)b1, (cuuint32_t)b2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, t, 3, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(TF_ECUDA, "cuTensorMapEncodeTiled(3D) failed (" + std::to_string((int)r) + ")");
     return TF_OK;
 }
 
@@ -175,13 +194,22 @@ int tensor_maps(const uint32_t *W, const uint16_t *s, const uint16_t *b, int N, 
         int rc = get_encoder();
         if (rc) return rc;
         MapSet ms;
-        // W box: one stage of codes plus 16 bytes (pitch = 16 mod 128 in shared memory).
-        rc = encode_2d(&ms.W, W, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, (long long)K * bits / 32, N,
-                       pl.wpitch / 4, TN);
-        if (!rc) rc = encode_2d(&ms.s, s, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / group, N,
-                                pl.sbpitch / 2, TN);
-        if (!rc) rc = encode_2d(&ms.b, b, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / group, N,
-                                pl.sbpitch / 2, TN);
+        const long long segw = SEG * bits / 32, rowb = (long long)K * bits / 8;
+        // W as {segment words, rows, segments}: a box of 16 rows x 8 segments of
+        // one stage lands segment-major with a row pitch of segment + 16 bytes
+        // (the 4 words past each segment's extent are zero-filled, not read).
+        rc = encode_3d(&ms.W, W, CU_TENSOR_MAP_DATA_TYPE_UINT32, segw, N, K / SEG, rowb, segw * 4,
+                       (int)segw + 4, TN, SEGS);
+        const int sbg = CHUNK / group;
+        for (int i = 0; i < 2 && !rc; ++i) {
+            CUtensorMap *m = i ? &ms.b : &ms.s;
+            const void *base = i ? (const void *)b : (const void *)s;
+            if (pl.sb3d)   // {stage groups, stages, rows}, box padded by 8 zero-filled groups
+                rc = encode_3d(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT16, sbg, K / CHUNK, N, sbg * 2,
+                               (long long)(K / group) * 2, sbg + 8, 1, TN);
+            else
+                rc = encode_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / group, N, sbg, TN);
+        }
         if (rc) return rc;
         if (g_maps.size() >= MAP_CACHE_MAX) g_maps.clear();
         it = g_maps.emplace(key, ms).first;
@@ -254,15 +282,15 @@ int stream_ws(cudaStream_t st, size_t floats, size_t counters, StreamWs **out) {
     return TF_OK;
 }
 
-cudaError_t launch(int bits, int group, int nt, const QmmParams &P, int grid, int smem,
+cudaError_t launch(int bits, int group, int rb, const QmmParams &P, int grid, int smem,
                    cudaStream_t st) {
     switch (bits) {
-        case 2: return launch_b2(group, nt, P, grid, smem, st);
-        case 3: return launch_b3(group, nt, P, grid, smem, st);
-        case 4: return launch_b4(group, nt, P, grid, smem, st);
-        case 5: return launch_b5(group, nt, P, grid, smem, st);
-        case 6: return launch_b6(group, nt, P, grid, smem, st);
-        case 8: return launch_b8(group, nt, P, grid, smem, st);
+        case 2: return launch_b2(group, rb, P, grid, smem, st);
+        case 3: return launch_b3(group, rb, P, grid, smem, st);
+        case 4: return launch_b4(group, rb, P, grid, smem, st);
+        case 5: return launch_b5(group, rb, P, grid, smem, st);
+        case 6: return launch_b6(group, rb, P, grid, smem, st);
+        case 8: return launch_b8(group, rb, P, grid, smem, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -276,7 +304,9 @@ int run_product(const uint16_t *x, int rows, int K, const uint32_t *W, const uin
     DevState *d = nullptr;
     int rc = dev_state(&d);
     if (rc) return rc;
-    const Plan pl = make_plan(N, K, bits, group, rows, d->nsm);
+    const bool bulk = aligned(s, 16) && aligned(b, 16) && K % SEG == 0 && K % (8 * group) == 0;
+    const bool sb3d = bulk && K % CHUNK == 0;
+    const Plan pl = make_plan(N, K, bits, group, rows, d->nsm, sb3d);
     QmmParams P{};
     P.x = x;
     P.W = W;
@@ -288,38 +318,39 @@ int run_product(const uint16_t *x, int rows, int K, const uint32_t *W, const uin
     P.rows = rows;
     P.K = K;
     P.N = N;
-    P.nct = pl.nct;
+    P.nmt = pl.nmt;
     P.nsl = pl.nsl;
     P.sl = pl.sl;
     P.nchunks = pl.nchunks;
-    P.n_items = pl.nct * pl.nsl;
+    P.n_items = pl.nmt * pl.nsl;
     P.stages = pl.stages;
-    P.bulk = aligned(s, 16) && aligned(b, 16) && (K % (8 * group) == 0);
-    if (P.bulk) {
+    P.bulk = bulk;
+    P.sb3d = sb3d;
+    if (bulk) {
         rc = tensor_maps(W, s, b, N, K, bits, group, pl, P);
         if (rc) return rc;
     }
-    P.wpitch = pl.wpitch;
+    P.segpitch = pl.segpitch;
     P.sbpitch = pl.sbpitch;
     P.stage_bytes = pl.stage_bytes;
     P.x_off = pl.x_off;
     P.sx_off = pl.sx_off;
+    P.pb_off = pl.pb_off;
     P.st_off = pl.st_off;
-    P.rows_even = pl.rows_even;
-    P.nseg = nseg;
+    P.ncs = nseg;
     for (int i = 0; i < nseg; ++i) {
-        P.seg_src[i] = seg_src[i];
-        P.seg_len[i] = seg_len[i];
-        P.seg_dst[i] = seg_dst[i];
+        P.cs_src[i] = seg_src[i];
+        P.cs_len[i] = seg_len[i];
+        P.cs_dst[i] = seg_dst[i];
     }
     if (pl.nsl > 1) {
         StreamWs *w = nullptr;
-        rc = stream_ws(st, (size_t)pl.nchunks * rows * N, (size_t)pl.nct, &w);
+        rc = stream_ws(st, (size_t)pl.nchunks * rows * N, (size_t)pl.nmt, &w);
         if (rc) return rc;
         P.ws = w->ws;
         P.counters = w->cnt;
     }
-    const cudaError_t e = launch(bits, group, rows > 8 ? 2 : 1, P, pl.grid, pl.smem, st);
+    const cudaError_t e = launch(bits, group, pl.rb, P, pl.grid, pl.smem, st);
     if (e != cudaSuccess) return cuda_fail(e, "qmm kernel launch");
     return TF_OK;
 }
@@ -407,10 +438,10 @@ int tf_qmm_stack(const uint16_t *x, int rows, int K, const tf_run *runs, int n_r
         }
     }
     for (int r = 0; r < n_runs; ++r) {
-        int src[MAXSEG], len[MAXSEG], dst[MAXSEG], n = 0;
+        int src[MAXCOLSEG], len[MAXCOLSEG], dst[MAXCOLSEG], n = 0;
         for (int i = 0; i < n_members; ++i) {
             if (members[i].run != r) continue;
-            if (n == MAXSEG) return fail(TF_ESTACK, "more than 16 members in one run");
+            if (n == MAXCOLSEG) return fail(TF_ESTACK, "more than 16 members in one run");
             src[n] = members[i].src_col;
             len[n] = members[i].n_cols;
             dst[n] = members[i].dst_col;

@@ -1,9 +1,9 @@
-// qmm_b8.cu -- kernel instantiations for 8-bit codes (groups 32/64/128, 1-8 and 9-16 rows).
+// qmm_b8.cu -- kernel instantiations for 8-bit codes (groups 32/64/128, row buckets 2/4/8/16).
 #include "internal.h"
 #include "qmm_kernel.cuh"
 
 namespace tfq {
-cudaError_t launch_b8(int group, int nt, const QmmParams &P, int grid, int smem, cudaStream_t st) {
-    return launch_width<8>(group, nt, P, grid, smem, st);
+cudaError_t launch_b8(int group, int rb, const QmmParams &P, int grid, int smem, cudaStream_t st) {
+    return launch_width<8>(group, rb, P, grid, smem, st);
 }
 }  // namespace tfq

@@ -5,13 +5,15 @@
 // group-sum form with fp32 group sums, PR #774 Exactness, Precision bullet).
 //
 // One CTA = 8 consumer warps + 1 producer warp, persistent over work items
-// (a tile of 128 output columns x one K slice).  The producer streams each
-// item's packed codes and scales/biases into a ring of shared-memory stages
-// with cp.async.bulk (TMA, completion on mbarriers).  Each consumer warp owns
-// 16 columns: it unpacks 8-code runs straight into bf16 A fragments (codes
-// exact), multiplies them by the activations with mma.sync m16n8k16 (rows are
-// the N dimension, so 1..8 rows cost one MMA and 9..16 two), and applies each
-// group's scale and bias to the fp32 group sum in registers.
+// (16 output columns x one K slice).  A pipeline stage is those 16 rows x
+// 2048 k: one 3D tensor-map TMA copy for the codes (a contiguous 8-32 KB of
+// HBM when the slice is the whole row) and one each for scales and biases,
+// completed on mbarriers.  Each consumer warp takes one 256-k segment of the
+// stage: it unpacks 8-code runs straight into bf16 A fragments (codes exact),
+// multiplies them by the activations with mma.sync m16n8k16 (rows are the N
+// dimension: 1..8 rows cost one MMA, 9..16 two), applies each group's scale
+// and bias to the fp32 group sum in registers, and the segment partials are
+// folded in k order through shared memory.
 //
 // Every wait on an mbarrier is bounded in time; on expiry the kernel records
 // it in the device status word, stops waiting and runs to completion.
@@ -43,6 +45,13 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Relaxed arrive: the caller passes a value computed from every shared-memory
+// read of the stage, so those reads have completed before the slot is released.
+__device__ __forceinline__ void mbar_arrive_after(uint64_t *bar, float dep) {
+    asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)), "f"(dep)
+                 : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_tx(uint64_t *bar, uint32_t tx) {
@@ -85,6 +94,14 @@ __device__ __forceinline__ void mbar_wait(uint64_t *bar, uint32_t parity, volati
     }
 }
 
+__device__ __forceinline__ void tma_3d(void *dst, const CUtensorMap *map, int x, int y, int z, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+            smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
@@ -111,23 +128,16 @@ __device__ __forceinline__ void named_bar_consumers() {
 // ---------------------------------------------------------- item walking --
 
 struct Item {
-    int ct, slice, k_lo, k_hi;
+    int mt, slice, k_lo, k_hi;
 };
 
 __device__ __forceinline__ Item item_of(const QmmParams &P, int it) {
     Item I;
-    I.slice = it / P.nct;
-    I.ct = it - I.slice * P.nct;
+    I.slice = it / P.nmt;
+    I.mt = it - I.slice * P.nmt;
     I.k_lo = I.slice * P.sl;
     I.k_hi = min(P.K, I.k_lo + P.sl);
     return I;
-}
-
-// Scale/bias placement of a stage: first group g0, `ng` groups, and the
-// offset of g0 inside the copied row (bulk copies start on a 16-byte boundary).
-template <int G>
-__device__ __forceinline__ int sb_offset(const QmmParams &P, int g0, int ng) {
-    return (P.bulk && ng * 2 < 16) ? (g0 & 7) : 0;
 }
 
 // -------------------------------------------------------------- producer --
@@ -135,10 +145,10 @@ __device__ __forceinline__ int sb_offset(const QmmParams &P, int g0, int ng) {
 template <int BITS, int G>
 __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint64_t *empty,
                          volatile int *abort) {
-    constexpr int SK = stage_k(BITS);
+    constexpr int SEGW = SEG * BITS / 32;     // words of one row segment
     const int lane = threadIdx.x & 31;
     const int S = P.stages;
-    const long long row_bytes = (long long)P.K * BITS / 8;
+    const long long row_words = (long long)P.K * BITS / 32;
     const int ngK = P.K / G;
     if (P.bulk && lane == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(&P.tmW) : "memory");
@@ -148,42 +158,44 @@ __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
     uint32_t it = 0;
     for (int item = blockIdx.x; item < P.n_items; item += gridDim.x) {
         const Item I = item_of(P, item);
-        const int n0 = I.ct * TN;
-        const int nrows = min(TN, P.N - n0);
-        for (int k0 = I.k_lo; k0 < I.k_hi; k0 += SK, ++it) {
-            const int k1 = min(I.k_hi, k0 + SK);
+        const int n0 = I.mt * TN;
+        for (int k0 = I.k_lo; k0 < I.k_hi; k0 += CHUNK, ++it) {
             const int slot = it % S;
             mbar_wait(&empty[slot], ((it / S) & 1u) ^ 1u, abort, P.status);
             uint8_t *st = smem + P.st_off + slot * P.stage_bytes;
-            uint8_t *sst = st + TN * P.wpitch;
+            uint8_t *sst = st + SEGS * TN * P.segpitch;
             uint8_t *bst = sst + TN * P.sbpitch;
-            const int wbytes = (k1 - k0) * BITS / 8;
-            const int g0 = k0 / G, ng = (k1 - k0) / G;
-            const int sboff = sb_offset<G>(P, g0, ng);
             if (P.bulk) {
-                // One 2D tensor copy each for codes, scales and biases; rows past N
-                // arrive zero-filled, and the full boxes count toward the bytes.
+                // Rows past N and segments past K arrive zero-filled; the full
+                // boxes count toward the transaction bytes.
                 if (lane == 0) {
                     mbar_arrive_tx(&full[slot], (uint32_t)P.stage_bytes);
-                    tma_2d(st, &P.tmW, k0 * BITS / 32, n0, &full[slot]);
-                    tma_2d(sst, &P.tmS, g0 - sboff, n0, &full[slot]);
-                    tma_2d(bst, &P.tmB, g0 - sboff, n0, &full[slot]);
+                    tma_3d(st, &P.tmW, 0, n0, k0 / SEG, &full[slot]);
+                    if (P.sb3d) {
+                        tma_3d(sst, &P.tmS, 0, k0 / CHUNK, n0, &full[slot]);
+                        tma_3d(bst, &P.tmB, 0, k0 / CHUNK, n0, &full[slot]);
+                    } else {
+                        tma_2d(sst, &P.tmS, k0 / G, n0, &full[slot]);
+                        tma_2d(bst, &P.tmB, k0 / G, n0, &full[slot]);
+                    }
                 }
             } else {
-                // Odd shapes or alignments: plain 4-byte / 2-byte copies by the warp.
-                const int wwords = wbytes / 4;
-                for (int e = lane; e < nrows * wwords; e += 32) {
-                    const int r = e / wwords, w = e - r * wwords;
-                    const uint32_t *src = reinterpret_cast<const uint32_t *>(
-                        reinterpret_cast<const uint8_t *>(P.W) + (long long)(n0 + r) * row_bytes +
-                        (long long)k0 * BITS / 8);
-                    reinterpret_cast<uint32_t *>(st + r * P.wpitch)[w] = __ldg(src + w);
+                // Odd shapes or alignments: plain copies by the warp into the same layout.
+                const int k1 = min(I.k_hi, k0 + CHUNK);
+                const int nrows = min(TN, P.N - n0);
+                const int kw = (k1 - k0) * BITS / 32;               // words of this stage per row
+                for (int e = lane; e < nrows * kw; e += 32) {
+                    const int r = e / kw, w = e - r * kw;
+                    const int seg = w / SEGW, sw = w - seg * SEGW;
+                    reinterpret_cast<uint32_t *>(st + (seg * TN + r) * P.segpitch)[sw] =
+                        __ldg(P.W + (long long)(n0 + r) * row_words + (long long)k0 * BITS / 32 + w);
                 }
+                const int ng = (k1 - k0) / G;
                 for (int e = lane; e < nrows * ng; e += 32) {
-                    const int r = e / ng, g = e - r * ng;
-                    const long long src = (long long)(n0 + r) * ngK + g0 + g;
-                    reinterpret_cast<uint16_t *>(sst + r * P.sbpitch)[g] = __ldg(P.s + src);
-                    reinterpret_cast<uint16_t *>(bst + r * P.sbpitch)[g] = __ldg(P.b + src);
+                    const int r = e / ng, gg = e - r * ng;
+                    const long long src = (long long)(n0 + r) * ngK + k0 / G + gg;
+                    reinterpret_cast<uint16_t *>(sst + r * P.sbpitch)[gg] = __ldg(P.s + src);
+                    reinterpret_cast<uint16_t *>(bst + r * P.sbpitch)[gg] = __ldg(P.b + src);
                 }
                 __threadfence_block();
                 __syncwarp();
@@ -202,19 +214,18 @@ __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
 // ------------------------------------------------------------- consumers --
 
 // Activations of one K slice, permuted into mma B-fragment order, and the
-// per-(group,row) sums of x.  Layout [k-step][R rows][4 quad lanes] of uint2
-// with R = 8*NT (rows >= `rows` are zero), so every B load of a warp is one
-// 8-byte access at a compile-time offset.  Entry (k-step, row, quad lane q)
-// holds the four x values that meet quad lane q's four codes in that step:
-// code i of an 8-code run is paired with code i+4, so a run x0..x7 feeds
-// step 2m as {(x0,x4),(x1,x5)} and step 2m+1 as {(x2,x6),(x3,x7)}.
-// sum_group(x) is the sequential fp32 sum of the group's x in k order.
-template <int G, int NT>
+// per-(group,row) sums of x.  Layout [k-step][RB rows][4 quad lanes] of uint2
+// (rows >= `rows` are zero), so every B load is one 8-byte access at a
+// compile-time offset.  Entry (k-step, row, quad lane q) holds the four x
+// values that meet quad lane q's four codes in that step: code i of an
+// 8-code run is paired with code i+4, so a run x0..x7 feeds step 2m as
+// {(x0,x4),(x1,x5)} and step 2m+1 as {(x2,x6),(x3,x7)}.  sum_group(x) is the
+// sequential fp32 sum of the group's x in k order, from 0.
+template <int G, int RB>
 __device__ void load_x_slice(const QmmParams &P, const Item &I, uint2 *Bf, float *sx, int tid) {
-    constexpr int R = 8 * NT;
     const int rows = P.rows;
     const int ngs = (I.k_hi - I.k_lo) / G;
-    for (int u = tid; u < R * ngs; u += NCW * 32) {
+    for (int u = tid; u < RB * ngs; u += NCW * 32) {
         const int r = u / ngs, gs = u - r * ngs;
         float acc = 0.f;
         const uint16_t *src = P.x + (long long)r * P.K + I.k_lo + gs * G;
@@ -224,8 +235,8 @@ __device__ void load_x_slice(const QmmParams &P, const Item &I, uint2 *Bf, float
             const int ks = gs * (G / 16) + 2 * m;
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
             if (r < rows) v = *reinterpret_cast<const uint4 *>(src + 8 * t);
-            Bf[(ks * R + r) * 4 + qq] = make_uint2(prmt(v.x, v.z, 0x5410u), prmt(v.x, v.z, 0x7632u));
-            Bf[((ks + 1) * R + r) * 4 + qq] = make_uint2(prmt(v.y, v.w, 0x5410u), prmt(v.y, v.w, 0x7632u));
+            Bf[(ks * RB + r) * 4 + qq] = make_uint2(prmt(v.x, v.z, 0x5410u), prmt(v.x, v.z, 0x7632u));
+            Bf[((ks + 1) * RB + r) * 4 + qq] = make_uint2(prmt(v.y, v.w, 0x5410u), prmt(v.y, v.w, 0x7632u));
             acc += bf16f((uint16_t)(v.x & 0xFFFF));
             acc += bf16f((uint16_t)(v.x >> 16));
             acc += bf16f((uint16_t)(v.y & 0xFFFF));
@@ -235,23 +246,25 @@ __device__ void load_x_slice(const QmmParams &P, const Item &I, uint2 *Bf, float
             acc += bf16f((uint16_t)(v.w & 0xFFFF));
             acc += bf16f((uint16_t)(v.w >> 16));
         }
-        sx[gs * R + r] = acc;
+        sx[gs * RB + r] = acc;
     }
 }
 
-// One group of this thread's two columns: T = tensor-core dot products of the
+// One group of this lane's two columns: T = tensor-core dot products of the
 // group's exact codes with x, then p = fma(s,T,p); p = fma(b,sum_group(x),p).
-// pr0/pr1[m]: run m of the thread's quarter in column rows g and g+8 (words);
-// woff: the group's word offset in the stage row; bq: this lane's B entry of
-// the group's first k-step; sxq: the group's sum_group(x) at rows 2q, 2q+1.
-template <int BITS, int G, int NT>
+// pr0/pr1[m]: run m of the lane's quarter in column rows g and g+8 (words);
+// woff: the group's word offset in the segment row; bq: this lane's B entry
+// of the group's first k-step; sxq: the group's sum_group(x) at rows 2q, 2q+1.
+template <int BITS, int G, int RB>
 __device__ __forceinline__ void group_body(const uint32_t *const (&pr0)[G / 32],
                                            const uint32_t *const (&pr1)[G / 32],
                                            const uint32_t (&sh)[G / 32], int woff, const uint2 *bq,
-                                           const uint16_t *s0, const uint16_t *s1,
+                                           bool b_lane, const uint16_t *s0, const uint16_t *s1,
                                            const uint16_t *b0, const uint16_t *b1,
-                                           const float *sxq, float (&p)[NT][4]) {
-    constexpr int RUNS = G / 32, R = 8 * NT;
+                                           const float *sxq, bool sx_lane,
+                                           float (&p)[(RB > 8 ? 2 : 1)][4]) {
+    constexpr int NT = RB > 8 ? 2 : 1;
+    constexpr int RUNS = G / 32;
     float c[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
@@ -264,14 +277,16 @@ __device__ __forceinline__ void group_body(const uint32_t *const (&pr0)[G / 32],
         for (int h = 0; h < 2; ++h)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                const uint2 bb = bq[((2 * m + h) * R + nt * 8) * 4];
+                uint2 bb = make_uint2(0u, 0u);
+                if (RB >= 8 || b_lane) bb = bq[((2 * m + h) * RB + nt * 8) * 4];
                 mma_bf16(c[nt], pa[2 * h], pb[2 * h], pa[2 * h + 1], pb[2 * h + 1], bb.x, bb.y);
             }
     }
     const float sg0 = bf16f(*s0), bg0 = bf16f(*b0), sg1 = bf16f(*s1), bg1 = bf16f(*b1);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        const float2 v = *reinterpret_cast<const float2 *>(sxq + nt * 8);
+        float2 v = make_float2(0.f, 0.f);
+        if (RB >= 8 || sx_lane) v = *reinterpret_cast<const float2 *>(sxq + nt * 8);
         p[nt][0] = fmaf(bg0, v.x, fmaf(sg0, c[nt][0], p[nt][0]));
         p[nt][1] = fmaf(bg0, v.y, fmaf(sg0, c[nt][1], p[nt][1]));
         p[nt][2] = fmaf(bg1, v.x, fmaf(sg1, c[nt][2], p[nt][2]));
@@ -280,9 +295,9 @@ __device__ __forceinline__ void group_body(const uint32_t *const (&pr0)[G / 32],
 }
 
 __device__ __forceinline__ int dst_col(const QmmParams &P, int n) {
-    for (int i = 0; i < P.nseg; ++i) {
-        const int d = n - P.seg_src[i];
-        if (d >= 0 && d < P.seg_len[i]) return P.seg_dst[i] + d;
+    for (int i = 0; i < P.ncs; ++i) {
+        const int d = n - P.cs_src[i];
+        if (d >= 0 && d < P.cs_len[i]) return P.cs_dst[i] + d;
     }
     return -1;
 }
@@ -294,22 +309,23 @@ __device__ __forceinline__ void store_y(const QmmParams &P, int r, int n, float 
     }
 }
 
-template <int BITS, int G, int NT>
+template <int BITS, int G, int RB>
 __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint64_t *empty,
                          volatile int *abort, volatile int *flag) {
-    constexpr int SK = stage_k(BITS);
-    constexpr int NG = SK / G;               // groups in a full stage
+    constexpr int NT = RB > 8 ? 2 : 1;
     constexpr int QG = G / 4;                // codes of a group per quad lane
     constexpr int RUNS = G / 32;             // 8-code runs per quad lane per group
     constexpr int STEPS = G / 16;            // mma k-steps per group
     constexpr int GW = G * BITS / 32;        // words per group of one row
-    constexpr int R = 8 * NT;
+    constexpr int NGS = SEG / G;             // groups per segment
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, q = lane & 3;
     const int S = P.stages, rows = P.rows;
     uint2 *Bf = reinterpret_cast<uint2 *>(smem + P.x_off);
     float *sx = reinterpret_cast<float *>(smem + P.sx_off);
+    float *pbuf = reinterpret_cast<float *>(smem + P.pb_off);   // [2][SEGS][TN][RB]
+    const bool b_lane = g < RB, sx_lane = 2 * q < RB;
     // This lane's runs inside any group: word offset and bit shift of run m.
     uint32_t wo[RUNS], sh[RUNS];
 #pragma unroll
@@ -318,113 +334,117 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
         wo[m] = bit >> 5;
         sh[m] = bit & 31u;
     }
-    const int row0 = warp * 16 + g;          // stage row of A row g (A row g+8 is row0+8)
+    // Fold threads: thread t < TN*RB owns output (column fc, row fr) of the item.
+    const int fc = tid / RB, fr = tid - (tid / RB) * RB;
+    const bool folder = tid < TN * RB;
     int cur_slice = -1;
     uint32_t it = 0;
     for (int item = blockIdx.x; item < P.n_items; item += gridDim.x) {
         const Item I = item_of(P, item);
         if (I.slice != cur_slice) {
             named_bar_consumers();
-            load_x_slice<G, NT>(P, I, Bf, sx, tid);
+            load_x_slice<G, RB>(P, I, Bf, sx, tid);
             named_bar_consumers();
             cur_slice = I.slice;
         }
-        const int col0 = I.ct * TN + row0;
-        float p[NT][4], yv[NT][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) p[nt][e] = yv[nt][e] = 0.f;
-
-        for (int k0 = I.k_lo; k0 < I.k_hi; k0 += SK, ++it) {
-            const int k1 = min(I.k_hi, k0 + SK);
+        const int n0 = I.mt * TN;
+        float yacc = 0.f;
+        for (int k0 = I.k_lo; k0 < I.k_hi; k0 += CHUNK, ++it) {
+            const int k1 = min(I.k_hi, k0 + CHUNK);
             const int slot = it % S;
+            const int buf = it & 1;
+            const int ks0 = k0 + warp * SEG;      // this warp's segment
+            const bool active = ks0 < k1;
             mbar_wait(&full[slot], (it / S) & 1u, abort, P.status);
-            const uint8_t *st = smem + P.st_off + slot * P.stage_bytes;
-            const uint32_t *wr0 = reinterpret_cast<const uint32_t *>(st + row0 * P.wpitch);
-            const uint32_t *wr1 = reinterpret_cast<const uint32_t *>(st + (row0 + 8) * P.wpitch);
-            const uint32_t *pr0[RUNS], *pr1[RUNS];
+            float p[NT][4];
 #pragma unroll
-            for (int m = 0; m < RUNS; ++m) {
-                pr0[m] = wr0 + wo[m];
-                pr1[m] = wr1 + wo[m];
-            }
-            const int ng = (k1 - k0) / G;
-            const int sboff = sb_offset<G>(P, k0 / G, ng);
-            const uint8_t *sbase = st + TN * P.wpitch;
-            const uint16_t *s0 = reinterpret_cast<const uint16_t *>(sbase + row0 * P.sbpitch) + sboff;
-            const uint16_t *s1 = reinterpret_cast<const uint16_t *>(sbase + (row0 + 8) * P.sbpitch) + sboff;
-            const uint16_t *b0 = reinterpret_cast<const uint16_t *>(sbase + (TN + row0) * P.sbpitch) + sboff;
-            const uint16_t *b1 = reinterpret_cast<const uint16_t *>(sbase + (TN + row0 + 8) * P.sbpitch) + sboff;
-            const int gs0 = (k0 - I.k_lo) / G;
-            const uint2 *bq = Bf + (gs0 * STEPS * R + g) * 4 + q;
-            const float *sxq = sx + gs0 * R + 2 * q;
-            if (ng == NG) {
+            for (int nt = 0; nt < NT; ++nt) p[nt][0] = p[nt][1] = p[nt][2] = p[nt][3] = 0.f;
+            if (active) {
+                const uint8_t *st = smem + P.st_off + slot * P.stage_bytes;
+                const uint8_t *blk = st + warp * TN * P.segpitch;
+                const uint32_t *wr0 = reinterpret_cast<const uint32_t *>(blk + g * P.segpitch);
+                const uint32_t *wr1 = reinterpret_cast<const uint32_t *>(blk + (g + 8) * P.segpitch);
+                const uint32_t *pr0[RUNS], *pr1[RUNS];
 #pragma unroll
-                for (int gl = 0; gl < NG; ++gl)
-                    group_body<BITS, G, NT>(pr0, pr1, sh, gl * GW, bq + gl * STEPS * R * 4, s0 + gl,
-                                            s1 + gl, b0 + gl, b1 + gl, sxq + gl * R, p);
-            } else {
+                for (int m = 0; m < RUNS; ++m) {
+                    pr0[m] = wr0 + wo[m];
+                    pr1[m] = wr1 + wo[m];
+                }
+                const uint8_t *sbase = st + SEGS * TN * P.segpitch;
+                const int gseg = (warp * SEG) / G;                      // first group of the segment in the stage
+                const uint16_t *s0 = reinterpret_cast<const uint16_t *>(sbase + g * P.sbpitch) + gseg;
+                const uint16_t *s1 = reinterpret_cast<const uint16_t *>(sbase + (g + 8) * P.sbpitch) + gseg;
+                const uint16_t *b0 = reinterpret_cast<const uint16_t *>(sbase + (TN + g) * P.sbpitch) + gseg;
+                const uint16_t *b1 = reinterpret_cast<const uint16_t *>(sbase + (TN + g + 8) * P.sbpitch) + gseg;
+                const int gs0 = (ks0 - I.k_lo) / G;                      // slice group index
+                const uint2 *bq = Bf + (gs0 * STEPS * RB + g) * 4 + q;
+                const float *sxq = sx + gs0 * RB + 2 * q;
+                const int ng = (min(k1, ks0 + SEG) - ks0) / G;
+                if (ng == NGS) {
+#pragma unroll
+                    for (int gl = 0; gl < NGS; ++gl)
+                        group_body<BITS, G, RB>(pr0, pr1, sh, gl * GW, bq + gl * STEPS * RB * 4, b_lane,
+                                                s0 + gl, s1 + gl, b0 + gl, b1 + gl, sxq + gl * RB, sx_lane, p);
+                } else {
 #pragma unroll 1
-                for (int gl = 0; gl < ng; ++gl)
-                    group_body<BITS, G, NT>(pr0, pr1, sh, gl * GW, bq + gl * STEPS * R * 4, s0 + gl,
-                                            s1 + gl, b0 + gl, b1 + gl, sxq + gl * R, p);
+                    for (int gl = 0; gl < ng; ++gl)
+                        group_body<BITS, G, RB>(pr0, pr1, sh, gl * GW, bq + gl * STEPS * RB * 4, b_lane,
+                                                s0 + gl, s1 + gl, b0 + gl, b1 + gl, sxq + gl * RB, sx_lane, p);
+                }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
-
-            if (k1 % CHUNK == 0 || k1 == P.K) {   // end of a canonical chunk
-                const int chunk = (k1 - 1) / CHUNK;
+            {   // release the slot once every shared read of it has been consumed
+                float dep = 0.f;
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    if (P.nsl == 1) {
+                for (int nt = 0; nt < NT; ++nt) dep += p[nt][0] + p[nt][1] + p[nt][2] + p[nt][3];
+                __syncwarp();
+                if (lane == 0) mbar_arrive_after(&empty[slot], dep);
+            }
+            // Segment partial -> pbuf[buf][warp][column][row].
+            float *pw = pbuf + ((buf * SEGS + warp) * TN) * RB;
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) yv[nt][e] = chunk == 0 ? p[nt][e] : yv[nt][e] + p[nt][e];
-                    } else {
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int r = nt * 8 + 2 * q + (e & 1);
-                            const int n = col0 + 8 * (e >> 1);
-                            if (r < rows && n < P.N)
-                                P.ws[((long long)chunk * rows + r) * P.N + n] = p[nt][e];
-                        }
-                    }
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) p[nt][e] = 0.f;
+                for (int e = 0; e < 4; ++e) {
+                    const int r = nt * 8 + 2 * q + (e & 1);
+                    const int c = g + 8 * (e >> 1);
+                    if (r < RB) pw[c * RB + r] = p[nt][e];
+                }
+            named_bar_consumers();
+            if (folder) {
+                // Chunk sum C = P_0 + P_1 + ... in segment order, then the chunk fold.
+                const int nseg = (k1 - k0 + SEG - 1) / SEG;
+                const float *pf = pbuf + (buf * SEGS * TN + fc) * RB + fr;
+                float C = pf[0];
+                for (int j = 1; j < nseg; ++j) C = C + pf[j * TN * RB];
+                const int chunk = k0 / CHUNK;
+                if (P.nsl == 1) {
+                    yacc = chunk == 0 ? C : yacc + C;
+                } else if (fr < rows && n0 + fc < P.N) {
+                    P.ws[((long long)chunk * rows + fr) * P.N + n0 + fc] = C;
                 }
             }
         }
 
         if (P.nsl == 1) {
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    store_y(P, nt * 8 + 2 * q + (e & 1), col0 + 8 * (e >> 1), yv[nt][e]);
+            if (folder) store_y(P, fr, n0 + fc, yacc);
         } else {
-            // Split K: the last CTA to finish a column tile folds its chunk
-            // partials in chunk order (an arrival ticket; nothing waits).
+            // Split K: the last CTA to finish an m-tile folds its chunk sums in
+            // chunk order (an arrival ticket; nothing waits).
             __threadfence();
             named_bar_consumers();
-            if (tid == 0) *flag = atomicAdd(&P.counters[I.ct], 1) == P.nsl - 1;
+            if (tid == 0) *flag = atomicAdd(&P.counters[I.mt], 1) == P.nsl - 1;
             named_bar_consumers();
             if (*flag) {
                 __threadfence();
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int r = nt * 8 + 2 * q + (e & 1);
-                        const int n = col0 + 8 * (e >> 1);
-                        if (r < rows && n < P.N) {
-                            float v = __ldcg(P.ws + (long long)r * P.N + n);
-                            for (int ch = 1; ch < P.nchunks; ++ch)
-                                v = v + __ldcg(P.ws + ((long long)ch * rows + r) * P.N + n);
-                            store_y(P, r, n, v);
-                        }
-                    }
+                if (folder && fr < rows && n0 + fc < P.N) {
+                    const long long n = n0 + fc;
+                    float v = __ldcg(P.ws + (long long)fr * P.N + n);
+                    for (int ch = 1; ch < P.nchunks; ++ch)
+                        v = v + __ldcg(P.ws + ((long long)ch * rows + fr) * P.N + n);
+                    store_y(P, fr, (int)n, v);
+                }
                 named_bar_consumers();
-                if (tid == 0) P.counters[I.ct] = 0;
+                if (tid == 0) P.counters[I.mt] = 0;
             }
         }
     }
@@ -432,7 +452,7 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
 
 // ------------------------------------------------------------------ kernel --
 
-template <int BITS, int G, int NT>
+template <int BITS, int G, int RB>
 __global__ void __launch_bounds__(NTHREADS, 2) qmm_kernel(const __grid_constant__ QmmParams P) {
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
@@ -452,15 +472,15 @@ __global__ void __launch_bounds__(NTHREADS, 2) qmm_kernel(const __grid_constant_
     if (threadIdx.x >= NCW * 32)
         producer<BITS, G>(P, smem, full, empty, abort);
     else
-        consumer<BITS, G, NT>(P, smem, full, empty, abort, flag);
+        consumer<BITS, G, RB>(P, smem, full, empty, abort, flag);
 }
 
-// Host-side launcher for one width: every group and row-tile count.
+// Host-side launcher for one width: every group and row bucket.
 template <int BITS>
-cudaError_t launch_width(int group, int nt, const QmmParams &P, int grid, int smem, cudaStream_t st) {
-#define TFQ_CASE(G_, NT_)                                                                     \
-    if (group == G_ && nt == NT_) {                                                           \
-        auto k = qmm_kernel<BITS, G_, NT_>;                                                   \
+cudaError_t launch_width(int group, int rb, const QmmParams &P, int grid, int smem, cudaStream_t st) {
+#define TFQ_CASE(G_, RB_)                                                                     \
+    if (group == G_ && rb == RB_) {                                                           \
+        auto k = qmm_kernel<BITS, G_, RB_>;                                                   \
         static unsigned attr_set = 0; /* one bit per device: smem limit raised */             \
         int dev = 0;                                                                          \
         cudaError_t e = cudaGetDevice(&dev);                                                  \
@@ -474,7 +494,9 @@ cudaError_t launch_width(int group, int nt, const QmmParams &P, int grid, int sm
         k<<<grid, NTHREADS, smem, st>>>(P);                                                   \
         return cudaGetLastError();                                                            \
     }
-    TFQ_CASE(32, 1) TFQ_CASE(32, 2) TFQ_CASE(64, 1) TFQ_CASE(64, 2) TFQ_CASE(128, 1) TFQ_CASE(128, 2)
+    TFQ_CASE(32, 2) TFQ_CASE(32, 4) TFQ_CASE(32, 8) TFQ_CASE(32, 16)
+    TFQ_CASE(64, 2) TFQ_CASE(64, 4) TFQ_CASE(64, 8) TFQ_CASE(64, 16)
+    TFQ_CASE(128, 2) TFQ_CASE(128, 4) TFQ_CASE(128, 8) TFQ_CASE(128, 16)
 #undef TFQ_CASE
     return cudaErrorInvalidValue;
 }
