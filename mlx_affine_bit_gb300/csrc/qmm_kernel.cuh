@@ -214,15 +214,14 @@ __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
 // ------------------------------------------------------------- consumers --
 
 // Activations of one K slice, permuted into mma B-fragment order, and the
-// per-(group,row) sums of x.  Layout [k-step][RB rows][4 quad lanes] of uint2
-// (rows >= `rows` are zero), so every B load is one 8-byte access at a
-// compile-time offset.  Entry (k-step, row, quad lane q) holds the four x
-// values that meet quad lane q's four codes in that step: code i of an
-// 8-code run is paired with code i+4, so a run x0..x7 feeds step 2m as
-// {(x0,x4),(x1,x5)} and step 2m+1 as {(x2,x6),(x3,x7)}.  sum_group(x) is the
-// sequential fp32 sum of the group's x in k order, from 0.
+// per-(group,row) sums of x.  Layout [run][RB rows][4 quad lanes] of uint4
+// (rows >= `rows` are zero): entry (run, row, quad lane q) holds the B
+// registers of the run's two k-steps, so one 16-byte load feeds two MMAs.
+// Code i of an 8-code run is paired with code i+4, so a run x0..x7 feeds its
+// first step as {(x0,x4),(x1,x5)} and its second as {(x2,x6),(x3,x7)}.
+// sum_group(x) is the sequential fp32 sum of the group's x in k order, from 0.
 template <int G, int RB>
-__device__ void load_x_slice(const QmmParams &P, const Item &I, uint2 *Bf, float *sx, int tid) {
+__device__ void load_x_slice(const QmmParams &P, const Item &I, uint4 *Bf, float *sx, int tid) {
     const int rows = P.rows;
     const int ngs = (I.k_hi - I.k_lo) / G;
     for (int u = tid; u < RB * ngs; u += NCW * 32) {
@@ -232,11 +231,11 @@ __device__ void load_x_slice(const QmmParams &P, const Item &I, uint2 *Bf, float
 #pragma unroll 4
         for (int t = 0; t < G / 8; ++t) {
             const int qq = (8 * t) / (G / 4), m = ((8 * t) % (G / 4)) / 8;
-            const int ks = gs * (G / 16) + 2 * m;
+            const int run = gs * (G / 32) + m;
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
             if (r < rows) v = *reinterpret_cast<const uint4 *>(src + 8 * t);
-            Bf[(ks * RB + r) * 4 + qq] = make_uint2(prmt(v.x, v.z, 0x5410u), prmt(v.x, v.z, 0x7632u));
-            Bf[((ks + 1) * RB + r) * 4 + qq] = make_uint2(prmt(v.y, v.w, 0x5410u), prmt(v.y, v.w, 0x7632u));
+            Bf[(run * RB + r) * 4 + qq] = make_uint4(prmt(v.x, v.z, 0x5410u), prmt(v.x, v.z, 0x7632u),
+                                                     prmt(v.y, v.w, 0x5410u), prmt(v.y, v.w, 0x7632u));
             acc += bf16f((uint16_t)(v.x & 0xFFFF));
             acc += bf16f((uint16_t)(v.x >> 16));
             acc += bf16f((uint16_t)(v.y & 0xFFFF));
@@ -250,17 +249,46 @@ __device__ void load_x_slice(const QmmParams &P, const Item &I, uint2 *Bf, float
     }
 }
 
+// Scales (or biases) of one segment for one row: NGS bf16 values, one vector load.
+template <int NGS>
+struct SegVals;
+template <>
+struct SegVals<8> {
+    uint4 v;
+    __device__ __forceinline__ void load(const uint16_t *p) { v = *reinterpret_cast<const uint4 *>(p); }
+    __device__ __forceinline__ float get(int i) const {
+        const uint32_t w = i < 2 ? v.x : i < 4 ? v.y : i < 6 ? v.z : v.w;
+        return __uint_as_float((i & 1) ? (w & 0xFFFF0000u) : (w << 16));
+    }
+};
+template <>
+struct SegVals<4> {
+    uint2 v;
+    __device__ __forceinline__ void load(const uint16_t *p) { v = *reinterpret_cast<const uint2 *>(p); }
+    __device__ __forceinline__ float get(int i) const {
+        const uint32_t w = i < 2 ? v.x : v.y;
+        return __uint_as_float((i & 1) ? (w & 0xFFFF0000u) : (w << 16));
+    }
+};
+template <>
+struct SegVals<2> {
+    uint32_t v;
+    __device__ __forceinline__ void load(const uint16_t *p) { v = *reinterpret_cast<const uint32_t *>(p); }
+    __device__ __forceinline__ float get(int i) const {
+        return __uint_as_float((i & 1) ? (v & 0xFFFF0000u) : (v << 16));
+    }
+};
+
 // One group of this lane's two columns: T = tensor-core dot products of the
 // group's exact codes with x, then p = fma(s,T,p); p = fma(b,sum_group(x),p).
 // pr0/pr1[m]: run m of the lane's quarter in column rows g and g+8 (words);
 // woff: the group's word offset in the segment row; bq: this lane's B entry
-// of the group's first k-step; sxq: the group's sum_group(x) at rows 2q, 2q+1.
+// of the group's first run; sxq: the group's sum_group(x) at rows 2q, 2q+1.
 template <int BITS, int G, int RB>
 __device__ __forceinline__ void group_body(const uint32_t *const (&pr0)[G / 32],
                                            const uint32_t *const (&pr1)[G / 32],
-                                           const uint32_t (&sh)[G / 32], int woff, const uint2 *bq,
-                                           bool b_lane, const uint16_t *s0, const uint16_t *s1,
-                                           const uint16_t *b0, const uint16_t *b1,
+                                           const uint32_t (&sh)[G / 32], int woff, const uint4 *bq,
+                                           bool b_lane, float sg0, float sg1, float bg0, float bg1,
                                            const float *sxq, bool sx_lane,
                                            float (&p)[(RB > 8 ? 2 : 1)][4]) {
     constexpr int NT = RB > 8 ? 2 : 1;
@@ -274,15 +302,13 @@ __device__ __forceinline__ void group_body(const uint32_t *const (&pr0)[G / 32],
         Unpack<BITS>::run(pr0[m] + woff, sh[m], pa);
         Unpack<BITS>::run(pr1[m] + woff, sh[m], pb);
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                uint2 bb = make_uint2(0u, 0u);
-                if (RB >= 8 || b_lane) bb = bq[((2 * m + h) * RB + nt * 8) * 4];
-                mma_bf16(c[nt], pa[2 * h], pb[2 * h], pa[2 * h + 1], pb[2 * h + 1], bb.x, bb.y);
-            }
+        for (int nt = 0; nt < NT; ++nt) {
+            uint4 bb = make_uint4(0u, 0u, 0u, 0u);
+            if (RB >= 8 || b_lane) bb = bq[(m * RB + nt * 8) * 4];
+            mma_bf16(c[nt], pa[0], pb[0], pa[1], pb[1], bb.x, bb.y);
+            mma_bf16(c[nt], pa[2], pb[2], pa[3], pb[3], bb.z, bb.w);
+        }
     }
-    const float sg0 = bf16f(*s0), bg0 = bf16f(*b0), sg1 = bf16f(*s1), bg1 = bf16f(*b1);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         float2 v = make_float2(0.f, 0.f);
@@ -309,20 +335,25 @@ __device__ __forceinline__ void store_y(const QmmParams &P, int r, int n, float 
     }
 }
 
+// A stage whose segment partials wait in pbuf to be folded by the fold warps.
+struct Pending {
+    int valid, buf, nseg, chunk, last, n0, it;
+};
+
 template <int BITS, int G, int RB>
 __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint64_t *empty,
-                         volatile int *abort, volatile int *flag) {
+                         uint64_t *ffull, uint64_t *fempty, volatile int *abort, volatile int *flag) {
     constexpr int NT = RB > 8 ? 2 : 1;
     constexpr int QG = G / 4;                // codes of a group per quad lane
     constexpr int RUNS = G / 32;             // 8-code runs per quad lane per group
-    constexpr int STEPS = G / 16;            // mma k-steps per group
     constexpr int GW = G * BITS / 32;        // words per group of one row
     constexpr int NGS = SEG / G;             // groups per segment
+    constexpr int NFW = RB / 2;              // fold warps: TN*RB outputs, one per thread
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, q = lane & 3;
     const int S = P.stages, rows = P.rows;
-    uint2 *Bf = reinterpret_cast<uint2 *>(smem + P.x_off);
+    uint4 *Bf = reinterpret_cast<uint4 *>(smem + P.x_off);
     float *sx = reinterpret_cast<float *>(smem + P.sx_off);
     float *pbuf = reinterpret_cast<float *>(smem + P.pb_off);   // [2][SEGS][TN][RB]
     const bool b_lane = g < RB, sx_lane = 2 * q < RB;
@@ -334,9 +365,28 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
         wo[m] = bit >> 5;
         sh[m] = bit & 31u;
     }
-    // Fold threads: thread t < TN*RB owns output (column fc, row fr) of the item.
+    // Fold threads: thread t < TN*RB (warps < NFW) owns output (column fc, row fr).
+    const bool fold_warp = warp < NFW;
     const int fc = tid / RB, fr = tid - (tid / RB) * RB;
-    const bool folder = tid < TN * RB;
+    float yacc = 0.f;
+    Pending pend{0, 0, 0, 0, 0, 0, 0};
+
+    // Fold a pending stage: C = P_0 + P_1 + ... (segment order), then the chunk fold.
+    auto fold = [&](const Pending &f) {
+        mbar_wait(&ffull[f.buf], (uint32_t)(f.it >> 1) & 1u, abort, P.status);
+        const float *pf = pbuf + (f.buf * SEGS * TN + fc) * RB + fr;
+        float C = pf[0];
+        for (int j = 1; j < f.nseg; ++j) C = C + pf[j * TN * RB];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&fempty[f.buf]);
+        if (P.nsl == 1) {
+            yacc = f.chunk == 0 ? C : yacc + C;
+            if (f.last) store_y(P, fr, f.n0 + fc, yacc);
+        } else if (fr < rows && f.n0 + fc < P.N) {
+            P.ws[((long long)f.chunk * rows + fr) * P.N + f.n0 + fc] = C;
+        }
+    };
+
     int cur_slice = -1;
     uint32_t it = 0;
     for (int item = blockIdx.x; item < P.n_items; item += gridDim.x) {
@@ -348,7 +398,6 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
             cur_slice = I.slice;
         }
         const int n0 = I.mt * TN;
-        float yacc = 0.f;
         for (int k0 = I.k_lo; k0 < I.k_hi; k0 += CHUNK, ++it) {
             const int k1 = min(I.k_hi, k0 + CHUNK);
             const int slot = it % S;
@@ -371,25 +420,32 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                     pr1[m] = wr1 + wo[m];
                 }
                 const uint8_t *sbase = st + SEGS * TN * P.segpitch;
-                const int gseg = (warp * SEG) / G;                      // first group of the segment in the stage
-                const uint16_t *s0 = reinterpret_cast<const uint16_t *>(sbase + g * P.sbpitch) + gseg;
-                const uint16_t *s1 = reinterpret_cast<const uint16_t *>(sbase + (g + 8) * P.sbpitch) + gseg;
-                const uint16_t *b0 = reinterpret_cast<const uint16_t *>(sbase + (TN + g) * P.sbpitch) + gseg;
-                const uint16_t *b1 = reinterpret_cast<const uint16_t *>(sbase + (TN + g + 8) * P.sbpitch) + gseg;
+                const int gseg = warp * NGS;                             // segment's first group in the stage
                 const int gs0 = (ks0 - I.k_lo) / G;                      // slice group index
-                const uint2 *bq = Bf + (gs0 * STEPS * RB + g) * 4 + q;
+                const uint4 *bq = Bf + (gs0 * RUNS * RB + g) * 4 + q;
                 const float *sxq = sx + gs0 * RB + 2 * q;
                 const int ng = (min(k1, ks0 + SEG) - ks0) / G;
+                const uint16_t *s0p = reinterpret_cast<const uint16_t *>(sbase + g * P.sbpitch) + gseg;
+                const uint16_t *s1p = reinterpret_cast<const uint16_t *>(sbase + (g + 8) * P.sbpitch) + gseg;
+                const uint16_t *b0p = reinterpret_cast<const uint16_t *>(sbase + (TN + g) * P.sbpitch) + gseg;
+                const uint16_t *b1p = reinterpret_cast<const uint16_t *>(sbase + (TN + g + 8) * P.sbpitch) + gseg;
                 if (ng == NGS) {
+                    SegVals<NGS> S0, S1, B0, B1;
+                    S0.load(s0p);
+                    S1.load(s1p);
+                    B0.load(b0p);
+                    B1.load(b1p);
 #pragma unroll
                     for (int gl = 0; gl < NGS; ++gl)
-                        group_body<BITS, G, RB>(pr0, pr1, sh, gl * GW, bq + gl * STEPS * RB * 4, b_lane,
-                                                s0 + gl, s1 + gl, b0 + gl, b1 + gl, sxq + gl * RB, sx_lane, p);
+                        group_body<BITS, G, RB>(pr0, pr1, sh, gl * GW, bq + gl * RUNS * RB * 4, b_lane,
+                                                S0.get(gl), S1.get(gl), B0.get(gl), B1.get(gl),
+                                                sxq + gl * RB, sx_lane, p);
                 } else {
 #pragma unroll 1
                     for (int gl = 0; gl < ng; ++gl)
-                        group_body<BITS, G, RB>(pr0, pr1, sh, gl * GW, bq + gl * STEPS * RB * 4, b_lane,
-                                                s0 + gl, s1 + gl, b0 + gl, b1 + gl, sxq + gl * RB, sx_lane, p);
+                        group_body<BITS, G, RB>(pr0, pr1, sh, gl * GW, bq + gl * RUNS * RB * 4, b_lane,
+                                                bf16f(s0p[gl]), bf16f(s1p[gl]), bf16f(b0p[gl]),
+                                                bf16f(b1p[gl]), sxq + gl * RB, sx_lane, p);
                 }
             }
             {   // release the slot once every shared read of it has been consumed
@@ -399,7 +455,9 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                 __syncwarp();
                 if (lane == 0) mbar_arrive_after(&empty[slot], dep);
             }
-            // Segment partial -> pbuf[buf][warp][column][row].
+            // Segment partial -> pbuf[buf][warp][column][row], once the fold of
+            // this buffer's previous use is done.
+            if (it >= 2) mbar_wait(&fempty[buf], ((it >> 1) - 1) & 1u, abort, P.status);
             float *pw = pbuf + ((buf * SEGS + warp) * TN) * RB;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
@@ -409,45 +467,41 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                     const int c = g + 8 * (e >> 1);
                     if (r < RB) pw[c * RB + r] = p[nt][e];
                 }
-            named_bar_consumers();
-            if (folder) {
-                // Chunk sum C = P_0 + P_1 + ... in segment order, then the chunk fold.
-                const int nseg = (k1 - k0 + SEG - 1) / SEG;
-                const float *pf = pbuf + (buf * SEGS * TN + fc) * RB + fr;
-                float C = pf[0];
-                for (int j = 1; j < nseg; ++j) C = C + pf[j * TN * RB];
-                const int chunk = k0 / CHUNK;
-                if (P.nsl == 1) {
-                    yacc = chunk == 0 ? C : yacc + C;
-                } else if (fr < rows && n0 + fc < P.N) {
-                    P.ws[((long long)chunk * rows + fr) * P.N + n0 + fc] = C;
-                }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ffull[buf]);
+            // Fold warps fold the previous stage (one stage behind, so nobody waits).
+            const Pending cur{1, buf, (k1 - k0 + SEG - 1) / SEG, k0 / CHUNK, k0 + CHUNK >= I.k_hi, n0, (int)it};
+            if (fold_warp) {
+                if (pend.valid) fold(pend);
+                pend = cur;
             }
         }
-
-        if (P.nsl == 1) {
-            if (folder) store_y(P, fr, n0 + fc, yacc);
-        } else {
-            // Split K: the last CTA to finish an m-tile folds its chunk sums in
-            // chunk order (an arrival ticket; nothing waits).
-            __threadfence();
-            named_bar_consumers();
-            if (tid == 0) *flag = atomicAdd(&P.counters[I.mt], 1) == P.nsl - 1;
-            named_bar_consumers();
-            if (*flag) {
+        if (P.nsl > 1) {
+            // Split K: fold this item's last chunk now, then the last CTA to finish
+            // the m-tile folds the chunk sums in chunk order (an arrival ticket).
+            if (fold_warp) {
+                if (pend.valid) fold(pend);
+                pend.valid = 0;
                 __threadfence();
-                if (folder && fr < rows && n0 + fc < P.N) {
-                    const long long n = n0 + fc;
-                    float v = __ldcg(P.ws + (long long)fr * P.N + n);
-                    for (int ch = 1; ch < P.nchunks; ++ch)
-                        v = v + __ldcg(P.ws + ((long long)ch * rows + fr) * P.N + n);
-                    store_y(P, fr, (int)n, v);
+                asm volatile("bar.sync 2, %0;" ::"r"(NFW * 32) : "memory");
+                if (tid == 0) *flag = atomicAdd(&P.counters[I.mt], 1) == P.nsl - 1;
+                asm volatile("bar.sync 2, %0;" ::"r"(NFW * 32) : "memory");
+                if (*flag) {
+                    __threadfence();
+                    if (fr < rows && n0 + fc < P.N) {
+                        const long long n = n0 + fc;
+                        float v = __ldcg(P.ws + (long long)fr * P.N + n);
+                        for (int ch = 1; ch < P.nchunks; ++ch)
+                            v = v + __ldcg(P.ws + ((long long)ch * rows + fr) * P.N + n);
+                        store_y(P, fr, (int)n, v);
+                    }
+                    asm volatile("bar.sync 2, %0;" ::"r"(NFW * 32) : "memory");
+                    if (tid == 0) P.counters[I.mt] = 0;
                 }
-                named_bar_consumers();
-                if (tid == 0) P.counters[I.mt] = 0;
             }
         }
     }
+    if (fold_warp && pend.valid) fold(pend);
 }
 
 // ------------------------------------------------------------------ kernel --
@@ -457,12 +511,18 @@ __global__ void __launch_bounds__(NTHREADS, 2) qmm_kernel(const __grid_constant_
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + MAX_STAGES;
-    volatile int *abort = reinterpret_cast<volatile int *>(smem + 16 * MAX_STAGES);
+    uint64_t *ffull = empty + MAX_STAGES;   // [2] segment partials written (8 warps)
+    uint64_t *fempty = ffull + 2;           // [2] segment partials folded (fold warps)
+    volatile int *abort = reinterpret_cast<volatile int *>(fempty + 2);
     volatile int *flag = abort + 1;
     if (threadIdx.x == 0) {
         for (int i = 0; i < P.stages; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], NCW);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ffull[i], NCW);
+            mbar_init(&fempty[i], RB / 2);
         }
         *abort = 0;
         *flag = 0;
@@ -472,7 +532,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) qmm_kernel(const __grid_constant_
     if (threadIdx.x >= NCW * 32)
         producer<BITS, G>(P, smem, full, empty, abort);
     else
-        consumer<BITS, G, RB>(P, smem, full, empty, abort, flag);
+        consumer<BITS, G, RB>(P, smem, full, empty, ffull, fempty, abort, flag);
 }
 
 // Host-side launcher for one width: every group and row bucket.
