@@ -287,9 +287,10 @@ struct SegVals<2> {
 template <int BITS, int G, int RB>
 __device__ __forceinline__ void group_body(const uint32_t *const (&pr0)[G / 32],
                                            const uint32_t *const (&pr1)[G / 32],
-                                           const uint32_t (&sh)[G / 32], int woff, const uint4 *bq,
+                                           const uint32_t (&ua)[G / 32], const uint32_t (&ub)[G / 32],
+                                           int woff, const uint4 *bq,
                                            bool b_lane, float sg0, float sg1, float bg0, float bg1,
-                                           const float *sxq, bool sx_lane,
+                                           const float *sxq, bool sx_lane, bool one_row,
                                            float (&p)[(RB > 8 ? 2 : 1)][4]) {
     constexpr int NT = RB > 8 ? 2 : 1;
     constexpr int RUNS = G / 32;
@@ -299,8 +300,8 @@ __device__ __forceinline__ void group_body(const uint32_t *const (&pr0)[G / 32],
 #pragma unroll
     for (int m = 0; m < RUNS; ++m) {
         uint32_t pa[4], pb[4];
-        Unpack<BITS>::run(pr0[m] + woff, sh[m], pa);
-        Unpack<BITS>::run(pr1[m] + woff, sh[m], pb);
+        Unpack<BITS>::run(pr0[m] + woff, ua[m], ub[m], pa);
+        Unpack<BITS>::run(pr1[m] + woff, ua[m], ub[m], pb);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             uint4 bb = make_uint4(0u, 0u, 0u, 0u);
@@ -308,6 +309,12 @@ __device__ __forceinline__ void group_body(const uint32_t *const (&pr0)[G / 32],
             mma_bf16(c[nt], pa[0], pb[0], pa[1], pb[1], bb.x, bb.y);
             mma_bf16(c[nt], pa[2], pb[2], pa[3], pb[3], bb.z, bb.w);
         }
+    }
+    if (RB == 2 && one_row) {   // a single activation row: only row 0 of the tile is live
+        const float x0 = sx_lane ? *sxq : 0.f;
+        p[0][0] = fmaf(bg0, x0, fmaf(sg0, c[0][0], p[0][0]));
+        p[0][2] = fmaf(bg1, x0, fmaf(sg1, c[0][2], p[0][2]));
+        return;
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -335,14 +342,9 @@ __device__ __forceinline__ void store_y(const QmmParams &P, int r, int n, float 
     }
 }
 
-// A stage whose segment partials wait in pbuf to be folded by the fold warps.
-struct Pending {
-    int valid, buf, nseg, chunk, last, n0, it;
-};
-
 template <int BITS, int G, int RB>
 __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint64_t *empty,
-                         uint64_t *ffull, uint64_t *fempty, volatile int *abort, volatile int *flag) {
+                           volatile int *abort, volatile int *flag) {
     constexpr int NT = RB > 8 ? 2 : 1;
     constexpr int QG = G / 4;                // codes of a group per quad lane
     constexpr int RUNS = G / 32;             // 8-code runs per quad lane per group
@@ -356,36 +358,19 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
     uint4 *Bf = reinterpret_cast<uint4 *>(smem + P.x_off);
     float *sx = reinterpret_cast<float *>(smem + P.sx_off);
     float *pbuf = reinterpret_cast<float *>(smem + P.pb_off);   // [2][SEGS][TN][RB]
-    const bool b_lane = g < RB, sx_lane = 2 * q < RB;
+    const bool b_lane = g < RB, sx_lane = 2 * q < RB, one_row = rows == 1;
     // This lane's runs inside any group: word offset and bit shift of run m.
-    uint32_t wo[RUNS], sh[RUNS];
+    uint32_t wo[RUNS], ua[RUNS], ub[RUNS];
 #pragma unroll
     for (int m = 0; m < RUNS; ++m) {
         const uint32_t bit = (uint32_t)(q * QG + 8 * m) * BITS;
         wo[m] = bit >> 5;
-        sh[m] = bit & 31u;
+        lane_args<BITS>(bit & 31u, ua[m], ub[m]);
     }
     // Fold threads: thread t < TN*RB (warps < NFW) owns output (column fc, row fr).
     const bool fold_warp = warp < NFW;
     const int fc = tid / RB, fr = tid - (tid / RB) * RB;
     float yacc = 0.f;
-    Pending pend{0, 0, 0, 0, 0, 0, 0};
-
-    // Fold a pending stage: C = P_0 + P_1 + ... (segment order), then the chunk fold.
-    auto fold = [&](const Pending &f) {
-        mbar_wait(&ffull[f.buf], (uint32_t)(f.it >> 1) & 1u, abort, P.status);
-        const float *pf = pbuf + (f.buf * SEGS * TN + fc) * RB + fr;
-        float C = pf[0];
-        for (int j = 1; j < f.nseg; ++j) C = C + pf[j * TN * RB];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&fempty[f.buf]);
-        if (P.nsl == 1) {
-            yacc = f.chunk == 0 ? C : yacc + C;
-            if (f.last) store_y(P, fr, f.n0 + fc, yacc);
-        } else if (fr < rows && f.n0 + fc < P.N) {
-            P.ws[((long long)f.chunk * rows + fr) * P.N + f.n0 + fc] = C;
-        }
-    };
 
     int cur_slice = -1;
     uint32_t it = 0;
@@ -437,15 +422,15 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                     B1.load(b1p);
 #pragma unroll
                     for (int gl = 0; gl < NGS; ++gl)
-                        group_body<BITS, G, RB>(pr0, pr1, sh, gl * GW, bq + gl * RUNS * RB * 4, b_lane,
+                        group_body<BITS, G, RB>(pr0, pr1, ua, ub, gl * GW, bq + gl * RUNS * RB * 4, b_lane,
                                                 S0.get(gl), S1.get(gl), B0.get(gl), B1.get(gl),
-                                                sxq + gl * RB, sx_lane, p);
+                                                sxq + gl * RB, sx_lane, one_row, p);
                 } else {
 #pragma unroll 1
                     for (int gl = 0; gl < ng; ++gl)
-                        group_body<BITS, G, RB>(pr0, pr1, sh, gl * GW, bq + gl * RUNS * RB * 4, b_lane,
+                        group_body<BITS, G, RB>(pr0, pr1, ua, ub, gl * GW, bq + gl * RUNS * RB * 4, b_lane,
                                                 bf16f(s0p[gl]), bf16f(s1p[gl]), bf16f(b0p[gl]),
-                                                bf16f(b1p[gl]), sxq + gl * RB, sx_lane, p);
+                                                bf16f(b1p[gl]), sxq + gl * RB, sx_lane, one_row, p);
                 }
             }
             {   // release the slot once every shared read of it has been consumed
@@ -455,9 +440,6 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                 __syncwarp();
                 if (lane == 0) mbar_arrive_after(&empty[slot], dep);
             }
-            // Segment partial -> pbuf[buf][warp][column][row], once the fold of
-            // this buffer's previous use is done.
-            if (it >= 2) mbar_wait(&fempty[buf], ((it >> 1) - 1) & 1u, abort, P.status);
             float *pw = pbuf + ((buf * SEGS + warp) * TN) * RB;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
@@ -467,21 +449,25 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                     const int c = g + 8 * (e >> 1);
                     if (r < RB) pw[c * RB + r] = p[nt][e];
                 }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ffull[buf]);
-            // Fold warps fold the previous stage (one stage behind, so nobody waits).
-            const Pending cur{1, buf, (k1 - k0 + SEG - 1) / SEG, k0 / CHUNK, k0 + CHUNK >= I.k_hi, n0, (int)it};
+            named_bar_consumers();
             if (fold_warp) {
-                if (pend.valid) fold(pend);
-                pend = cur;
+                const float *pf = pbuf + (buf * SEGS * TN + fc) * RB + fr;
+                const int nseg = (k1 - k0 + SEG - 1) / SEG;
+                float C = pf[0];
+                for (int j = 1; j < nseg; ++j) C = C + pf[j * TN * RB];
+                const int chunk = k0 / CHUNK;
+                if (P.nsl == 1) {
+                    yacc = chunk == 0 ? C : yacc + C;
+                    if (k0 + CHUNK >= I.k_hi) store_y(P, fr, n0 + fc, yacc);
+                } else if (fr < rows && n0 + fc < P.N) {
+                    P.ws[((long long)chunk * rows + fr) * P.N + n0 + fc] = C;
+                }
             }
         }
         if (P.nsl > 1) {
             // Split K: fold this item's last chunk now, then the last CTA to finish
             // the m-tile folds the chunk sums in chunk order (an arrival ticket).
             if (fold_warp) {
-                if (pend.valid) fold(pend);
-                pend.valid = 0;
                 __threadfence();
                 asm volatile("bar.sync 2, %0;" ::"r"(NFW * 32) : "memory");
                 if (tid == 0) *flag = atomicAdd(&P.counters[I.mt], 1) == P.nsl - 1;
@@ -501,7 +487,6 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
             }
         }
     }
-    if (fold_warp && pend.valid) fold(pend);
 }
 
 // ------------------------------------------------------------------ kernel --
@@ -511,18 +496,12 @@ __global__ void __launch_bounds__(NTHREADS, 2) qmm_kernel(const __grid_constant_
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + MAX_STAGES;
-    uint64_t *ffull = empty + MAX_STAGES;   // [2] segment partials written (8 warps)
-    uint64_t *fempty = ffull + 2;           // [2] segment partials folded (fold warps)
-    volatile int *abort = reinterpret_cast<volatile int *>(fempty + 2);
+    volatile int *abort = reinterpret_cast<volatile int *>(empty + MAX_STAGES);
     volatile int *flag = abort + 1;
     if (threadIdx.x == 0) {
         for (int i = 0; i < P.stages; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], NCW);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&ffull[i], NCW);
-            mbar_init(&fempty[i], RB / 2);
         }
         *abort = 0;
         *flag = 0;
@@ -532,7 +511,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) qmm_kernel(const __grid_constant_
     if (threadIdx.x >= NCW * 32)
         producer<BITS, G>(P, smem, full, empty, abort);
     else
-        consumer<BITS, G, RB>(P, smem, full, empty, ffull, fempty, abort, flag);
+        consumer<BITS, G, RB>(P, smem, full, empty, abort, flag);
 }
 
 // Host-side launcher for one width: every group and row bucket.

@@ -104,14 +104,15 @@ constexpr uint32_t Q3 = 0x3E003E00u, NEG16 = 0xC180C180u;   // p=3: 1/8, -16
 constexpr uint32_t Q4 = 0x3D803D80u, NEG8 = 0xC100C100u;    // p=4: 1/16, -8
 
 // Run of 8 codes -> pairs p[i] = (c_i | c_{i+4} << 16) as exact bf16 values.
-// `w` points at the 32-bit word holding the run's first bit; `sh` is that
-// bit's position in the word.  Reads at most w[0], w[1].
+// `w` points at the 32-bit word holding the run's first bit; `ua`/`ub` come
+// from lane_args<BITS>(sh) with `sh` that bit's position in the word (they are
+// per-lane constants, computed once).  Reads at most w[0], w[1].
 template <int BITS>
 struct Unpack;
 
 template <>
 struct Unpack<2> {  // 16 bits; sh in {0, 16}
-    static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t p[4]) {
+    static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t, uint32_t p[4]) {
         uint32_t v = w[0] >> sh;
         uint32_t u = halves(v, v << 8);              // c0..c3 @0,2,4,6 | c4..c7 @16,18,20,22
         p[0] = hfma2(mask_or(u, 0x00030003u, MAGIC), ONE2, NEG128);
@@ -123,7 +124,7 @@ struct Unpack<2> {  // 16 bits; sh in {0, 16}
 
 template <>
 struct Unpack<4> {  // 32 bits; sh == 0
-    static TF_HD void run(const uint32_t *w, uint32_t, uint32_t p[4]) {
+    static TF_HD void run(const uint32_t *w, uint32_t, uint32_t, uint32_t p[4]) {
         uint32_t v = w[0];
         p[0] = hfma2(mask_or(v, 0x000F000Fu, MAGIC), ONE2, NEG128);
         p[1] = hfma2(mask_or(v >> 4, 0x000F000Fu, MAGIC), ONE2, NEG128);
@@ -141,7 +142,7 @@ struct Unpack<8> {  // 64 bits; sh == 0
         uint32_t add = ~sgn & NEG128;                       // -128 if c < 128, else 0
         return hfma2(mant, ONE2, add);
     }
-    static TF_HD void run(const uint32_t *w, uint32_t, uint32_t p[4]) {
+    static TF_HD void run(const uint32_t *w, uint32_t, uint32_t, uint32_t p[4]) {
         uint32_t lo = w[0], hi = w[1];
         p[0] = one(prmt(lo, hi, 0x0400u));   // byte i of lo -> 0, byte i of hi -> 2
         p[1] = one(prmt(lo, hi, 0x0501u));
@@ -152,7 +153,7 @@ struct Unpack<8> {  // 64 bits; sh == 0
 
 template <>
 struct Unpack<3> {  // 24 bits; sh in {0, 8, 16, 24}
-    static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t p[4]) {
+    static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t, uint32_t p[4]) {
         uint32_t v = funnel(w[0], w[1], sh);
         uint32_t u = halves(v, v << 4);   // c0..c3 @0,3,6,9 | c4..c7 @16,19,22,25
         p[0] = hfma2(mask_or(u, 0x00070007u, MAGIC), ONE2, NEG128);
@@ -165,7 +166,7 @@ struct Unpack<3> {  // 24 bits; sh in {0, 8, 16, 24}
 
 template <>
 struct Unpack<5> {  // 40 bits; sh in {0, 8, 16, 24}
-    static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t p[4]) {
+    static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t, uint32_t p[4]) {
         uint32_t lo = funnel(w[0], w[1], sh);               // run bits 0..31
         uint32_t hi = w[1] >> sh;                           // run bits 32..39 at 0..7
         uint32_t u = halves(lo, funnel(lo, hi, 4));         // c0,c1,c2 @0,5,10 | c4,c5,c6 @16,21,26
@@ -179,10 +180,8 @@ struct Unpack<5> {  // 40 bits; sh in {0, 8, 16, 24}
 
 template <>
 struct Unpack<6> {  // 48 bits; sh in {0, 16}
-    static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t p[4]) {
-        // Run bytes {0,1,3,4} and {1,2,4,5}; raw byte = run byte + sh/8.
-        uint32_t s0 = sh ? 0x6532u : 0x4310u;
-        uint32_t s2 = sh ? 0x7643u : 0x5421u;
+    // Run bytes {0,1,3,4} and {1,2,4,5}; raw byte = run byte + sh/8 (sh = 0 or 16).
+    static TF_HD void run(const uint32_t *w, uint32_t s0, uint32_t s2, uint32_t p[4]) {
         uint32_t P0 = prmt(w[0], w[1], s0);   // c0 @0, c1 @6 | c4 @16, c5 @22
         uint32_t P2 = prmt(w[0], w[1], s2);   // c2 @4, c3 @10 | c6 @20, c7 @26
         p[0] = hfma2(mask_or(P0, 0x003F003Fu, MAGIC), ONE2, NEG128);
@@ -191,6 +190,18 @@ struct Unpack<6> {  // 48 bits; sh in {0, 16}
         p[3] = hfma2(mask_or(P2 >> 10, 0x003F003Fu, MAGIC), ONE2, NEG128);
     }
 };
+
+// Per-lane arguments of Unpack<BITS>::run for a run starting at bit `sh` of a word.
+template <int BITS>
+TF_HD void lane_args(uint32_t sh, uint32_t &ua, uint32_t &ub) {
+    if (BITS == 6) {
+        ua = sh ? 0x6532u : 0x4310u;
+        ub = sh ? 0x7643u : 0x5421u;
+    } else {
+        ua = sh;
+        ub = 0u;
+    }
+}
 
 // Position of code (step j, slot e) inside a thread's quarter of a group:
 // step j takes pairs 2*(j%2) and 2*(j%2)+1 of run j/2; slot e = 0,1 are the

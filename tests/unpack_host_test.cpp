@@ -29,7 +29,9 @@ static int check(std::mt19937 &rng, int sh) {
         for (auto &x : w) x = rng();
         if (t < 4) for (auto &x : w) x = (t & 1) ? 0xFFFFFFFFu : 0u;
         uint32_t p[4];
-        tfq::Unpack<BITS>::run(w, (uint32_t)sh, p);
+        uint32_t ua, ub;
+        tfq::lane_args<BITS>((uint32_t)sh, ua, ub);
+        tfq::Unpack<BITS>::run(w, ua, ub, p);
         for (int i = 0; i < 4; ++i) {
             int lo = bf16_int((uint16_t)(p[i] & 0xFFFF)), hi = bf16_int((uint16_t)(p[i] >> 16));
             int want_lo = (int)bit_code(w, BITS, sh, i), want_hi = (int)bit_code(w, BITS, sh, i + 4);
