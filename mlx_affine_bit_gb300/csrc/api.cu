@@ -59,7 +59,7 @@ int check_io(const uint16_t *x, int rows, const float *y) {
 
 struct Plan {
     int nmt, nsl, sl, nchunks, stages, smem, grid, segpitch, sbpitch, stage_bytes, x_off, sx_off,
-        pb_off, st_off, rb, ctas;
+        pb_off, z_off, st_off, rb, ctas;
     bool sb3d;
 };
 
@@ -74,7 +74,8 @@ Plan layout(int N, int K, int bits, int group, int rows, int nsm, int ctas, bool
     const int budget = ctas == 2 ? SMEM_PER_SM / 2 - 1024 : SMEM_MAX;
     p.nmt = ceil_div(N, TN);
     p.nchunks = ceil_div(K, CHUNK);
-    const int max_cps = std::max(1, xs_max / (p.rb * 2 * CHUNK));   // chunks of x a CTA holds
+    const int lr = layout_rows(p.rb);
+    const int max_cps = std::max(1, xs_max / (lr * 2 * CHUNK));   // chunks of x a CTA holds
     const long long slots = (long long)ctas * nsm;
     double best = 1e30;
     int best_cps = p.nchunks;
@@ -95,13 +96,14 @@ Plan layout(int N, int K, int bits, int group, int rows, int nsm, int ctas, bool
     p.segpitch = SEG * bits / 8 + 16;
     p.sbpitch = sb3d ? (sbg + 8) * 2 : sbg * 2;
     p.stage_bytes = SEGS * TN * p.segpitch + 2 * TN * p.sbpitch;
-    const int x_bytes = (p.rb * len * 2 + 127) & ~127;
-    const int sx_bytes = ((len / group) * p.rb * 4 + 127) & ~127;
-    const int pb_bytes = 2 * SEGS * TN * p.rb * 4;
+    const int x_bytes = (lr * len * 2 + 127) & ~127;
+    const int sx_bytes = ((len / group) * lr * 4 + 127) & ~127;
+    const int pb_bytes = 2 * SEGS * TN * lr * 4;
     p.x_off = HDR_BYTES;
     p.sx_off = p.x_off + x_bytes;
     p.pb_off = p.sx_off + sx_bytes;
-    p.st_off = (p.pb_off + pb_bytes + 127) & ~127;
+    p.z_off = (p.pb_off + pb_bytes + 127) & ~127;
+    p.st_off = p.z_off + (lr < 8 ? ZERO_BYTES : 0);
     p.stages = std::min(MAX_STAGES, (budget - p.st_off) / p.stage_bytes);
     p.smem = p.st_off + p.stages * p.stage_bytes;
     p.grid = (int)std::min<long long>((long long)p.nmt * p.nsl, slots);
@@ -336,6 +338,7 @@ int run_product(const uint16_t *x, int rows, int K, const uint32_t *W, const uin
     P.x_off = pl.x_off;
     P.sx_off = pl.sx_off;
     P.pb_off = pl.pb_off;
+    P.z_off = pl.z_off;
     P.st_off = pl.st_off;
     P.ncs = nseg;
     for (int i = 0; i < nseg; ++i) {

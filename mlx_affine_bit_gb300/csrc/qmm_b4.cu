@@ -1,4 +1,4 @@
-// qmm_b4.cu -- kernel instantiations for 4-bit codes (groups 32/64/128, row buckets 2/4/8/16).
+// qmm_b4.cu -- kernel instantiations for 4-bit codes (groups 32/64/128, row buckets 1/2/4/8/16).
 #include "internal.h"
 #include "qmm_kernel.cuh"
 

@@ -29,8 +29,13 @@ constexpr int SMEM_MAX = 227 * 1024;       // dynamic shared memory per CTA on s
 constexpr int SMEM_PER_SM = 228 * 1024;    // shared memory per SM (each CTA reserves 1 KB)
 constexpr int HDR_BYTES = 256;             // mbarriers + flags at the start of smem
 
-// Padded activation rows of the B-fragment layout for `rows` activation rows.
-TFQ_HD constexpr int row_bucket(int rows) { return rows <= 2 ? 2 : rows <= 4 ? 4 : rows <= 8 ? 8 : 16; }
+// Row bucket of a launch (a kernel template parameter): 1 (a single row),
+// 2, 4, 8 or 16; the B-fragment layout holds layout_rows(bucket) rows.
+TFQ_HD constexpr int row_bucket(int rows) {
+    return rows == 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : rows <= 8 ? 8 : 16;
+}
+TFQ_HD constexpr int layout_rows(int rb) { return rb < 2 ? 2 : rb; }
+constexpr int ZERO_BYTES = 2048;           // zero block that idle lanes of small buckets read
 
 struct QmmParams {
     // TMA descriptors (bulk mode).  W: [K/SEG segments][N rows][SEG*bits/32
@@ -57,7 +62,7 @@ struct QmmParams {
     int segpitch;       // bytes per W row inside a segment block (SEG*bits/8 + 16)
     int sbpitch;        // bytes per scale (or bias) row in a stage
     int stage_bytes;    // W blocks + scales + biases
-    int x_off, sx_off, pb_off, st_off;   // smem offsets
+    int x_off, sx_off, pb_off, z_off, st_off;   // smem offsets
     int ncs;            // column-map segments
     int cs_src[MAXCOLSEG], cs_len[MAXCOLSEG], cs_dst[MAXCOLSEG];
 };

@@ -222,6 +222,7 @@ __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
 // sum_group(x) is the sequential fp32 sum of the group's x in k order, from 0.
 template <int G, int RB>
 __device__ void load_x_slice(const QmmParams &P, const Item &I, uint4 *Bf, float *sx, int tid) {
+    static_assert(RB >= 2, "layout rows");
     const int rows = P.rows;
     const int ngs = (I.k_hi - I.k_lo) / G;
     for (int u = tid; u < RB * ngs; u += NCW * 32) {
@@ -288,11 +289,11 @@ template <int BITS, int G, int RB>
 __device__ __forceinline__ void group_body(const uint32_t *const (&pr0)[G / 32],
                                            const uint32_t *const (&pr1)[G / 32],
                                            const uint32_t (&ua)[G / 32], const uint32_t (&ub)[G / 32],
-                                           int woff, const uint4 *bq,
-                                           bool b_lane, float sg0, float sg1, float bg0, float bg1,
-                                           const float *sxq, bool sx_lane, bool one_row,
+                                           int woff, const uint4 *bq, float sg0, float sg1, float bg0,
+                                           float bg1, const float *sxq,
                                            float (&p)[(RB > 8 ? 2 : 1)][4]) {
     constexpr int NT = RB > 8 ? 2 : 1;
+    constexpr int LR = layout_rows(RB);
     constexpr int RUNS = G / 32;
     float c[NT][4];
 #pragma unroll
@@ -304,26 +305,24 @@ __device__ __forceinline__ void group_body(const uint32_t *const (&pr0)[G / 32],
         Unpack<BITS>::run(pr1[m] + woff, ua[m], ub[m], pb);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            uint4 bb = make_uint4(0u, 0u, 0u, 0u);
-            if (RB >= 8 || b_lane) bb = bq[(m * RB + nt * 8) * 4];
+            const uint4 bb = bq[(m * LR + nt * 8) * 4];
             mma_bf16(c[nt], pa[0], pb[0], pa[1], pb[1], bb.x, bb.y);
             mma_bf16(c[nt], pa[2], pb[2], pa[3], pb[3], bb.z, bb.w);
         }
     }
-    if (RB == 2 && one_row) {   // a single activation row: only row 0 of the tile is live
-        const float x0 = sx_lane ? *sxq : 0.f;
+    if (RB == 1) {   // a single activation row: only row 0 of the tile is live
+        const float x0 = *sxq;
         p[0][0] = fmaf(bg0, x0, fmaf(sg0, c[0][0], p[0][0]));
         p[0][2] = fmaf(bg1, x0, fmaf(sg1, c[0][2], p[0][2]));
-        return;
-    }
+    } else {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        float2 v = make_float2(0.f, 0.f);
-        if (RB >= 8 || sx_lane) v = *reinterpret_cast<const float2 *>(sxq + nt * 8);
-        p[nt][0] = fmaf(bg0, v.x, fmaf(sg0, c[nt][0], p[nt][0]));
-        p[nt][1] = fmaf(bg0, v.y, fmaf(sg0, c[nt][1], p[nt][1]));
-        p[nt][2] = fmaf(bg1, v.x, fmaf(sg1, c[nt][2], p[nt][2]));
-        p[nt][3] = fmaf(bg1, v.y, fmaf(sg1, c[nt][3], p[nt][3]));
+        for (int nt = 0; nt < NT; ++nt) {
+            const float2 v = *reinterpret_cast<const float2 *>(sxq + nt * 8);
+            p[nt][0] = fmaf(bg0, v.x, fmaf(sg0, c[nt][0], p[nt][0]));
+            p[nt][1] = fmaf(bg0, v.y, fmaf(sg0, c[nt][1], p[nt][1]));
+            p[nt][2] = fmaf(bg1, v.x, fmaf(sg1, c[nt][2], p[nt][2]));
+            p[nt][3] = fmaf(bg1, v.y, fmaf(sg1, c[nt][3], p[nt][3]));
+        }
     }
 }
 
@@ -350,15 +349,21 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
     constexpr int RUNS = G / 32;             // 8-code runs per quad lane per group
     constexpr int GW = G * BITS / 32;        // words per group of one row
     constexpr int NGS = SEG / G;             // groups per segment
-    constexpr int NFW = RB / 2;              // fold warps: TN*RB outputs, one per thread
+    constexpr int LR = layout_rows(RB);      // rows of the B / sum_group(x) layouts
+    constexpr int NFW = LR / 2;              // fold warps: TN*LR outputs, one per thread
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, q = lane & 3;
     const int S = P.stages, rows = P.rows;
     uint4 *Bf = reinterpret_cast<uint4 *>(smem + P.x_off);
     float *sx = reinterpret_cast<float *>(smem + P.sx_off);
-    float *pbuf = reinterpret_cast<float *>(smem + P.pb_off);   // [2][SEGS][TN][RB]
-    const bool b_lane = g < RB, sx_lane = 2 * q < RB, one_row = rows == 1;
+    float *pbuf = reinterpret_cast<float *>(smem + P.pb_off);   // [2][SEGS][TN][LR]
+    const uint8_t *zero = smem + P.z_off;
+    // Lanes past the bucket's rows read a zero block instead of B / sum_group(x).
+    const bool b_lane = g < LR, sx_lane = 2 * q < LR;
+    if (LR < 8) {
+        for (int i = tid; i < ZERO_BYTES / 4; i += NCW * 32) reinterpret_cast<uint32_t *>(smem + P.z_off)[i] = 0u;
+    }
     // This lane's runs inside any group: word offset and bit shift of run m.
     uint32_t wo[RUNS], ua[RUNS], ub[RUNS];
 #pragma unroll
@@ -369,7 +374,7 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
     }
     // Fold threads: thread t < TN*RB (warps < NFW) owns output (column fc, row fr).
     const bool fold_warp = warp < NFW;
-    const int fc = tid / RB, fr = tid - (tid / RB) * RB;
+    const int fc = tid / LR, fr = tid - (tid / LR) * LR;
     float yacc = 0.f;
 
     int cur_slice = -1;
@@ -378,7 +383,7 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
         const Item I = item_of(P, item);
         if (I.slice != cur_slice) {
             named_bar_consumers();
-            load_x_slice<G, RB>(P, I, Bf, sx, tid);
+            load_x_slice<G, LR>(P, I, Bf, sx, tid);
             named_bar_consumers();
             cur_slice = I.slice;
         }
@@ -407,8 +412,10 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                 const uint8_t *sbase = st + SEGS * TN * P.segpitch;
                 const int gseg = warp * NGS;                             // segment's first group in the stage
                 const int gs0 = (ks0 - I.k_lo) / G;                      // slice group index
-                const uint4 *bq = Bf + (gs0 * RUNS * RB + g) * 4 + q;
-                const float *sxq = sx + gs0 * RB + 2 * q;
+                const uint4 *bq = (LR >= 8 || b_lane) ? Bf + (gs0 * RUNS * LR + g) * 4 + q
+                                                      : reinterpret_cast<const uint4 *>(zero) + q;
+                const float *sxq = (LR >= 8 || sx_lane) ? sx + gs0 * LR + 2 * q
+                                                        : reinterpret_cast<const float *>(zero);
                 const int ng = (min(k1, ks0 + SEG) - ks0) / G;
                 const uint16_t *s0p = reinterpret_cast<const uint16_t *>(sbase + g * P.sbpitch) + gseg;
                 const uint16_t *s1p = reinterpret_cast<const uint16_t *>(sbase + (g + 8) * P.sbpitch) + gseg;
@@ -422,15 +429,15 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                     B1.load(b1p);
 #pragma unroll
                     for (int gl = 0; gl < NGS; ++gl)
-                        group_body<BITS, G, RB>(pr0, pr1, ua, ub, gl * GW, bq + gl * RUNS * RB * 4, b_lane,
+                        group_body<BITS, G, RB>(pr0, pr1, ua, ub, gl * GW, bq + gl * RUNS * LR * 4,
                                                 S0.get(gl), S1.get(gl), B0.get(gl), B1.get(gl),
-                                                sxq + gl * RB, sx_lane, one_row, p);
+                                                sxq + gl * LR, p);
                 } else {
 #pragma unroll 1
                     for (int gl = 0; gl < ng; ++gl)
-                        group_body<BITS, G, RB>(pr0, pr1, ua, ub, gl * GW, bq + gl * RUNS * RB * 4, b_lane,
+                        group_body<BITS, G, RB>(pr0, pr1, ua, ub, gl * GW, bq + gl * RUNS * LR * 4,
                                                 bf16f(s0p[gl]), bf16f(s1p[gl]), bf16f(b0p[gl]),
-                                                bf16f(b1p[gl]), sxq + gl * RB, sx_lane, one_row, p);
+                                                bf16f(b1p[gl]), sxq + gl * LR, p);
                 }
             }
             {   // release the slot once every shared read of it has been consumed
@@ -440,21 +447,21 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                 __syncwarp();
                 if (lane == 0) mbar_arrive_after(&empty[slot], dep);
             }
-            float *pw = pbuf + ((buf * SEGS + warp) * TN) * RB;
+            float *pw = pbuf + ((buf * SEGS + warp) * TN) * LR;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int r = nt * 8 + 2 * q + (e & 1);
                     const int c = g + 8 * (e >> 1);
-                    if (r < RB) pw[c * RB + r] = p[nt][e];
+                    if (r < LR) pw[c * LR + r] = p[nt][e];
                 }
             named_bar_consumers();
             if (fold_warp) {
-                const float *pf = pbuf + (buf * SEGS * TN + fc) * RB + fr;
+                const float *pf = pbuf + (buf * SEGS * TN + fc) * LR + fr;
                 const int nseg = (k1 - k0 + SEG - 1) / SEG;
                 float C = pf[0];
-                for (int j = 1; j < nseg; ++j) C = C + pf[j * TN * RB];
+                for (int j = 1; j < nseg; ++j) C = C + pf[j * TN * LR];
                 const int chunk = k0 / CHUNK;
                 if (P.nsl == 1) {
                     yacc = chunk == 0 ? C : yacc + C;
@@ -533,9 +540,9 @@ cudaError_t launch_width(int group, int rb, const QmmParams &P, int grid, int sm
         k<<<grid, NTHREADS, smem, st>>>(P);                                                   \
         return cudaGetLastError();                                                            \
     }
-    TFQ_CASE(32, 2) TFQ_CASE(32, 4) TFQ_CASE(32, 8) TFQ_CASE(32, 16)
-    TFQ_CASE(64, 2) TFQ_CASE(64, 4) TFQ_CASE(64, 8) TFQ_CASE(64, 16)
-    TFQ_CASE(128, 2) TFQ_CASE(128, 4) TFQ_CASE(128, 8) TFQ_CASE(128, 16)
+    TFQ_CASE(32, 1) TFQ_CASE(32, 2) TFQ_CASE(32, 4) TFQ_CASE(32, 8) TFQ_CASE(32, 16)
+    TFQ_CASE(64, 1) TFQ_CASE(64, 2) TFQ_CASE(64, 4) TFQ_CASE(64, 8) TFQ_CASE(64, 16)
+    TFQ_CASE(128, 1) TFQ_CASE(128, 2) TFQ_CASE(128, 4) TFQ_CASE(128, 8) TFQ_CASE(128, 16)
 #undef TFQ_CASE
     return cudaErrorInvalidValue;
 }
