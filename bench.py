@@ -177,6 +177,8 @@ def run_gpu(args, cases):
     if world > 1:
         dist.barrier()
     tf.lib()
+    tf.tf_set_launch_mode({"plain": 0, "pdl": tf.TF_LAUNCH_PDL,
+                           "early": tf.TF_LAUNCH_EARLY_WEIGHTS}[args.launch])
     stream = torch.cuda.current_stream()
 
     # Device-resident inputs; enough weight copies that a buffer is reused only
@@ -327,6 +329,9 @@ def run_gpu(args, cases):
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOAD_TEXT[args.workload], "parallelism": "replicas" if world > 1 else "1 GPU",
+                       "launch": {"plain": "plain launches", "pdl": "programmatic dependent launch",
+                                  "early": "programmatic dependent launch; weights streamed before the "
+                                           "dependency wait (weights are never written in the step)"}[args.launch],
                        "l2": "weights rotate over %d copies (%.0f MB a step, >= 4x L2 between reuses)"
                              % (copies, per_step / 1e6)},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -354,6 +359,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="sweep", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--launch", default="early", choices=["plain", "pdl", "early"])
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     cases = workload_cases(args.workload)

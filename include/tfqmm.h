@@ -18,13 +18,15 @@
  * window of 1..16 rows), and a strided or stacked output equals the contiguous
  * one bit for bit (the canonical order below fixes the arithmetic).
  *
- * Canonical order of one output y[r][n]: K is cut into chunks of 512 k (the
- * last may be shorter).  Inside a chunk, group by group in k order,
+ * Canonical order of one output y[r][n]: K is cut into segments of 256 k and
+ * chunks of 2048 k (the last of each may be shorter).  Inside a segment, group
+ * by group in k order,
  *     T = sum over the group of x*q     (tensor-core dot products, exact codes)
  *     p = fma(scale, T, p); p = fma(bias, sum_group(x), p)     (p starts at 0)
- * where sum_group(x) is the sequential fp32 sum of the group's x.  Then
- * y = p_0, y = y + p_1, ... in chunk order.  Row count, N, output stride,
- * split-K and stack membership never enter this order.
+ * where sum_group(x) is the sequential fp32 sum of the group's x.  A chunk's
+ * sum is C = p_0 + p_1 + ... over its segments in order, and y = C_0 + C_1 +
+ * ... over the chunks in order.  Row count, N, output stride, split-K, launch
+ * mode and stack membership never enter this order.
  *
  * Memory: every pointer of tf_qmm / tf_qmm_stack / tf_widen is DEVICE memory
  * owned by the caller; the library never frees or retains it.  Calls are
@@ -130,6 +132,22 @@ int tf_qmm_bytes(int N, int K, int bits, int group, int64_t *w_bytes, int64_t *s
  * the device).  TF_OK, or TF_EDEVICE if a kernel gave up a bounded wait.
  */
 int tf_device_status(void);
+
+/*
+ * Launch mode of later tf_qmm / tf_qmm_stack calls (process wide); returns the
+ * previous mode.  Not on the pages: a GB300 launch option.
+ *   TF_LAUNCH_PDL: programmatic dependent launch -- a product may start its
+ *     prologue while the previous kernel of the stream finishes; it waits for
+ *     that kernel before reading x or writing y (always safe).
+ *   TF_LAUNCH_EARLY_WEIGHTS: as TF_LAUNCH_PDL, and the product also streams its
+ *     weights, scales and biases before that wait.  Only valid when the kernel
+ *     just before it in the stream does not write them (e.g. a decode step whose
+ *     weights are fixed).
+ * 0 (the default) launches plainly.  Negative status for unknown bits.
+ */
+#define TF_LAUNCH_PDL 1
+#define TF_LAUNCH_EARLY_WEIGHTS 2
+int tf_set_launch_mode(int mode);
 
 /* Message for the last failing call on this host thread ("" if none). */
 const char *tf_last_error_string(void);

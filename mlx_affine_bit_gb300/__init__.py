@@ -24,7 +24,8 @@ STATUS = {
     -9: "TF_ESTACK", -10: "TF_ECUDA", -11: "TF_EDEVICE",
 }
 SYMBOLS = ("tf_qmm", "tf_qmm_stack", "tf_widen", "tf_common_width", "tf_qmm_bytes",
-           "tf_device_status", "tf_last_error_string", "tf_version")
+           "tf_device_status", "tf_set_launch_mode", "tf_last_error_string", "tf_version")
+TF_LAUNCH_PDL, TF_LAUNCH_EARLY_WEIGHTS = 1, 2
 
 
 class TfError(RuntimeError):
@@ -61,10 +62,11 @@ def lib():
         L.tf_common_width.argtypes = [P, P, i32, P, P]
         L.tf_qmm_bytes.argtypes = [i32, i32, i32, i32, P, P]
         L.tf_device_status.argtypes = []
+        L.tf_set_launch_mode.argtypes = [i32]
         L.tf_last_error_string.restype = ctypes.c_char_p
         L.tf_version.restype = ctypes.c_char_p
         for name in ("tf_qmm", "tf_qmm_stack", "tf_widen", "tf_common_width", "tf_qmm_bytes",
-                     "tf_device_status"):
+                     "tf_device_status", "tf_set_launch_mode"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -129,6 +131,14 @@ def tf_qmm_bytes(N, K, bits, group) -> tuple[int, int]:
 
 def tf_device_status() -> None:
     _check(lib().tf_device_status())
+
+
+def tf_set_launch_mode(mode: int) -> int:
+    """Set the launch mode (TF_LAUNCH_* bits) of later calls; returns the previous mode."""
+    rc = lib().tf_set_launch_mode(mode)
+    if rc < 0:
+        _check(rc)
+    return rc
 
 
 def tf_version() -> str:

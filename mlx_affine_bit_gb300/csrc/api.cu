@@ -7,6 +7,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <string>
@@ -237,6 +238,7 @@ struct DevState {
 };
 
 std::mutex g_mu;
+std::atomic<int> g_launch_mode{0};
 std::map<int, DevState> g_dev;
 std::map<std::pair<int, cudaStream_t>, StreamWs> g_ws;
 
@@ -285,14 +287,14 @@ int stream_ws(cudaStream_t st, size_t floats, size_t counters, StreamWs **out) {
 }
 
 cudaError_t launch(int bits, int group, int rb, const QmmParams &P, int grid, int smem,
-                   cudaStream_t st) {
+                   cudaStream_t st, bool pdl) {
     switch (bits) {
-        case 2: return launch_b2(group, rb, P, grid, smem, st);
-        case 3: return launch_b3(group, rb, P, grid, smem, st);
-        case 4: return launch_b4(group, rb, P, grid, smem, st);
-        case 5: return launch_b5(group, rb, P, grid, smem, st);
-        case 6: return launch_b6(group, rb, P, grid, smem, st);
-        case 8: return launch_b8(group, rb, P, grid, smem, st);
+        case 2: return launch_b2(group, rb, P, grid, smem, st, pdl);
+        case 3: return launch_b3(group, rb, P, grid, smem, st, pdl);
+        case 4: return launch_b4(group, rb, P, grid, smem, st, pdl);
+        case 5: return launch_b5(group, rb, P, grid, smem, st, pdl);
+        case 6: return launch_b6(group, rb, P, grid, smem, st, pdl);
+        case 8: return launch_b8(group, rb, P, grid, smem, st, pdl);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -353,7 +355,10 @@ int run_product(const uint16_t *x, int rows, int K, const uint32_t *W, const uin
         P.ws = w->ws;
         P.counters = w->cnt;
     }
-    const cudaError_t e = launch(bits, group, pl.rb, P, pl.grid, pl.smem, st);
+    const int mode = g_launch_mode.load(std::memory_order_relaxed);
+    P.early_w = (mode & TF_LAUNCH_EARLY_WEIGHTS) != 0;
+    const cudaError_t e = launch(bits, group, pl.rb, P, pl.grid, pl.smem, st,
+                                 (mode & (TF_LAUNCH_PDL | TF_LAUNCH_EARLY_WEIGHTS)) != 0);
     if (e != cudaSuccess) return cuda_fail(e, "qmm kernel launch");
     return TF_OK;
 }
@@ -526,6 +531,12 @@ int tf_device_status(void) {
         return fail(TF_EDEVICE, "a kernel gave up a bounded wait");
     }
     return TF_OK;
+}
+
+int tf_set_launch_mode(int mode) {
+    g_err.clear();
+    if (mode & ~(TF_LAUNCH_PDL | TF_LAUNCH_EARLY_WEIGHTS)) return fail(TF_EINVAL_SIZE, "unknown launch mode bits");
+    return g_launch_mode.exchange(mode);
 }
 
 const char *tf_last_error_string(void) { return g_err.c_str(); }

@@ -3,7 +3,8 @@
 #include "qmm_kernel.cuh"
 
 namespace tfq {
-cudaError_t launch_b6(int group, int rb, const QmmParams &P, int grid, int smem, cudaStream_t st) {
-    return launch_width<6>(group, rb, P, grid, smem, st);
+cudaError_t launch_b6(int group, int rb, const QmmParams &P, int grid, int smem, cudaStream_t st,
+                      bool pdl) {
+    return launch_width<6>(group, rb, P, grid, smem, st, pdl);
 }
 }  // namespace tfq

@@ -119,6 +119,10 @@ __device__ __forceinline__ void mma_bf16(float c[4], uint32_t a0, uint32_t a1, u
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Wait until the grids this one depends on (programmatic dependent launch) have
+// completed and their memory is visible; returns at once otherwise.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ float bf16f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
 
 __device__ __forceinline__ void named_bar_consumers() {
@@ -131,14 +135,43 @@ struct Item {
     int mt, slice, k_lo, k_hi;
 };
 
-__device__ __forceinline__ Item item_of(const QmmParams &P, int it) {
-    Item I;
-    I.slice = it / P.nmt;
-    I.mt = it - I.slice * P.nmt;
-    I.k_lo = I.slice * P.sl;
-    I.k_hi = min(P.K, I.k_lo + P.sl);
-    return I;
-}
+// This CTA's work items blockIdx.x, blockIdx.x + gridDim.x, ... (slice-major),
+// walked without divisions.
+struct ItemWalk {
+    int item, mt, slice;
+    __device__ __forceinline__ explicit ItemWalk(const QmmParams &P) : item(blockIdx.x) {
+        slice = blockIdx.x / P.nmt;
+        mt = blockIdx.x - slice * P.nmt;
+    }
+    __device__ __forceinline__ bool more(const QmmParams &P) const { return item < P.n_items; }
+    __device__ __forceinline__ Item get(const QmmParams &P) const {
+        Item I;
+        I.mt = mt;
+        I.slice = slice;
+        I.k_lo = slice * P.sl;
+        I.k_hi = min(P.K, I.k_lo + P.sl);
+        return I;
+    }
+    __device__ __forceinline__ void next(const QmmParams &P) {
+        item += gridDim.x;
+        mt += gridDim.x;
+        while (mt >= P.nmt) {
+            mt -= P.nmt;
+            ++slice;
+        }
+    }
+};
+
+// Ring position of the stage sequence: slot and mbarrier phase, no divisions.
+struct Ring {
+    uint32_t slot = 0, phase = 0;
+    __device__ __forceinline__ void next(int S) {
+        if (++slot == (uint32_t)S) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+};
 
 // -------------------------------------------------------------- producer --
 
@@ -155,13 +188,17 @@ __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
         asm volatile("prefetch.tensormap [%0];" ::"l"(&P.tmS) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(&P.tmB) : "memory");
     }
+    // Under programmatic dependent launch the previous kernel of the stream may
+    // still run: wait for it unless the caller declared the weights unwritten by it.
+    if (!P.early_w) grid_dependency_wait();
     uint32_t it = 0;
-    for (int item = blockIdx.x; item < P.n_items; item += gridDim.x) {
-        const Item I = item_of(P, item);
+    Ring ring;
+    for (ItemWalk w(P); w.more(P); w.next(P)) {
+        const Item I = w.get(P);
         const int n0 = I.mt * TN;
-        for (int k0 = I.k_lo; k0 < I.k_hi; k0 += CHUNK, ++it) {
-            const int slot = it % S;
-            mbar_wait(&empty[slot], ((it / S) & 1u) ^ 1u, abort, P.status);
+        for (int k0 = I.k_lo; k0 < I.k_hi; k0 += CHUNK, ++it, ring.next(S)) {
+            const int slot = (int)ring.slot;
+            mbar_wait(&empty[slot], ring.phase ^ 1u, abort, P.status);
             uint8_t *st = smem + P.st_off + slot * P.stage_bytes;
             uint8_t *sst = st + SEGS * TN * P.segpitch;
             uint8_t *bst = sst + TN * P.sbpitch;
@@ -203,11 +240,19 @@ __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
             }
         }
     }
-    // Drain: the last stages' copies must land before the CTA may exit.
+    // Drain: the last stages' copies must land before the CTA may exit
+    // (walk the ring back over the last min(it, S) stages).
     if (P.bulk && lane == 0) {
-        const uint32_t first = it > (uint32_t)S ? it - (uint32_t)S : 0u;
-        for (uint32_t j = first; j < it; ++j)
-            mbar_wait(&full[j % S], (j / S) & 1u, abort, P.status, false);
+        const uint32_t n = it < (uint32_t)S ? it : (uint32_t)S;
+        uint32_t slot = ring.slot, phase = ring.phase;
+        for (uint32_t j = 0; j < n; ++j) {
+            if (slot == 0) {
+                slot = (uint32_t)S;
+                phase ^= 1u;
+            }
+            --slot;
+            mbar_wait(&full[slot], phase, abort, P.status, false);
+        }
     }
 }
 
@@ -377,10 +422,14 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
     const int fc = tid / LR, fr = tid - (tid / LR) * LR;
     float yacc = 0.f;
 
+    // x, y and the split-K workspace may be touched by the previous kernel of
+    // the stream (programmatic dependent launch): wait for it first.
+    grid_dependency_wait();
     int cur_slice = -1;
     uint32_t it = 0;
-    for (int item = blockIdx.x; item < P.n_items; item += gridDim.x) {
-        const Item I = item_of(P, item);
+    Ring ring;
+    for (ItemWalk iw(P); iw.more(P); iw.next(P)) {
+        const Item I = iw.get(P);
         if (I.slice != cur_slice) {
             named_bar_consumers();
             load_x_slice<G, LR>(P, I, Bf, sx, tid);
@@ -388,13 +437,13 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
             cur_slice = I.slice;
         }
         const int n0 = I.mt * TN;
-        for (int k0 = I.k_lo; k0 < I.k_hi; k0 += CHUNK, ++it) {
+        for (int k0 = I.k_lo; k0 < I.k_hi; k0 += CHUNK, ++it, ring.next(S)) {
             const int k1 = min(I.k_hi, k0 + CHUNK);
-            const int slot = it % S;
+            const int slot = (int)ring.slot;
             const int buf = it & 1;
             const int ks0 = k0 + warp * SEG;      // this warp's segment
             const bool active = ks0 < k1;
-            mbar_wait(&full[slot], (it / S) & 1u, abort, P.status);
+            mbar_wait(&full[slot], ring.phase, abort, P.status);
             float p[NT][4];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) p[nt][0] = p[nt][1] = p[nt][2] = p[nt][3] = 0.f;
@@ -515,6 +564,9 @@ __global__ void __launch_bounds__(NTHREADS, 2) qmm_kernel(const __grid_constant_
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    // The next kernel of the stream may start its prologue once every CTA of
+    // this grid is resident (no effect without programmatic dependent launch).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x >= NCW * 32)
         producer<BITS, G>(P, smem, full, empty, abort);
     else
@@ -523,7 +575,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) qmm_kernel(const __grid_constant_
 
 // Host-side launcher for one width: every group and row bucket.
 template <int BITS>
-cudaError_t launch_width(int group, int rb, const QmmParams &P, int grid, int smem, cudaStream_t st) {
+cudaError_t launch_width(int group, int rb, const QmmParams &P, int grid, int smem, cudaStream_t st,
+                         bool pdl) {
 #define TFQ_CASE(G_, RB_)                                                                     \
     if (group == G_ && rb == RB_) {                                                           \
         auto k = qmm_kernel<BITS, G_, RB_>;                                                   \
@@ -537,8 +590,17 @@ cudaError_t launch_width(int group, int rb, const QmmParams &P, int grid, int sm
             if (e != cudaSuccess) return e;                                                   \
             __atomic_fetch_or(&attr_set, bit, __ATOMIC_RELEASE);                              \
         }                                                                                     \
-        k<<<grid, NTHREADS, smem, st>>>(P);                                                   \
-        return cudaGetLastError();                                                            \
+        cudaLaunchConfig_t cfg = {};                                                          \
+        cfg.gridDim = dim3(grid);                                                             \
+        cfg.blockDim = dim3(NTHREADS);                                                        \
+        cfg.dynamicSmemBytes = smem;                                                          \
+        cfg.stream = st;                                                                      \
+        cudaLaunchAttribute attr[1];                                                          \
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;                      \
+        attr[0].val.programmaticStreamSerializationAllowed = 1;                               \
+        cfg.attrs = attr;                                                                     \
+        cfg.numAttrs = pdl ? 1 : 0;                                                           \
+        return cudaLaunchKernelEx(&cfg, k, P);                                                \
     }
     TFQ_CASE(32, 1) TFQ_CASE(32, 2) TFQ_CASE(32, 4) TFQ_CASE(32, 8) TFQ_CASE(32, 16)
     TFQ_CASE(64, 1) TFQ_CASE(64, 2) TFQ_CASE(64, 4) TFQ_CASE(64, 8) TFQ_CASE(64, 16)

@@ -246,3 +246,23 @@ def test_lmhead_sampled(bits, group, seed):
     cols = sample_cols(m.N, 64, seed)
     oracle_check(m, x[0:1], y1.cpu().numpy(), cols)
     oracle_check(m, x, y16.cpu().numpy(), cols)
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_launch_modes_bit_identical(mode):
+    # A back-to-back sequence of products (including a split-K shape) gives the
+    # same bits with programmatic dependent launch as with plain launches.
+    mats = [synth.make_matrix(N, K, b, g, 70 + i, 0.001, 0.03)
+            for i, (N, K, b, g) in enumerate([(4096, 4096, 4, 64), (2048, 12288, 6, 32),
+                                              (300, 2048, 3, 128), (4096, 4096, 8, 32)])]
+    dms = [DevMatrix(m) for m in mats]
+    xs = [dev(synth.make_x(3, m.K, 80 + i)) for i, m in enumerate(mats)]
+    ref = [run_qmm(dm, x) for dm, x in zip(dms, xs)]
+    old = tf.tf_set_launch_mode(mode)
+    try:
+        for _ in range(3):
+            got = [run_qmm(dm, x) for dm, x in zip(dms, xs)]
+            for a, b in zip(ref, got):
+                assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    finally:
+        tf.tf_set_launch_mode(old)
