@@ -74,6 +74,31 @@ int tf_qmm(const uint16_t *x, int rows, int K,
            float *y, int64_t y_stride, void *stream);
 
 /*
+ * tf_qmm_noalloc -- tf_qmm for callers that cannot let a library allocate
+ * device memory: code running while a stream is captured into a CUDA graph,
+ * engines that give all device memory to their own pool at start-up, and
+ * processes that must not grow their footprint later.  The paper has no
+ * counterpart; it is a deployment variant of tf_qmm.
+ *
+ * Same arguments, layouts and results as tf_qmm (plain launches, whatever the
+ * launch mode).  Its split-K scratch and status word come from one fixed
+ * 4 MiB device array built into the library instead of a cudaMalloc: every
+ * GPU that loads the library holds that array until exit, and the call
+ * allocates nothing.  A product whose split-K partials need more than the
+ * array holds (rows * N * ceil(K/2048) * 4 bytes, about 4 MiB, when the
+ * planner splits K) is refused with TF_EINVAL_SIZE before any launch.
+ * The first call on a device looks up the array's device address (set-up);
+ * make that first call before any stream capture.  All calls share the
+ * array: each clears what it needs at zero on its own stream, and calls that
+ * overlap on the GPU race.  A bounded wait that runs out is recorded in the
+ * array, not in the word tf_device_status reads.
+ */
+int tf_qmm_noalloc(const uint16_t *x, int rows, int K,
+                   const uint32_t *W, const uint16_t *scales, const uint16_t *biases,
+                   int N, int bits, int group,
+                   float *y, int64_t y_stride, void *stream);
+
+/*
  * Fused stack of members written through one strided output (PR #788, "a
  * fused stack of 48-column members at mixed widths written through the
  * stride"; PR #774, runs and members of the _stacked split rule and the

@@ -23,7 +23,7 @@ STATUS = {
     -5: "TF_EINVAL_PTR", -6: "TF_EINVAL_SIZE", -7: "TF_ENARROW", -8: "TF_EGROUP",
     -9: "TF_ESTACK", -10: "TF_ECUDA", -11: "TF_EDEVICE",
 }
-SYMBOLS = ("tf_qmm", "tf_qmm_stack", "tf_widen", "tf_common_width", "tf_qmm_bytes",
+SYMBOLS = ("tf_qmm", "tf_qmm_noalloc", "tf_qmm_stack", "tf_widen", "tf_common_width", "tf_qmm_bytes",
            "tf_device_status", "tf_set_launch_mode", "tf_last_error_string", "tf_version")
 TF_LAUNCH_PDL, TF_LAUNCH_EARLY_WEIGHTS = 1, 2
 
@@ -56,6 +56,7 @@ def lib():
         L = ctypes.CDLL(SO)
         P, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
         L.tf_qmm.argtypes = [P, i32, i32, P, P, P, i32, i32, i32, P, i64, P]
+        L.tf_qmm_noalloc.argtypes = [P, i32, i32, P, P, P, i32, i32, i32, P, i64, P]
         L.tf_qmm_stack.argtypes = [P, i32, i32, ctypes.POINTER(TfRun), i32,
                                    ctypes.POINTER(TfMember), i32, P, i64, P]
         L.tf_widen.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, i32, i32, P]
@@ -65,7 +66,7 @@ def lib():
         L.tf_set_launch_mode.argtypes = [i32]
         L.tf_last_error_string.restype = ctypes.c_char_p
         L.tf_version.restype = ctypes.c_char_p
-        for name in ("tf_qmm", "tf_qmm_stack", "tf_widen", "tf_common_width", "tf_qmm_bytes",
+        for name in ("tf_qmm", "tf_qmm_noalloc", "tf_qmm_stack", "tf_widen", "tf_common_width", "tf_qmm_bytes",
                      "tf_device_status", "tf_set_launch_mode"):
             getattr(L, name).restype = i32
         _lib = L
@@ -97,6 +98,12 @@ def _check(rc: int) -> None:
 def tf_qmm(x, rows, K, W, scales, biases, N, bits, group, y, y_stride, stream=None) -> None:
     _check(lib().tf_qmm(_ptr(x), rows, K, _ptr(W), _ptr(scales), _ptr(biases), N, bits, group,
                         _ptr(y), y_stride, _stream(stream)))
+
+
+def tf_qmm_noalloc(x, rows, K, W, scales, biases, N, bits, group, y, y_stride, stream=None) -> None:
+    """tf_qmm with no device allocation (fixed built-in scratch; see include/tfqmm.h)."""
+    _check(lib().tf_qmm_noalloc(_ptr(x), rows, K, _ptr(W), _ptr(scales), _ptr(biases), N, bits,
+                                group, _ptr(y), y_stride, _stream(stream)))
 
 
 def tf_qmm_stack(x, rows, K, runs, members, y, y_stride, stream=None) -> None:

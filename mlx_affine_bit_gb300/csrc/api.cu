@@ -399,6 +399,90 @@ __global__ void widen_groups(const uint16_t *s, const uint16_t *b, uint16_t *so,
 
 }  // namespace
 
+// Product with caller-provided scratch: the split-K partials, arrival counters
+// and status word live in memory the caller owns (used by tf_qmm_noalloc).
+// Allocates nothing: tensor maps are encoded into locals, no cache is grown.
+int tfq::product_with_scratch(const uint16_t *x, int rows, int K, const uint32_t *W,
+                              const uint16_t *s, const uint16_t *b, int N, int bits, int group,
+                              float *y, int64_t y_stride, cudaStream_t st, int nsm, float *ws,
+                              size_t ws_floats, int *counters, size_t n_counters, int *status) {
+    g_err.clear();
+    int rc = check_matrix(K, W, s, b, N, bits, group);
+    if (rc) return rc;
+    rc = check_io(x, rows, y);
+    if (rc) return rc;
+    if (y_stride < N) return fail(TF_EINVAL_STRIDE, "y_stride below N is refused");
+    const bool bulk = aligned(s, 16) && aligned(b, 16) && K % SEG == 0 && K % (8 * group) == 0;
+    const bool sb3d = bulk && K % CHUNK == 0;
+    const Plan pl = make_plan(N, K, bits, group, rows, nsm, sb3d);
+    if (pl.nsl > 1 && ((size_t)pl.nchunks * rows * N > ws_floats || (size_t)pl.nmt > n_counters))
+        return fail(TF_EINVAL_SIZE, "split-K partials (" + std::to_string((size_t)pl.nchunks * rows * N * 4) +
+                                        " bytes) exceed the fixed scratch of the no-allocation entry point");
+    QmmParams P{};
+    P.x = x;
+    P.W = W;
+    P.s = s;
+    P.b = b;
+    P.y = y;
+    P.status = status;
+    P.y_stride = y_stride;
+    P.rows = rows;
+    P.K = K;
+    P.N = N;
+    P.nmt = pl.nmt;
+    P.nsl = pl.nsl;
+    P.sl = pl.sl;
+    P.nchunks = pl.nchunks;
+    P.n_items = pl.nmt * pl.nsl;
+    P.stages = pl.stages;
+    P.bulk = bulk;
+    P.sb3d = sb3d;
+    if (bulk) {
+        rc = get_encoder();
+        if (rc) return rc;
+        const long long segw = SEG * bits / 32, rowb = (long long)K * bits / 8;
+        rc = encode_3d(&P.tmW, W, CU_TENSOR_MAP_DATA_TYPE_UINT32, segw, N, K / SEG, rowb, segw * 4,
+                       (int)segw + 4, TN, SEGS);
+        const int sbg = CHUNK / group;
+        for (int i = 0; i < 2 && !rc; ++i) {
+            CUtensorMap *m = i ? &P.tmB : &P.tmS;
+            const void *base = i ? (const void *)b : (const void *)s;
+            if (sb3d)
+                rc = encode_3d(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT16, sbg, K / CHUNK, N, sbg * 2,
+                               (long long)(K / group) * 2, sbg + 8, 1, TN);
+            else
+                rc = encode_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / group, N, sbg, TN);
+        }
+        if (rc) return rc;
+    }
+    P.segpitch = pl.segpitch;
+    P.sbpitch = pl.sbpitch;
+    P.stage_bytes = pl.stage_bytes;
+    P.x_off = pl.x_off;
+    P.sx_off = pl.sx_off;
+    P.pb_off = pl.pb_off;
+    P.z_off = pl.z_off;
+    P.st_off = pl.st_off;
+    P.ncs = 1;
+    P.cs_src[0] = 0;
+    P.cs_len[0] = N;
+    P.cs_dst[0] = 0;
+    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(scratch status)");
+    if (pl.nsl > 1) {
+        // The scratch keeps the last call's contents: the arrival counters must start at zero.
+        e = cudaMemsetAsync(counters, 0, (size_t)pl.nmt * sizeof(int), st);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(scratch counters)");
+        P.ws = ws;
+        P.counters = counters;
+    }
+    e = launch(bits, group, pl.rb, P, pl.grid, pl.smem, st, false);
+    if (e != cudaSuccess) return cuda_fail(e, "qmm kernel launch");
+    return TF_OK;
+}
+
+int tfq::fail_message(int code, const char *msg) { return fail(code, msg); }
+
 // ============================================================== C ABI ====
 
 extern "C" {

@@ -2,6 +2,9 @@
 #pragma once
 #include <cuda_runtime.h>
 
+#include <stddef.h>
+#include <stdint.h>
+
 #include "qmm_common.h"
 
 namespace tfq {
@@ -19,5 +22,14 @@ cudaError_t launch_b6(int group, int rb, const QmmParams &P, int grid, int smem,
                       bool pdl);
 cudaError_t launch_b8(int group, int rb, const QmmParams &P, int grid, int smem, cudaStream_t st,
                       bool pdl);
+
+// Product whose split-K scratch and status word the caller provides (api.cu).
+int product_with_scratch(const uint16_t *x, int rows, int K, const uint32_t *W, const uint16_t *s,
+                         const uint16_t *b, int N, int bits, int group, float *y, int64_t y_stride,
+                         cudaStream_t st, int nsm, float *ws, size_t ws_floats, int *counters,
+                         size_t n_counters, int *status);
+
+// Records `msg` as the calling thread's last error and returns `code` (api.cu).
+int fail_message(int code, const char *msg);
 
 }  // namespace tfq
