@@ -307,12 +307,12 @@ def run_gpu(args, cases):
                           "gbs": round(it["bytes"] / (med * 1e-3) / 1e9, 1),
                           "frac_of_peak": round(it["bytes"] / (med * 1e-3) / 1e9 / peak, 4)})
     traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic_%s.json" % args.workload)
+    tpath = os.path.join(ROOT, "profiles", "traffic_%s.txt" % args.workload)
     if os.path.exists(tpath):
-        try:
-            traffic = json.load(open(tpath)).get("dram_bytes_per_step")
-        except Exception:
-            traffic = None
+        for line in open(tpath):
+            f = line.split()
+            if len(f) == 2 and f[0] == "dram_bytes_per_step":
+                traffic = int(f[1])
     if rank == 0:
         h2d = sum(it["x_pin"].numel() * 2 for it in items)
         d2h = sum(it["y_pin"].numel() * 4 for it in items)
@@ -337,6 +337,7 @@ def run_gpu(args, cases):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "traffic": traffic,
+                         "traffic_unit": "bytes per step (ncu, all qmm launches of one step)",
                          "kernel": "tfq::qmm_kernel (all products of the step, bytes / summed launch time)"},
             "cpu_baseline": cpu,
             "e2e": {"value": per_step * e2e_steps / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
