@@ -19,6 +19,9 @@
 // primitives (byte permute, funnel shift, bf16x2 fma).
 #pragma once
 #include <stdint.h>
+#if defined(__CUDACC__)
+#include <cuda_bf16.h>
+#endif
 
 #if defined(__CUDACC__)
 #define TF_HD __host__ __device__ __forceinline__
@@ -32,9 +35,7 @@ namespace tfq {
 // bit 3 of a selector nibble replicates that byte's top bit instead.
 TF_HD uint32_t prmt(uint32_t a, uint32_t b, uint32_t s) {
 #if defined(__CUDA_ARCH__)
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(s));
-    return d;
+    return __byte_perm(a, b, s);
 #else
     uint64_t v = ((uint64_t)b << 32) | a;
     uint32_t d = 0;
@@ -80,9 +81,10 @@ inline uint16_t float_to_bf16_host_exact(float f) {
 // d = a * b + c on two bf16 lanes (round to nearest even); exact in every use here.
 TF_HD uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
 #if defined(__CUDA_ARCH__)
-    uint32_t d;
-    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
+    const __nv_bfloat162 r = __hfma2(*reinterpret_cast<const __nv_bfloat162 *>(&a),
+                                     *reinterpret_cast<const __nv_bfloat162 *>(&b),
+                                     *reinterpret_cast<const __nv_bfloat162 *>(&c));
+    return *reinterpret_cast<const uint32_t *>(&r);
 #else
     uint32_t d = 0;
     for (int h = 0; h < 2; ++h) {
