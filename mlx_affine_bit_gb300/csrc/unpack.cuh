@@ -19,6 +19,7 @@
 // primitives (byte permute, funnel shift, bf16x2 fma).
 #pragma once
 #include <stdint.h>
+#include <string.h>
 #if defined(__CUDACC__)
 #include <cuda_bf16.h>
 #endif
@@ -85,10 +86,14 @@ inline uint16_t float_to_bf16_host_exact(float f) {
 // d = a * b + c on two bf16 lanes (round to nearest even); exact in every use here.
 TF_HD uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
 #if defined(__CUDA_ARCH__)
-    const __nv_bfloat162 r = __hfma2(*reinterpret_cast<const __nv_bfloat162 *>(&a),
-                                     *reinterpret_cast<const __nv_bfloat162 *>(&b),
-                                     *reinterpret_cast<const __nv_bfloat162 *>(&c));
-    return *reinterpret_cast<const uint32_t *>(&r);
+    __nv_bfloat162 A, B, C;   // bit copies (no type-punned pointers)
+    memcpy(&A, &a, 4);
+    memcpy(&B, &b, 4);
+    memcpy(&C, &c, 4);
+    const __nv_bfloat162 r = __hfma2(A, B, C);
+    uint32_t d;
+    memcpy(&d, &r, 4);
+    return d;
 #else
     uint32_t d = 0;
     for (int h = 0; h < 2; ++h) {
