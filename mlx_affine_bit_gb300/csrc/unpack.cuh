@@ -33,11 +33,9 @@
 namespace tfq {
 
 // Byte permute: result byte i = byte (s >> 4i) & 7 of the 8-byte value {b:a};
-// bit 3 of a selector nibble replicates that byte's top bit instead (that mode
-// needs the PTX instruction: the __byte_perm intrinsic ignores bit 3).
+// bit 3 of a selector nibble replicates that byte's top bit instead.
 TF_HD uint32_t prmt(uint32_t a, uint32_t b, uint32_t s) {
 #if defined(__CUDA_ARCH__)
-    if (__builtin_constant_p(s) && (s & 0x8888u) == 0) return __byte_perm(a, b, s);
     uint32_t d;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(s));
     return d;
