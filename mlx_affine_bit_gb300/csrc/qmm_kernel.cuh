@@ -123,6 +123,16 @@ __device__ __forceinline__ void mma_bf16(float c[4], uint32_t a0, uint32_t a1, u
 // completed and their memory is visible; returns at once otherwise.
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// d = A*B with a zero accumulator (no registers to clear first).
+__device__ __forceinline__ void mma_bf16_first(float c[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+        : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+
 __device__ __forceinline__ float bf16f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
 
 __device__ __forceinline__ void named_bar_consumers() {
@@ -342,8 +352,6 @@ __device__ __forceinline__ void group_body(const uint32_t *const (&pr0)[G / 32],
     constexpr int RUNS = G / 32;
     float c[NT][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
-#pragma unroll
     for (int m = 0; m < RUNS; ++m) {
         uint32_t pa[4], pb[4];
         Unpack<BITS>::run(pr0[m] + woff, ua[m], ub[m], pa);
@@ -351,7 +359,10 @@ __device__ __forceinline__ void group_body(const uint32_t *const (&pr0)[G / 32],
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const uint4 bb = bq[(m * LR + nt * 8) * 4];
-            mma_bf16(c[nt], pa[0], pb[0], pa[1], pb[1], bb.x, bb.y);
+            if (m == 0)
+                mma_bf16_first(c[nt], pa[0], pb[0], pa[1], pb[1], bb.x, bb.y);
+            else
+                mma_bf16(c[nt], pa[0], pb[0], pa[1], pb[1], bb.x, bb.y);
             mma_bf16(c[nt], pa[2], pb[2], pa[3], pb[3], bb.z, bb.w);
         }
     }
