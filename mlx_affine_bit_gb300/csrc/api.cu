@@ -60,20 +60,22 @@ int check_io(const uint16_t *x, int rows, const float *y) {
 
 struct Plan {
     int nmt, nsl, sl, nchunks, stages, smem, grid, segpitch, sbpitch, stage_bytes, x_off, sx_off,
-        pb_off, z_off, st_off, rb, ctas;
+        pb_off, z_off, st_off, rb, ctas, mt;
     bool sb3d;
 };
 
 int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
-Plan layout(int N, int K, int bits, int group, int rows, int nsm, int ctas, bool sb3d) {
+Plan layout(int N, int K, int bits, int group, int rows, int nsm, int ctas, bool sb3d, int mt) {
     Plan p{};
     p.rb = row_bucket(rows);
     p.ctas = ctas;
     p.sb3d = sb3d;
+    p.mt = mt;
+    const int rws = TN * mt;                                // output columns (W rows) per item
     const int xs_max = ctas == 2 ? XS_MAX / 2 : XS_MAX;
     const int budget = ctas == 2 ? SMEM_PER_SM / 2 - 1024 : SMEM_MAX;
-    p.nmt = ceil_div(N, TN);
+    p.nmt = ceil_div(N, rws);
     p.nchunks = ceil_div(K, CHUNK);
     const int lr = layout_rows(p.rb);
     const int max_cps = std::max(1, xs_max / (lr * 2 * CHUNK));   // chunks of x a CTA holds
@@ -96,10 +98,10 @@ Plan layout(int N, int K, int bits, int group, int rows, int nsm, int ctas, bool
     const int sbg = CHUNK / group;                          // groups of one stage
     p.segpitch = SEG * bits / 8 + 16;
     p.sbpitch = sb3d ? (sbg + 8) * 2 : sbg * 2;
-    p.stage_bytes = SEGS * TN * p.segpitch + 2 * TN * p.sbpitch;
+    p.stage_bytes = SEGS * rws * p.segpitch + 2 * rws * p.sbpitch;
     const int x_bytes = (lr * len * 2 + 127) & ~127;
     const int sx_bytes = ((len / group) * lr * 4 + 127) & ~127;
-    const int pb_bytes = 2 * SEGS * TN * lr * 4;
+    const int pb_bytes = 2 * SEGS * rws * lr * 4;
     p.x_off = HDR_BYTES;
     p.sx_off = p.x_off + x_bytes;
     p.pb_off = p.sx_off + sx_bytes;
@@ -111,12 +113,19 @@ Plan layout(int N, int K, int bits, int group, int rows, int nsm, int ctas, bool
     return p;
 }
 
-// Two CTAs per SM (16 consumer warps) when three stages of each still fit;
-// otherwise one CTA per SM with a deeper ring.
+// Two m-tiles (32 columns) per item with one CTA per SM when there are at
+// least two such items per SM (shared activation loads, half the per-stage
+// overhead); else one m-tile per item with two CTAs per SM when three stages
+// of each still fit; else one CTA per SM with a deeper ring.  The choice never
+// changes a result's bits.
 Plan make_plan(int N, int K, int bits, int group, int rows, int nsm, bool sb3d) {
-    const Plan two = layout(N, K, bits, group, rows, nsm, 2, sb3d);
+    if (row_bucket(rows) <= 8) {
+        const Plan wide = layout(N, K, bits, group, rows, nsm, 1, sb3d, 2);
+        if (wide.stages >= 3 && (long long)wide.nmt * wide.nsl >= 2LL * nsm) return wide;
+    }
+    const Plan two = layout(N, K, bits, group, rows, nsm, 2, sb3d, 1);
     if (two.stages >= 3) return two;
-    return layout(N, K, bits, group, rows, nsm, 1, sb3d);
+    return layout(N, K, bits, group, rows, nsm, 1, sb3d, 1);
 }
 
 // ------------------------------------------------------------ TMA maps --
@@ -172,7 +181,7 @@ int encode_3d(CUtensorMap *m, const void *base, CUtensorMapDataType t, long long
 // Encoded maps of recently used matrices (a map holds only address and shape).
 struct MapKey {
     const void *W, *s, *b;
-    int N, K, bits, group;
+    int N, K, bits, group, mt;
     bool operator<(const MapKey &o) const {
         if (W != o.W) return W < o.W;
         if (s != o.s) return s < o.s;
@@ -180,6 +189,7 @@ struct MapKey {
         if (N != o.N) return N < o.N;
         if (K != o.K) return K < o.K;
         if (bits != o.bits) return bits < o.bits;
+        if (mt != o.mt) return mt < o.mt;
         return group < o.group;
     }
 };
@@ -191,7 +201,7 @@ constexpr size_t MAP_CACHE_MAX = 512;
 
 int tensor_maps(const uint32_t *W, const uint16_t *s, const uint16_t *b, int N, int K, int bits,
                 int group, const Plan &pl, QmmParams &P) {
-    const MapKey key{W, s, b, N, K, bits, group};
+    const MapKey key{W, s, b, N, K, bits, group, pl.mt};
     auto it = g_maps.find(key);
     if (it == g_maps.end()) {
         int rc = get_encoder();
@@ -202,16 +212,16 @@ int tensor_maps(const uint32_t *W, const uint16_t *s, const uint16_t *b, int N, 
         // one stage lands segment-major with a row pitch of segment + 16 bytes
         // (the 4 words past each segment's extent are zero-filled, not read).
         rc = encode_3d(&ms.W, W, CU_TENSOR_MAP_DATA_TYPE_UINT32, segw, N, K / SEG, rowb, segw * 4,
-                       (int)segw + 4, TN, SEGS);
+                       (int)segw + 4, TN * pl.mt, SEGS);
         const int sbg = CHUNK / group;
         for (int i = 0; i < 2 && !rc; ++i) {
             CUtensorMap *m = i ? &ms.b : &ms.s;
             const void *base = i ? (const void *)b : (const void *)s;
             if (pl.sb3d)   // {stage groups, stages, rows}, box padded by 8 zero-filled groups
                 rc = encode_3d(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT16, sbg, K / CHUNK, N, sbg * 2,
-                               (long long)(K / group) * 2, sbg + 8, 1, TN);
+                               (long long)(K / group) * 2, sbg + 8, 1, TN * pl.mt);
             else
-                rc = encode_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / group, N, sbg, TN);
+                rc = encode_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / group, N, sbg, TN * pl.mt);
         }
         if (rc) return rc;
         if (g_maps.size() >= MAP_CACHE_MAX) g_maps.clear();
@@ -286,15 +296,15 @@ int stream_ws(cudaStream_t st, size_t floats, size_t counters, StreamWs **out) {
     return TF_OK;
 }
 
-cudaError_t launch(int bits, int group, int rb, const QmmParams &P, int grid, int smem,
+cudaError_t launch(int bits, int group, int rb, int mt, const QmmParams &P, int grid, int smem,
                    cudaStream_t st, bool pdl) {
     switch (bits) {
-        case 2: return launch_b2(group, rb, P, grid, smem, st, pdl);
-        case 3: return launch_b3(group, rb, P, grid, smem, st, pdl);
-        case 4: return launch_b4(group, rb, P, grid, smem, st, pdl);
-        case 5: return launch_b5(group, rb, P, grid, smem, st, pdl);
-        case 6: return launch_b6(group, rb, P, grid, smem, st, pdl);
-        case 8: return launch_b8(group, rb, P, grid, smem, st, pdl);
+        case 2: return launch_b2(group, rb, mt, P, grid, smem, st, pdl);
+        case 3: return launch_b3(group, rb, mt, P, grid, smem, st, pdl);
+        case 4: return launch_b4(group, rb, mt, P, grid, smem, st, pdl);
+        case 5: return launch_b5(group, rb, mt, P, grid, smem, st, pdl);
+        case 6: return launch_b6(group, rb, mt, P, grid, smem, st, pdl);
+        case 8: return launch_b8(group, rb, mt, P, grid, smem, st, pdl);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -357,7 +367,7 @@ int run_product(const uint16_t *x, int rows, int K, const uint32_t *W, const uin
     }
     const int mode = g_launch_mode.load(std::memory_order_relaxed);
     P.early_w = (mode & TF_LAUNCH_EARLY_WEIGHTS) != 0;
-    const cudaError_t e = launch(bits, group, pl.rb, P, pl.grid, pl.smem, st,
+    const cudaError_t e = launch(bits, group, pl.rb, pl.mt, P, pl.grid, pl.smem, st,
                                  (mode & (TF_LAUNCH_PDL | TF_LAUNCH_EARLY_WEIGHTS)) != 0);
     if (e != cudaSuccess) return cuda_fail(e, "qmm kernel launch");
     return TF_OK;
@@ -442,16 +452,16 @@ int tfq::product_with_scratch(const uint16_t *x, int rows, int K, const uint32_t
         if (rc) return rc;
         const long long segw = SEG * bits / 32, rowb = (long long)K * bits / 8;
         rc = encode_3d(&P.tmW, W, CU_TENSOR_MAP_DATA_TYPE_UINT32, segw, N, K / SEG, rowb, segw * 4,
-                       (int)segw + 4, TN, SEGS);
+                       (int)segw + 4, TN * pl.mt, SEGS);
         const int sbg = CHUNK / group;
         for (int i = 0; i < 2 && !rc; ++i) {
             CUtensorMap *m = i ? &P.tmB : &P.tmS;
             const void *base = i ? (const void *)b : (const void *)s;
             if (sb3d)
                 rc = encode_3d(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT16, sbg, K / CHUNK, N, sbg * 2,
-                               (long long)(K / group) * 2, sbg + 8, 1, TN);
+                               (long long)(K / group) * 2, sbg + 8, 1, TN * pl.mt);
             else
-                rc = encode_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / group, N, sbg, TN);
+                rc = encode_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, K / group, N, sbg, TN * pl.mt);
         }
         if (rc) return rc;
     }
@@ -476,7 +486,7 @@ int tfq::product_with_scratch(const uint16_t *x, int rows, int K, const uint32_t
         P.ws = ws;
         P.counters = counters;
     }
-    e = launch(bits, group, pl.rb, P, pl.grid, pl.smem, st, false);
+    e = launch(bits, group, pl.rb, pl.mt, P, pl.grid, pl.smem, st, false);
     if (e != cudaSuccess) return cuda_fail(e, "qmm kernel launch");
     return TF_OK;
 }

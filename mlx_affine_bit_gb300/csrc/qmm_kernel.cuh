@@ -185,9 +185,18 @@ struct Ring {
 
 // -------------------------------------------------------------- producer --
 
-template <int BITS, int G>
+// Stage layout: W [SEGS segments][ROWS rows][SEGP bytes], then scales and
+// biases [ROWS rows][sbpitch bytes] each.  SEGP = segment bytes + 16.
+template <int BITS>
+struct Pitch {
+    static constexpr int SEGP = SEG * BITS / 8 + 16;
+};
+
+template <int BITS, int G, int MT>
 __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint64_t *empty,
                          volatile int *abort) {
+    constexpr int ROWS = TN * MT;
+    constexpr int SEGP = Pitch<BITS>::SEGP;
     constexpr int SEGW = SEG * BITS / 32;     // words of one row segment
     const int lane = threadIdx.x & 31;
     const int S = P.stages;
@@ -205,13 +214,13 @@ __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
     Ring ring;
     for (ItemWalk w(P); w.more(P); w.next(P)) {
         const Item I = w.get(P);
-        const int n0 = I.mt * TN;
+        const int n0 = I.mt * ROWS;
         for (int k0 = I.k_lo; k0 < I.k_hi; k0 += CHUNK, ++it, ring.next(S)) {
             const int slot = (int)ring.slot;
             mbar_wait(&empty[slot], ring.phase ^ 1u, abort, P.status);
             uint8_t *st = smem + P.st_off + slot * P.stage_bytes;
-            uint8_t *sst = st + SEGS * TN * P.segpitch;
-            uint8_t *bst = sst + TN * P.sbpitch;
+            uint8_t *sst = st + SEGS * ROWS * SEGP;
+            uint8_t *bst = sst + ROWS * P.sbpitch;
             if (P.bulk) {
                 // Rows past N and segments past K arrive zero-filled; the full
                 // boxes count toward the transaction bytes.
@@ -229,13 +238,13 @@ __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
             } else {
                 // Odd shapes or alignments: plain copies by the warp into the same layout.
                 const int k1 = min(I.k_hi, k0 + CHUNK);
-                const int nrows = min(TN, P.N - n0);
+                const int nrows = min(ROWS, P.N - n0);
                 const int kw = (k1 - k0) * BITS / 32;               // words of this stage per row
                 for (int e = lane; e < nrows * kw; e += 32) {
-                    const int r = e / kw, w = e - r * kw;
-                    const int seg = w / SEGW, sw = w - seg * SEGW;
-                    reinterpret_cast<uint32_t *>(st + (seg * TN + r) * P.segpitch)[sw] =
-                        __ldg(P.W + (long long)(n0 + r) * row_words + (long long)k0 * BITS / 32 + w);
+                    const int r = e / kw, wd = e - r * kw;
+                    const int seg = wd / SEGW, sw = wd - seg * SEGW;
+                    reinterpret_cast<uint32_t *>(st + (seg * ROWS + r) * SEGP)[sw] =
+                        __ldg(P.W + (long long)(n0 + r) * row_words + (long long)k0 * BITS / 32 + wd);
                 }
                 const int ng = (k1 - k0) / G;
                 for (int e = lane; e < nrows * ng; e += 32) {
@@ -335,49 +344,61 @@ struct SegVals<2> {
     }
 };
 
-// One group of this lane's two columns: T = tensor-core dot products of the
-// group's exact codes with x, then p = fma(s,T,p); p = fma(b,sum_group(x),p).
-// pr0/pr1[m]: run m of the lane's quarter in column rows g and g+8 (words);
-// woff: the group's word offset in the segment row; bq: this lane's B entry
-// of the group's first run; sxq: the group's sum_group(x) at rows 2q, 2q+1.
-template <int BITS, int G, int RB>
-__device__ __forceinline__ void group_body(const uint32_t *const (&pr0)[G / 32],
-                                           const uint32_t *const (&pr1)[G / 32],
+// One group of this lane's 2*MT columns (rows t*16+g and t*16+g+8 of each
+// m-tile t): T = tensor-core dot products of the group's exact codes with x,
+// then p = fma(s,T,p); p = fma(b,sum_group(x),p).  pr[m]: run m of the lane's
+// quarter in row g of m-tile 0 (other rows at compile-time offsets); woff: the
+// group's word offset in the segment row; bq: this lane's B entry of the
+// group's first run (shared by the m-tiles); sxq: the group's sum_group(x).
+template <int BITS, int G, int RB, int MT>
+__device__ __forceinline__ void group_body(const uint32_t *const (&pr)[G / 32],
                                            const uint32_t (&ua)[G / 32], const uint32_t (&ub)[G / 32],
-                                           int woff, const uint4 *bq, float sg0, float sg1, float bg0,
-                                           float bg1, const float *sxq,
-                                           float (&p)[(RB > 8 ? 2 : 1)][4]) {
+                                           int woff, const uint4 *bq, const float (&sg)[MT][2],
+                                           const float (&bg)[MT][2], const float *sxq,
+                                           float (&p)[MT][(RB > 8 ? 2 : 1)][4]) {
     constexpr int NT = RB > 8 ? 2 : 1;
     constexpr int LR = layout_rows(RB);
     constexpr int RUNS = G / 32;
-    float c[NT][4];
+    constexpr int RW = Pitch<BITS>::SEGP / 4;     // words between rows of a segment block
+    float c[MT][NT][4];
 #pragma unroll
     for (int m = 0; m < RUNS; ++m) {
-        uint32_t pa[4], pb[4];
-        Unpack<BITS>::run(pr0[m] + woff, ua[m], ub[m], pa);
-        Unpack<BITS>::run(pr1[m] + woff, ua[m], ub[m], pb);
+        uint4 bb[NT];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const uint4 bb = bq[(m * LR + nt * 8) * 4];
-            if (m == 0)
-                mma_bf16_first(c[nt], pa[0], pb[0], pa[1], pb[1], bb.x, bb.y);
-            else
-                mma_bf16(c[nt], pa[0], pb[0], pa[1], pb[1], bb.x, bb.y);
-            mma_bf16(c[nt], pa[2], pb[2], pa[3], pb[3], bb.z, bb.w);
+        for (int nt = 0; nt < NT; ++nt) bb[nt] = bq[(m * LR + nt * 8) * 4];
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+            uint32_t pa[4], pb[4];
+            Unpack<BITS>::run(pr[m] + woff + (t * 16) * RW, ua[m], ub[m], pa);
+            Unpack<BITS>::run(pr[m] + woff + (t * 16 + 8) * RW, ua[m], ub[m], pb);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                if (m == 0)
+                    mma_bf16_first(c[t][nt], pa[0], pb[0], pa[1], pb[1], bb[nt].x, bb[nt].y);
+                else
+                    mma_bf16(c[t][nt], pa[0], pb[0], pa[1], pb[1], bb[nt].x, bb[nt].y);
+                mma_bf16(c[t][nt], pa[2], pb[2], pa[3], pb[3], bb[nt].z, bb[nt].w);
+            }
         }
     }
     if (RB == 1) {   // a single activation row: only row 0 of the tile is live
         const float x0 = *sxq;
-        p[0][0] = fmaf(bg0, x0, fmaf(sg0, c[0][0], p[0][0]));
-        p[0][2] = fmaf(bg1, x0, fmaf(sg1, c[0][2], p[0][2]));
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+            p[t][0][0] = fmaf(bg[t][0], x0, fmaf(sg[t][0], c[t][0][0], p[t][0][0]));
+            p[t][0][2] = fmaf(bg[t][1], x0, fmaf(sg[t][1], c[t][0][2], p[t][0][2]));
+        }
     } else {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const float2 v = *reinterpret_cast<const float2 *>(sxq + nt * 8);
-            p[nt][0] = fmaf(bg0, v.x, fmaf(sg0, c[nt][0], p[nt][0]));
-            p[nt][1] = fmaf(bg0, v.y, fmaf(sg0, c[nt][1], p[nt][1]));
-            p[nt][2] = fmaf(bg1, v.x, fmaf(sg1, c[nt][2], p[nt][2]));
-            p[nt][3] = fmaf(bg1, v.y, fmaf(sg1, c[nt][3], p[nt][3]));
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                p[t][nt][0] = fmaf(bg[t][0], v.x, fmaf(sg[t][0], c[t][nt][0], p[t][nt][0]));
+                p[t][nt][1] = fmaf(bg[t][0], v.y, fmaf(sg[t][0], c[t][nt][1], p[t][nt][1]));
+                p[t][nt][2] = fmaf(bg[t][1], v.x, fmaf(sg[t][1], c[t][nt][2], p[t][nt][2]));
+                p[t][nt][3] = fmaf(bg[t][1], v.y, fmaf(sg[t][1], c[t][nt][3], p[t][nt][3]));
+            }
         }
     }
 }
@@ -397,30 +418,33 @@ __device__ __forceinline__ void store_y(const QmmParams &P, int r, int n, float 
     }
 }
 
-template <int BITS, int G, int RB>
+template <int BITS, int G, int RB, int MT>
 __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint64_t *empty,
-                           volatile int *abort, volatile int *flag) {
+                         volatile int *abort, volatile int *flag) {
     constexpr int NT = RB > 8 ? 2 : 1;
+    constexpr int ROWS = TN * MT;
+    constexpr int SEGP = Pitch<BITS>::SEGP;
     constexpr int QG = G / 4;                // codes of a group per quad lane
     constexpr int RUNS = G / 32;             // 8-code runs per quad lane per group
     constexpr int GW = G * BITS / 32;        // words per group of one row
     constexpr int NGS = SEG / G;             // groups per segment
     constexpr int LR = layout_rows(RB);      // rows of the B / sum_group(x) layouts
-    constexpr int NFW = LR / 2;              // fold warps: TN*LR outputs, one per thread
+    constexpr int NOUT = ROWS * LR;          // outputs of an item (padded rows)
+    constexpr int OUTS = (NOUT + NCW * 32 - 1) / (NCW * 32);   // outputs folded per thread
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, q = lane & 3;
     const int S = P.stages, rows = P.rows;
     uint4 *Bf = reinterpret_cast<uint4 *>(smem + P.x_off);
     float *sx = reinterpret_cast<float *>(smem + P.sx_off);
-    float *pbuf = reinterpret_cast<float *>(smem + P.pb_off);   // [2][SEGS][TN][LR]
+    float *pbuf = reinterpret_cast<float *>(smem + P.pb_off);   // [2][SEGS][ROWS][LR]
     const uint8_t *zero = smem + P.z_off;
     // Lanes past the bucket's rows read a zero block instead of B / sum_group(x).
     const bool b_lane = g < LR, sx_lane = 2 * q < LR;
     if (LR < 8) {
         for (int i = tid; i < ZERO_BYTES / 4; i += NCW * 32) reinterpret_cast<uint32_t *>(smem + P.z_off)[i] = 0u;
     }
-    // This lane's runs inside any group: word offset and bit shift of run m.
+    // This lane's runs inside any group: word offset and unpack arguments of run m.
     uint32_t wo[RUNS], ua[RUNS], ub[RUNS];
 #pragma unroll
     for (int m = 0; m < RUNS; ++m) {
@@ -428,10 +452,9 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
         wo[m] = bit >> 5;
         lane_args<BITS>(bit & 31u, ua[m], ub[m]);
     }
-    // Fold threads: thread t < TN*RB (warps < NFW) owns output (column fc, row fr).
-    const bool fold_warp = warp < NFW;
-    const int fc = tid / LR, fr = tid - (tid / LR) * LR;
-    float yacc = 0.f;
+    float yacc[OUTS];
+#pragma unroll
+    for (int i = 0; i < OUTS; ++i) yacc[i] = 0.f;
 
     // x, y and the split-K workspace may be touched by the previous kernel of
     // the stream (programmatic dependent launch): wait for it first.
@@ -447,7 +470,7 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
             named_bar_consumers();
             cur_slice = I.slice;
         }
-        const int n0 = I.mt * TN;
+        const int n0 = I.mt * ROWS;
         for (int k0 = I.k_lo; k0 < I.k_hi; k0 += CHUNK, ++it, ring.next(S)) {
             const int k1 = min(I.k_hi, k0 + CHUNK);
             const int slot = (int)ring.slot;
@@ -455,21 +478,18 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
             const int ks0 = k0 + warp * SEG;      // this warp's segment
             const bool active = ks0 < k1;
             mbar_wait(&full[slot], ring.phase, abort, P.status);
-            float p[NT][4];
+            float p[MT][NT][4];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) p[nt][0] = p[nt][1] = p[nt][2] = p[nt][3] = 0.f;
+            for (int t = 0; t < MT; ++t)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) p[t][nt][0] = p[t][nt][1] = p[t][nt][2] = p[t][nt][3] = 0.f;
             if (active) {
                 const uint8_t *st = smem + P.st_off + slot * P.stage_bytes;
-                const uint8_t *blk = st + warp * TN * P.segpitch;
-                const uint32_t *wr0 = reinterpret_cast<const uint32_t *>(blk + g * P.segpitch);
-                const uint32_t *wr1 = reinterpret_cast<const uint32_t *>(blk + (g + 8) * P.segpitch);
-                const uint32_t *pr0[RUNS], *pr1[RUNS];
+                const uint32_t *wr = reinterpret_cast<const uint32_t *>(st + (warp * ROWS + g) * SEGP);
+                const uint32_t *pr[RUNS];
 #pragma unroll
-                for (int m = 0; m < RUNS; ++m) {
-                    pr0[m] = wr0 + wo[m];
-                    pr1[m] = wr1 + wo[m];
-                }
-                const uint8_t *sbase = st + SEGS * TN * P.segpitch;
+                for (int m = 0; m < RUNS; ++m) pr[m] = wr + wo[m];
+                const uint8_t *sbase = st + SEGS * ROWS * SEGP;
                 const int gseg = warp * NGS;                             // segment's first group in the stage
                 const int gs0 = (ks0 - I.k_lo) / G;                      // slice group index
                 const uint4 *bq = (LR >= 8 || b_lane) ? Bf + (gs0 * RUNS * LR + g) * 4 + q
@@ -477,80 +497,114 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                 const float *sxq = (LR >= 8 || sx_lane) ? sx + gs0 * LR + 2 * q
                                                         : reinterpret_cast<const float *>(zero);
                 const int ng = (min(k1, ks0 + SEG) - ks0) / G;
-                const uint16_t *s0p = reinterpret_cast<const uint16_t *>(sbase + g * P.sbpitch) + gseg;
-                const uint16_t *s1p = reinterpret_cast<const uint16_t *>(sbase + (g + 8) * P.sbpitch) + gseg;
-                const uint16_t *b0p = reinterpret_cast<const uint16_t *>(sbase + (TN + g) * P.sbpitch) + gseg;
-                const uint16_t *b1p = reinterpret_cast<const uint16_t *>(sbase + (TN + g + 8) * P.sbpitch) + gseg;
+                const uint16_t *sp = reinterpret_cast<const uint16_t *>(sbase + g * P.sbpitch) + gseg;
+                const uint16_t *bp = reinterpret_cast<const uint16_t *>(sbase + (ROWS + g) * P.sbpitch) + gseg;
+                const int rstep = 8 * P.sbpitch / 2;                     // 8 rows, in bf16 elements
                 if (ng == NGS) {
-                    SegVals<NGS> S0, S1, B0, B1;
-                    S0.load(s0p);
-                    S1.load(s1p);
-                    B0.load(b0p);
-                    B1.load(b1p);
+                    SegVals<NGS> Sv[MT][2], Bv[MT][2];
 #pragma unroll
-                    for (int gl = 0; gl < NGS; ++gl)
-                        group_body<BITS, G, RB>(pr0, pr1, ua, ub, gl * GW, bq + gl * RUNS * LR * 4,
-                                                S0.get(gl), S1.get(gl), B0.get(gl), B1.get(gl),
-                                                sxq + gl * LR, p);
+                    for (int t = 0; t < MT; ++t)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            Sv[t][h].load(sp + (2 * t + h) * rstep);
+                            Bv[t][h].load(bp + (2 * t + h) * rstep);
+                        }
+#pragma unroll
+                    for (int gl = 0; gl < NGS; ++gl) {
+                        float sg[MT][2], bg[MT][2];
+#pragma unroll
+                        for (int t = 0; t < MT; ++t)
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                sg[t][h] = Sv[t][h].get(gl);
+                                bg[t][h] = Bv[t][h].get(gl);
+                            }
+                        group_body<BITS, G, RB, MT>(pr, ua, ub, gl * GW, bq + gl * RUNS * LR * 4, sg, bg,
+                                                    sxq + gl * LR, p);
+                    }
                 } else {
 #pragma unroll 1
-                    for (int gl = 0; gl < ng; ++gl)
-                        group_body<BITS, G, RB>(pr0, pr1, ua, ub, gl * GW, bq + gl * RUNS * LR * 4,
-                                                bf16f(s0p[gl]), bf16f(s1p[gl]), bf16f(b0p[gl]),
-                                                bf16f(b1p[gl]), sxq + gl * LR, p);
+                    for (int gl = 0; gl < ng; ++gl) {
+                        float sg[MT][2], bg[MT][2];
+#pragma unroll
+                        for (int t = 0; t < MT; ++t)
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                sg[t][h] = bf16f(sp[(2 * t + h) * rstep + gl]);
+                                bg[t][h] = bf16f(bp[(2 * t + h) * rstep + gl]);
+                            }
+                        group_body<BITS, G, RB, MT>(pr, ua, ub, gl * GW, bq + gl * RUNS * LR * 4, sg, bg,
+                                                    sxq + gl * LR, p);
+                    }
                 }
             }
             {   // release the slot once every shared read of it has been consumed
                 float dep = 0.f;
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) dep += p[nt][0] + p[nt][1] + p[nt][2] + p[nt][3];
+                for (int t = 0; t < MT; ++t)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) dep += p[t][nt][0] + p[t][nt][2];
                 __syncwarp();
                 if (lane == 0) mbar_arrive_after(&empty[slot], dep);
             }
-            float *pw = pbuf + ((buf * SEGS + warp) * TN) * LR;
+            // Segment partial -> pbuf[buf][warp][row][padded activation row].
+            float *pw = pbuf + ((buf * SEGS + warp) * ROWS) * LR;
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+            for (int t = 0; t < MT; ++t)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int r = nt * 8 + 2 * q + (e & 1);
-                    const int c = g + 8 * (e >> 1);
-                    if (r < LR) pw[c * LR + r] = p[nt][e];
-                }
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int r = nt * 8 + 2 * q + (e & 1);
+                        const int c = t * 16 + g + 8 * (e >> 1);
+                        if (r < LR) pw[c * LR + r] = p[t][nt][e];
+                    }
             named_bar_consumers();
-            if (fold_warp) {
-                const float *pf = pbuf + (buf * SEGS * TN + fc) * LR + fr;
-                const int nseg = (k1 - k0 + SEG - 1) / SEG;
-                float C = pf[0];
-                for (int j = 1; j < nseg; ++j) C = C + pf[j * TN * LR];
-                const int chunk = k0 / CHUNK;
-                if (P.nsl == 1) {
-                    yacc = chunk == 0 ? C : yacc + C;
-                    if (k0 + CHUNK >= I.k_hi) store_y(P, fr, n0 + fc, yacc);
-                } else if (fr < rows && n0 + fc < P.N) {
-                    P.ws[((long long)chunk * rows + fr) * P.N + n0 + fc] = C;
+            // Chunk sum C = P_0 + P_1 + ... in segment order, then the chunk fold.
+            const int nseg = (k1 - k0 + SEG - 1) / SEG;
+            const int chunk = k0 / CHUNK;
+#pragma unroll
+            for (int i = 0; i < OUTS; ++i) {
+                const int o = tid + i * NCW * 32;
+                if (o < NOUT) {
+                    const int fc = o / LR, fr = o - (o / LR) * LR;
+                    const float *pf = pbuf + (buf * SEGS * ROWS + fc) * LR + fr;
+                    float C = pf[0];
+                    for (int j = 1; j < nseg; ++j) C = C + pf[j * ROWS * LR];
+                    if (P.nsl == 1) {
+                        yacc[i] = chunk == 0 ? C : yacc[i] + C;
+                        if (k0 + CHUNK >= I.k_hi) store_y(P, fr, n0 + fc, yacc[i]);
+                    } else if (fr < rows && n0 + fc < P.N) {
+                        P.ws[((long long)chunk * rows + fr) * P.N + n0 + fc] = C;
+                    }
                 }
             }
         }
         if (P.nsl > 1) {
-            // Split K: fold this item's last chunk now, then the last CTA to finish
-            // the m-tile folds the chunk sums in chunk order (an arrival ticket).
-            if (fold_warp) {
+            // Split K: the last CTA to finish an item folds its chunk sums in
+            // chunk order (an arrival ticket; nothing waits).
+            __threadfence();
+            named_bar_consumers();
+            if (tid == 0) *flag = atomicAdd(&P.counters[I.mt], 1) == P.nsl - 1;
+            named_bar_consumers();
+            if (*flag) {
                 __threadfence();
-                asm volatile("bar.sync 2, %0;" ::"r"(NFW * 32) : "memory");
-                if (tid == 0) *flag = atomicAdd(&P.counters[I.mt], 1) == P.nsl - 1;
-                asm volatile("bar.sync 2, %0;" ::"r"(NFW * 32) : "memory");
-                if (*flag) {
-                    __threadfence();
-                    if (fr < rows && n0 + fc < P.N) {
-                        const long long n = n0 + fc;
-                        float v = __ldcg(P.ws + (long long)fr * P.N + n);
-                        for (int ch = 1; ch < P.nchunks; ++ch)
-                            v = v + __ldcg(P.ws + ((long long)ch * rows + fr) * P.N + n);
-                        store_y(P, fr, (int)n, v);
+#pragma unroll
+                for (int i = 0; i < OUTS; ++i) {
+                    const int o = tid + i * NCW * 32;
+                    if (o < NOUT) {
+                        const int fc = o / LR, fr = o - (o / LR) * LR;
+                        if (fr < rows && n0 + fc < P.N) {
+                            const long long n = n0 + fc;
+                            float v = __ldcg(P.ws + (long long)fr * P.N + n);
+                            for (int ch = 1; ch < P.nchunks; ++ch)
+                                v = v + __ldcg(P.ws + ((long long)ch * rows + fr) * P.N + n);
+                            store_y(P, fr, (int)n, v);
+                        }
                     }
-                    asm volatile("bar.sync 2, %0;" ::"r"(NFW * 32) : "memory");
-                    if (tid == 0) P.counters[I.mt] = 0;
                 }
+                named_bar_consumers();
+                if (tid == 0) P.counters[I.mt] = 0;
             }
         }
     }
@@ -558,8 +612,8 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
 
 // ------------------------------------------------------------------ kernel --
 
-template <int BITS, int G, int RB>
-__global__ void __launch_bounds__(NTHREADS, 2) qmm_kernel(const __grid_constant__ QmmParams P) {
+template <int BITS, int G, int RB, int MT>
+__global__ void __launch_bounds__(NTHREADS, MT == 1 ? 2 : 1) qmm_kernel(const __grid_constant__ QmmParams P) {
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + MAX_STAGES;
@@ -579,18 +633,18 @@ __global__ void __launch_bounds__(NTHREADS, 2) qmm_kernel(const __grid_constant_
     // this grid is resident (no effect without programmatic dependent launch).
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x >= NCW * 32)
-        producer<BITS, G>(P, smem, full, empty, abort);
+        producer<BITS, G, MT>(P, smem, full, empty, abort);
     else
-        consumer<BITS, G, RB>(P, smem, full, empty, abort, flag);
+        consumer<BITS, G, RB, MT>(P, smem, full, empty, abort, flag);
 }
 
 // Host-side launcher for one width: every group and row bucket.
 template <int BITS>
-cudaError_t launch_width(int group, int rb, const QmmParams &P, int grid, int smem, cudaStream_t st,
-                         bool pdl) {
-#define TFQ_CASE(G_, RB_)                                                                     \
-    if (group == G_ && rb == RB_) {                                                           \
-        auto k = qmm_kernel<BITS, G_, RB_>;                                                   \
+cudaError_t launch_width(int group, int rb, int mt, const QmmParams &P, int grid, int smem,
+                         cudaStream_t st, bool pdl) {
+#define TFQ_CASE(G_, RB_, MT_)                                                                \
+    if (group == G_ && rb == RB_ && mt == MT_) {                                              \
+        auto k = qmm_kernel<BITS, G_, RB_, MT_>;                                              \
         static unsigned attr_set = 0; /* one bit per device: smem limit raised */             \
         int dev = 0;                                                                          \
         cudaError_t e = cudaGetDevice(&dev);                                                  \
@@ -613,9 +667,10 @@ cudaError_t launch_width(int group, int rb, const QmmParams &P, int grid, int sm
         cfg.numAttrs = pdl ? 1 : 0;                                                           \
         return cudaLaunchKernelEx(&cfg, k, P);                                                \
     }
-    TFQ_CASE(32, 1) TFQ_CASE(32, 2) TFQ_CASE(32, 4) TFQ_CASE(32, 8) TFQ_CASE(32, 16)
-    TFQ_CASE(64, 1) TFQ_CASE(64, 2) TFQ_CASE(64, 4) TFQ_CASE(64, 8) TFQ_CASE(64, 16)
-    TFQ_CASE(128, 1) TFQ_CASE(128, 2) TFQ_CASE(128, 4) TFQ_CASE(128, 8) TFQ_CASE(128, 16)
+#define TFQ_ROWS(G_) TFQ_CASE(G_, 1, 1) TFQ_CASE(G_, 2, 1) TFQ_CASE(G_, 4, 1) TFQ_CASE(G_, 8, 1)      \
+    TFQ_CASE(G_, 16, 1) TFQ_CASE(G_, 1, 2) TFQ_CASE(G_, 2, 2) TFQ_CASE(G_, 4, 2) TFQ_CASE(G_, 8, 2)
+    TFQ_ROWS(32) TFQ_ROWS(64) TFQ_ROWS(128)
+#undef TFQ_ROWS
 #undef TFQ_CASE
     return cudaErrorInvalidValue;
 }
