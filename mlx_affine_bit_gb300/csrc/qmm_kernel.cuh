@@ -368,16 +368,17 @@ __device__ __forceinline__ void group_body(const uint32_t *const (&pr)[G / 32],
         for (int nt = 0; nt < NT; ++nt) bb[nt] = bq[(m * LR + nt * 8) * 4];
 #pragma unroll
         for (int t = 0; t < MT; ++t) {
-            uint32_t pa[4], pb[4];
-            Unpack<BITS>::run(pr[m] + woff + (t * 16) * RW, ua[m], ub[m], pa);
-            Unpack<BITS>::run(pr[m] + woff + (t * 16 + 8) * RW, ua[m], ub[m], pb);
+            // A registers in MMA operand order: a[2i] = pair i of row g, a[2i+1] of row g+8.
+            uint32_t a[8];
+            Unpack<BITS>::template run<2>(pr[m] + woff + (t * 16) * RW, ua[m], ub[m], a);
+            Unpack<BITS>::template run<2>(pr[m] + woff + (t * 16 + 8) * RW, ua[m], ub[m], a + 1);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 if (m == 0)
-                    mma_bf16_first(c[t][nt], pa[0], pb[0], pa[1], pb[1], bb[nt].x, bb[nt].y);
+                    mma_bf16_first(c[t][nt], a[0], a[1], a[2], a[3], bb[nt].x, bb[nt].y);
                 else
-                    mma_bf16(c[t][nt], pa[0], pb[0], pa[1], pb[1], bb[nt].x, bb[nt].y);
-                mma_bf16(c[t][nt], pa[2], pb[2], pa[3], pb[3], bb[nt].z, bb[nt].w);
+                    mma_bf16(c[t][nt], a[0], a[1], a[2], a[3], bb[nt].x, bb[nt].y);
+                mma_bf16(c[t][nt], a[4], a[5], a[6], a[7], bb[nt].z, bb[nt].w);
             }
         }
     }

@@ -112,7 +112,7 @@ constexpr uint32_t Q2 = 0x3E803E80u, NEG32 = 0xC200C200u;   // p=2: 1/4, -32
 constexpr uint32_t Q3 = 0x3E003E00u, NEG16 = 0xC180C180u;   // p=3: 1/8, -16
 constexpr uint32_t Q4 = 0x3D803D80u, NEG8 = 0xC100C100u;    // p=4: 1/16, -8
 
-// Run of 8 codes -> pairs p[i] = (c_i | c_{i+4} << 16) as exact bf16 values.
+// Run of 8 codes -> pairs p[i*ST] = (c_i | c_{i+4} << 16) as exact bf16 values.
 // `w` points at the 32-bit word holding the run's first bit; `ua`/`ub` come
 // from lane_args<BITS>(sh) with `sh` that bit's position in the word (they are
 // per-lane constants, computed once).  Reads at most w[0], w[1].
@@ -121,24 +121,26 @@ struct Unpack;
 
 template <>
 struct Unpack<2> {  // 16 bits; sh in {0, 16}
-    static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t, uint32_t p[4]) {
+    template <int ST = 1>
+    static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t, uint32_t *p) {
         uint32_t v = w[0] >> sh;
         uint32_t u = halves(v, v << 8);              // c0..c3 @0,2,4,6 | c4..c7 @16,18,20,22
-        p[0] = hfma2(mask_or(u, 0x00030003u, MAGIC), ONE2, NEG128);
-        p[1] = hfma2(mask_or(u, 0x000C000Cu, MAGIC), Q2, NEG32);
-        p[2] = hfma2(mask_or(u, 0x00300030u, MAGIC), Q4, NEG8);
-        p[3] = hfma2(mask_or(u >> 2, 0x00300030u, MAGIC), Q4, NEG8);
+        p[0 * ST] = hfma2(mask_or(u, 0x00030003u, MAGIC), ONE2, NEG128);
+        p[1 * ST] = hfma2(mask_or(u, 0x000C000Cu, MAGIC), Q2, NEG32);
+        p[2 * ST] = hfma2(mask_or(u, 0x00300030u, MAGIC), Q4, NEG8);
+        p[3 * ST] = hfma2(mask_or(u >> 2, 0x00300030u, MAGIC), Q4, NEG8);
     }
 };
 
 template <>
 struct Unpack<4> {  // 32 bits; sh == 0
-    static TF_HD void run(const uint32_t *w, uint32_t, uint32_t, uint32_t p[4]) {
+    template <int ST = 1>
+    static TF_HD void run(const uint32_t *w, uint32_t, uint32_t, uint32_t *p) {
         uint32_t v = w[0];
-        p[0] = hfma2(mask_or(v, 0x000F000Fu, MAGIC), ONE2, NEG128);
-        p[1] = hfma2(mask_or(v >> 4, 0x000F000Fu, MAGIC), ONE2, NEG128);
-        p[2] = hfma2(mask_or(v >> 8, 0x000F000Fu, MAGIC), ONE2, NEG128);
-        p[3] = hfma2(mask_or(v >> 12, 0x000F000Fu, MAGIC), ONE2, NEG128);
+        p[0 * ST] = hfma2(mask_or(v, 0x000F000Fu, MAGIC), ONE2, NEG128);
+        p[1 * ST] = hfma2(mask_or(v >> 4, 0x000F000Fu, MAGIC), ONE2, NEG128);
+        p[2 * ST] = hfma2(mask_or(v >> 8, 0x000F000Fu, MAGIC), ONE2, NEG128);
+        p[3 * ST] = hfma2(mask_or(v >> 12, 0x000F000Fu, MAGIC), ONE2, NEG128);
     }
 };
 
@@ -151,52 +153,56 @@ struct Unpack<8> {  // 64 bits; sh == 0
         uint32_t add = ~sgn & NEG128;                       // -128 if c < 128, else 0
         return hfma2(mant, ONE2, add);
     }
-    static TF_HD void run(const uint32_t *w, uint32_t, uint32_t, uint32_t p[4]) {
+    template <int ST = 1>
+    static TF_HD void run(const uint32_t *w, uint32_t, uint32_t, uint32_t *p) {
         uint32_t lo = w[0], hi = w[1];
-        p[0] = one(prmt(lo, hi, 0x0400u));   // byte i of lo -> 0, byte i of hi -> 2
-        p[1] = one(prmt(lo, hi, 0x0501u));
-        p[2] = one(prmt(lo, hi, 0x0602u));
-        p[3] = one(prmt(lo, hi, 0x0703u));
+        p[0 * ST] = one(prmt(lo, hi, 0x0400u));   // byte i of lo -> 0, byte i of hi -> 2
+        p[1 * ST] = one(prmt(lo, hi, 0x0501u));
+        p[2 * ST] = one(prmt(lo, hi, 0x0602u));
+        p[3 * ST] = one(prmt(lo, hi, 0x0703u));
     }
 };
 
 template <>
 struct Unpack<3> {  // 24 bits; sh in {0, 8, 16, 24}
-    static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t, uint32_t p[4]) {
+    template <int ST = 1>
+    static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t, uint32_t *p) {
         uint32_t v = funnel(w[0], w[1], sh);
         uint32_t u = halves(v, v << 4);   // c0..c3 @0,3,6,9 | c4..c7 @16,19,22,25
-        p[0] = hfma2(mask_or(u, 0x00070007u, MAGIC), ONE2, NEG128);
-        p[1] = hfma2(mask_or(u, 0x00380038u, MAGIC), Q3, NEG16);
+        p[0 * ST] = hfma2(mask_or(u, 0x00070007u, MAGIC), ONE2, NEG128);
+        p[1 * ST] = hfma2(mask_or(u, 0x00380038u, MAGIC), Q3, NEG16);
         uint32_t u2 = u >> 6;             // c2 @0, c3 @3 | c6 @16, c7 @19
-        p[2] = hfma2(mask_or(u2, 0x00070007u, MAGIC), ONE2, NEG128);
-        p[3] = hfma2(mask_or(u2, 0x00380038u, MAGIC), Q3, NEG16);
+        p[2 * ST] = hfma2(mask_or(u2, 0x00070007u, MAGIC), ONE2, NEG128);
+        p[3 * ST] = hfma2(mask_or(u2, 0x00380038u, MAGIC), Q3, NEG16);
     }
 };
 
 template <>
 struct Unpack<5> {  // 40 bits; sh in {0, 8, 16, 24}
-    static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t, uint32_t p[4]) {
+    template <int ST = 1>
+    static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t, uint32_t *p) {
         uint32_t lo = funnel(w[0], w[1], sh);               // run bits 0..31
         uint32_t hi = w[1] >> sh;                           // run bits 32..39 at 0..7
         uint32_t u = halves(lo, funnel(lo, hi, 4));         // c0,c1,c2 @0,5,10 | c4,c5,c6 @16,21,26
-        p[0] = hfma2(mask_or(u, 0x001F001Fu, MAGIC), ONE2, NEG128);
-        p[1] = hfma2(mask_or(u >> 5, 0x001F001Fu, MAGIC), ONE2, NEG128);
-        p[2] = hfma2(mask_or(u >> 10, 0x001F001Fu, MAGIC), ONE2, NEG128);
+        p[0 * ST] = hfma2(mask_or(u, 0x001F001Fu, MAGIC), ONE2, NEG128);
+        p[1 * ST] = hfma2(mask_or(u >> 5, 0x001F001Fu, MAGIC), ONE2, NEG128);
+        p[2 * ST] = hfma2(mask_or(u >> 10, 0x001F001Fu, MAGIC), ONE2, NEG128);
         uint32_t u3 = halves(lo >> 15, funnel(lo, hi, 19)); // c3 @0 | c7 @16
-        p[3] = hfma2(mask_or(u3, 0x001F001Fu, MAGIC), ONE2, NEG128);
+        p[3 * ST] = hfma2(mask_or(u3, 0x001F001Fu, MAGIC), ONE2, NEG128);
     }
 };
 
 template <>
 struct Unpack<6> {  // 48 bits; sh in {0, 16}
     // Run bytes {0,1,3,4} and {1,2,4,5}; raw byte = run byte + sh/8 (sh = 0 or 16).
-    static TF_HD void run(const uint32_t *w, uint32_t s0, uint32_t s2, uint32_t p[4]) {
+    template <int ST = 1>
+    static TF_HD void run(const uint32_t *w, uint32_t s0, uint32_t s2, uint32_t *p) {
         uint32_t P0 = prmt(w[0], w[1], s0);   // c0 @0, c1 @6 | c4 @16, c5 @22
         uint32_t P2 = prmt(w[0], w[1], s2);   // c2 @4, c3 @10 | c6 @20, c7 @26
-        p[0] = hfma2(mask_or(P0, 0x003F003Fu, MAGIC), ONE2, NEG128);
-        p[1] = hfma2(mask_or(P0 >> 6, 0x003F003Fu, MAGIC), ONE2, NEG128);
-        p[2] = hfma2(mask_or(P2 >> 4, 0x003F003Fu, MAGIC), ONE2, NEG128);
-        p[3] = hfma2(mask_or(P2 >> 10, 0x003F003Fu, MAGIC), ONE2, NEG128);
+        p[0 * ST] = hfma2(mask_or(P0, 0x003F003Fu, MAGIC), ONE2, NEG128);
+        p[1 * ST] = hfma2(mask_or(P0 >> 6, 0x003F003Fu, MAGIC), ONE2, NEG128);
+        p[2 * ST] = hfma2(mask_or(P2 >> 4, 0x003F003Fu, MAGIC), ONE2, NEG128);
+        p[3 * ST] = hfma2(mask_or(P2 >> 10, 0x003F003Fu, MAGIC), ONE2, NEG128);
     }
 };
 
