@@ -51,6 +51,9 @@ def workload_cases(name: str):
     if name == "lmhead16":
         return [("lmhead %d/%d r16" % (b, g), synth.LMHEAD_N, synth.LMHEAD_K, b, g, s, 16)
                 for (b, g, s) in synth.LMHEAD_CASES]
+    if name == "stack":
+        return [("stack 5/64 run r%d" % r, 6192, synth.STACK_K, 5, 64, 21, r) for r in synth.STACK_ROWS] + \
+               [("stack 6/64 run r%d" % r, 48, synth.STACK_K, 6, 64, 24, r) for r in synth.STACK_ROWS]
     if name == "decode":
         return [("decode %dx%d r%d" % (N, K, r), N, K, 6, 32, s, r)
                 for (N, K, s) in synth.DECODE_SHAPES for r in synth.DECODE_ROWS]
@@ -61,6 +64,7 @@ WORKLOAD_TEXT = {
     "sweep": "width sweep: N=K=4096, 1 bf16 row, bits {2,3,4,5,6,8} x group {32,64,128} (18 GEMVs a step)",
     "lmhead": "LM head: N=248320, K=2048, 1 row, 6-bit g32 and 4-bit g64 (2 GEMVs a step)",
     "lmhead16": "LM head: N=248320, K=2048, 16 rows, 6-bit g32 and 4-bit g64 (2 GEMVs a step)",
+    "stack": "fused-stack runs: 5-bit g64 6192 x 2048 and 6-bit g64 48 x 2048, rows 1 and 16 (4 GEMVs a step)",
     "decode": "decode windows: 6-bit g32, 12288x2048 and 2048x12288, rows {1,2,3,8,16} (10 GEMVs a step)",
 }
 
