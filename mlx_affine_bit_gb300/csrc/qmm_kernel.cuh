@@ -60,14 +60,18 @@ __device__ __forceinline__ void mbar_arrive_tx(uint64_t *bar, uint32_t tx) {
                  : "memory");
 }
 
+// One test of the phase of `parity`; an incomplete phase suspends the thread
+// until it completes or about SUSPEND_NS pass, so a waiting warp issues few
+// instructions and leaves its scheduler's slots to the warps that compute.
+constexpr uint32_t SUSPEND_NS = 1000000u;
 __device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(SUSPEND_NS)
         : "memory");
     return ok != 0;
 }
@@ -83,7 +87,7 @@ __device__ __forceinline__ void mbar_wait(uint64_t *bar, uint32_t parity, volati
     unsigned long long t0 = global_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try(bar, parity)) return;
-        if ((it & 255u) == 0) {
+        if ((it & 15u) == 0) {
             if (honor_abort && *abort) return;
             if (global_ns() - t0 > WAIT_LIMIT_NS) {
                 *abort = 1;
@@ -353,7 +357,7 @@ struct SegVals<2> {
 template <int BITS, int G, int RB, int MT>
 __device__ __forceinline__ void group_body(const uint32_t *const (&pr)[G / 32],
                                            const uint32_t (&ua)[G / 32], const uint32_t (&ub)[G / 32],
-                                           int woff, const uint4 *bq, const float (&sg)[MT][2],
+                                           uint32_t mg, int woff, const uint4 *bq, const float (&sg)[MT][2],
                                            const float (&bg)[MT][2], const float *sxq,
                                            float (&p)[MT][(RB > 8 ? 2 : 1)][4]) {
     constexpr int NT = RB > 8 ? 2 : 1;
@@ -370,8 +374,8 @@ __device__ __forceinline__ void group_body(const uint32_t *const (&pr)[G / 32],
         for (int t = 0; t < MT; ++t) {
             // A registers in MMA operand order: a[2i] = pair i of row g, a[2i+1] of row g+8.
             uint32_t a[8];
-            Unpack<BITS>::template run<2>(pr[m] + woff + (t * 16) * RW, ua[m], ub[m], a);
-            Unpack<BITS>::template run<2>(pr[m] + woff + (t * 16 + 8) * RW, ua[m], ub[m], a + 1);
+            Unpack<BITS>::template run<2>(pr[m] + woff + (t * 16) * RW, ua[m], ub[m], mg, a);
+            Unpack<BITS>::template run<2>(pr[m] + woff + (t * 16 + 8) * RW, ua[m], ub[m], mg, a + 1);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 if (m == 0)
@@ -421,7 +425,7 @@ __device__ __forceinline__ void store_y(const QmmParams &P, int r, int n, float 
 
 template <int BITS, int G, int RB, int MT>
 __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint64_t *empty,
-                         volatile int *abort, volatile int *flag) {
+                         volatile int *abort, volatile int *flag, const volatile uint32_t *magic) {
     constexpr int NT = RB > 8 ? 2 : 1;
     constexpr int ROWS = TN * MT;
     constexpr int SEGP = Pitch<BITS>::SEGP;
@@ -456,6 +460,7 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
     float yacc[OUTS];
 #pragma unroll
     for (int i = 0; i < OUTS; ++i) yacc[i] = 0.f;
+    const uint32_t mg = *magic;   // MAGIC, read at run time: held in one register
 
     // x, y and the split-K workspace may be touched by the previous kernel of
     // the stream (programmatic dependent launch): wait for it first.
@@ -520,7 +525,7 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                                 sg[t][h] = Sv[t][h].get(gl);
                                 bg[t][h] = Bv[t][h].get(gl);
                             }
-                        group_body<BITS, G, RB, MT>(pr, ua, ub, gl * GW, bq + gl * RUNS * LR * 4, sg, bg,
+                        group_body<BITS, G, RB, MT>(pr, ua, ub, mg, gl * GW, bq + gl * RUNS * LR * 4, sg, bg,
                                                     sxq + gl * LR, p);
                     }
                 } else {
@@ -534,7 +539,7 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                                 sg[t][h] = bf16f(sp[(2 * t + h) * rstep + gl]);
                                 bg[t][h] = bf16f(bp[(2 * t + h) * rstep + gl]);
                             }
-                        group_body<BITS, G, RB, MT>(pr, ua, ub, gl * GW, bq + gl * RUNS * LR * 4, sg, bg,
+                        group_body<BITS, G, RB, MT>(pr, ua, ub, mg, gl * GW, bq + gl * RUNS * LR * 4, sg, bg,
                                                     sxq + gl * LR, p);
                     }
                 }
@@ -620,6 +625,7 @@ __global__ void __launch_bounds__(NTHREADS, MT == 1 ? 2 : 1) qmm_kernel(const __
     uint64_t *empty = full + MAX_STAGES;
     volatile int *abort = reinterpret_cast<volatile int *>(empty + MAX_STAGES);
     volatile int *flag = abort + 1;
+    volatile uint32_t *magic = reinterpret_cast<volatile uint32_t *>(abort + 2);
     if (threadIdx.x == 0) {
         for (int i = 0; i < P.stages; ++i) {
             mbar_init(&full[i], 1);
@@ -627,6 +633,7 @@ __global__ void __launch_bounds__(NTHREADS, MT == 1 ? 2 : 1) qmm_kernel(const __
         }
         *abort = 0;
         *flag = 0;
+        *magic = MAGIC;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -636,7 +643,7 @@ __global__ void __launch_bounds__(NTHREADS, MT == 1 ? 2 : 1) qmm_kernel(const __
     if (threadIdx.x >= NCW * 32)
         producer<BITS, G, MT>(P, smem, full, empty, abort);
     else
-        consumer<BITS, G, RB, MT>(P, smem, full, empty, abort, flag);
+        consumer<BITS, G, RB, MT>(P, smem, full, empty, abort, flag, magic);
 }
 
 // Host-side launcher for one width: every group and row bucket.

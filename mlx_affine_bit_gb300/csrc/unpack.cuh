@@ -10,9 +10,9 @@
 //
 // Method: a code sitting at bit p of a 16-bit half (p + BITS <= 7) is OR-ed
 // into the mantissa of bf16 128.0 (0x4300), giving 128 + c*2^p exactly; one
-// bf16x2 FMA with (2^-p, -128*2^-p) then yields c exactly.  8-bit codes do not
-// fit the 7 mantissa bits: the low 7 bits enter that way and the top bit picks
-// an addend of -128 or 0.
+// bf16x2 add of -128 (p = 0) or one bf16x2 FMA with (2^-p, -128*2^-p) then
+// yields c exactly.  8-bit codes do not fit the 7 mantissa bits: the low 7
+// bits enter that way and the top bit picks an addend of -128 or 0.
 //
 // The header compiles as CUDA device code and as plain host C++ (for the CPU
 // unit test of the extraction); host builds emulate the three device
@@ -104,91 +104,111 @@ TF_HD uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
 #endif
 }
 
+// d = a + b on two bf16 lanes (round to nearest even); exact in every use here.
+TF_HD uint32_t hadd2(uint32_t a, uint32_t b) {
+#if defined(__CUDA_ARCH__)
+    uint32_t d;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+#else
+    return hfma2(a, 0x3F803F80u, b);
+#endif
+}
+
 // bf16x2 constants: 128.0 magic, and (scale, addend) per mantissa position p.
 constexpr uint32_t MAGIC = 0x43004300u;            // 128.0 | 128.0
-constexpr uint32_t ONE2 = 0x3F803F80u;             // 1.0
 constexpr uint32_t NEG128 = 0xC300C300u;           // -128
 constexpr uint32_t Q2 = 0x3E803E80u, NEG32 = 0xC200C200u;   // p=2: 1/4, -32
 constexpr uint32_t Q3 = 0x3E003E00u, NEG16 = 0xC180C180u;   // p=3: 1/8, -16
 constexpr uint32_t Q4 = 0x3D803D80u, NEG8 = 0xC100C100u;    // p=4: 1/16, -8
 
+// Code pair at mantissa position p = 0: (128 + c) - 128.
+TF_HD uint32_t at0(uint32_t u, uint32_t m, uint32_t mg) { return hadd2(mask_or(u, m, mg), NEG128); }
+// Code pair at position p > 0: (128 + c*2^p) * 2^-p - 128*2^-p.
+TF_HD uint32_t atp(uint32_t u, uint32_t m, uint32_t mg, uint32_t q, uint32_t neg) {
+    return hfma2(mask_or(u, m, mg), q, neg);
+}
+
 // Run of 8 codes -> pairs p[i*ST] = (c_i | c_{i+4} << 16) as exact bf16 values.
 // `w` points at the 32-bit word holding the run's first bit; `ua`/`ub` come
 // from lane_args<BITS>(sh) with `sh` that bit's position in the word (they are
-// per-lane constants, computed once).  Reads at most w[0], w[1].
+// per-lane constants, computed once).  `mg` is MAGIC, passed in a register so
+// that each mask-and-insert stays one three-input logic operation.  Reads at
+// most w[0], w[1].
 template <int BITS>
 struct Unpack;
 
 template <>
 struct Unpack<2> {  // 16 bits; sh in {0, 16}
     template <int ST = 1>
-    static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t, uint32_t *p) {
+    static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t, uint32_t mg, uint32_t *p) {
         uint32_t v = w[0] >> sh;
         uint32_t u = halves(v, v << 8);              // c0..c3 @0,2,4,6 | c4..c7 @16,18,20,22
-        p[0 * ST] = hfma2(mask_or(u, 0x00030003u, MAGIC), ONE2, NEG128);
-        p[1 * ST] = hfma2(mask_or(u, 0x000C000Cu, MAGIC), Q2, NEG32);
-        p[2 * ST] = hfma2(mask_or(u, 0x00300030u, MAGIC), Q4, NEG8);
-        p[3 * ST] = hfma2(mask_or(u >> 2, 0x00300030u, MAGIC), Q4, NEG8);
+        p[0 * ST] = at0(u, 0x00030003u, mg);
+        p[1 * ST] = atp(u, 0x000C000Cu, mg, Q2, NEG32);
+        p[2 * ST] = atp(u, 0x00300030u, mg, Q4, NEG8);
+        p[3 * ST] = atp(u >> 2, 0x00300030u, mg, Q4, NEG8);
     }
 };
 
 template <>
 struct Unpack<4> {  // 32 bits; sh == 0
+    // A 4-bit code fits the 7-bit mantissa only at p <= 3: every pair is moved to p = 0.
     template <int ST = 1>
-    static TF_HD void run(const uint32_t *w, uint32_t, uint32_t, uint32_t *p) {
-        uint32_t v = w[0];
-        p[0 * ST] = hfma2(mask_or(v, 0x000F000Fu, MAGIC), ONE2, NEG128);
-        p[1 * ST] = hfma2(mask_or(v >> 4, 0x000F000Fu, MAGIC), ONE2, NEG128);
-        p[2 * ST] = hfma2(mask_or(v >> 8, 0x000F000Fu, MAGIC), ONE2, NEG128);
-        p[3 * ST] = hfma2(mask_or(v >> 12, 0x000F000Fu, MAGIC), ONE2, NEG128);
+    static TF_HD void run(const uint32_t *w, uint32_t, uint32_t, uint32_t mg, uint32_t *p) {
+        uint32_t v = w[0];                           // c0..c3 @0,4,8,12 | c4..c7 @16,20,24,28
+        p[0 * ST] = at0(v, 0x000F000Fu, mg);
+        p[1 * ST] = at0(v >> 4, 0x000F000Fu, mg);
+        p[2 * ST] = at0(v >> 8, 0x000F000Fu, mg);
+        p[3 * ST] = at0(v >> 12, 0x000F000Fu, mg);
     }
 };
 
 template <>
 struct Unpack<8> {  // 64 bits; sh == 0
-    static TF_HD uint32_t one(uint32_t t) {
+    static TF_HD uint32_t one(uint32_t t, uint32_t mg) {
         // t: code a in byte 0, code b in byte 2.
-        uint32_t mant = mask_or(t, 0x007F007Fu, MAGIC);     // 128 + (c & 127)
+        uint32_t mant = mask_or(t, 0x007F007Fu, mg);        // 128 + (c & 127)
         uint32_t sgn = prmt(t, 0u, 0xA484u);                // 0xFF00 per half if c >= 128
         uint32_t add = ~sgn & NEG128;                       // -128 if c < 128, else 0
-        return hfma2(mant, ONE2, add);
+        return hadd2(mant, add);
     }
     template <int ST = 1>
-    static TF_HD void run(const uint32_t *w, uint32_t, uint32_t, uint32_t *p) {
+    static TF_HD void run(const uint32_t *w, uint32_t, uint32_t, uint32_t mg, uint32_t *p) {
         uint32_t lo = w[0], hi = w[1];
-        p[0 * ST] = one(prmt(lo, hi, 0x0400u));   // byte i of lo -> 0, byte i of hi -> 2
-        p[1 * ST] = one(prmt(lo, hi, 0x0501u));
-        p[2 * ST] = one(prmt(lo, hi, 0x0602u));
-        p[3 * ST] = one(prmt(lo, hi, 0x0703u));
+        p[0 * ST] = one(prmt(lo, hi, 0x0400u), mg);   // byte i of lo -> 0, byte i of hi -> 2
+        p[1 * ST] = one(prmt(lo, hi, 0x0501u), mg);
+        p[2 * ST] = one(prmt(lo, hi, 0x0602u), mg);
+        p[3 * ST] = one(prmt(lo, hi, 0x0703u), mg);
     }
 };
 
 template <>
 struct Unpack<3> {  // 24 bits; sh in {0, 8, 16, 24}
     template <int ST = 1>
-    static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t, uint32_t *p) {
+    static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t, uint32_t mg, uint32_t *p) {
         uint32_t v = funnel(w[0], w[1], sh);
         uint32_t u = halves(v, v << 4);   // c0..c3 @0,3,6,9 | c4..c7 @16,19,22,25
-        p[0 * ST] = hfma2(mask_or(u, 0x00070007u, MAGIC), ONE2, NEG128);
-        p[1 * ST] = hfma2(mask_or(u, 0x00380038u, MAGIC), Q3, NEG16);
         uint32_t u2 = u >> 6;             // c2 @0, c3 @3 | c6 @16, c7 @19
-        p[2 * ST] = hfma2(mask_or(u2, 0x00070007u, MAGIC), ONE2, NEG128);
-        p[3 * ST] = hfma2(mask_or(u2, 0x00380038u, MAGIC), Q3, NEG16);
+        p[0 * ST] = at0(u, 0x00070007u, mg);
+        p[1 * ST] = atp(u, 0x00380038u, mg, Q3, NEG16);
+        p[2 * ST] = at0(u2, 0x00070007u, mg);
+        p[3 * ST] = atp(u2, 0x00380038u, mg, Q3, NEG16);
     }
 };
 
 template <>
 struct Unpack<5> {  // 40 bits; sh in {0, 8, 16, 24}
     template <int ST = 1>
-    static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t, uint32_t *p) {
+    static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t, uint32_t mg, uint32_t *p) {
         uint32_t lo = funnel(w[0], w[1], sh);               // run bits 0..31
         uint32_t hi = w[1] >> sh;                           // run bits 32..39 at 0..7
         uint32_t u = halves(lo, funnel(lo, hi, 4));         // c0,c1,c2 @0,5,10 | c4,c5,c6 @16,21,26
-        p[0 * ST] = hfma2(mask_or(u, 0x001F001Fu, MAGIC), ONE2, NEG128);
-        p[1 * ST] = hfma2(mask_or(u >> 5, 0x001F001Fu, MAGIC), ONE2, NEG128);
-        p[2 * ST] = hfma2(mask_or(u >> 10, 0x001F001Fu, MAGIC), ONE2, NEG128);
         uint32_t u3 = halves(lo >> 15, funnel(lo, hi, 19)); // c3 @0 | c7 @16
-        p[3 * ST] = hfma2(mask_or(u3, 0x001F001Fu, MAGIC), ONE2, NEG128);
+        p[0 * ST] = at0(u, 0x001F001Fu, mg);
+        p[1 * ST] = at0(u >> 5, 0x001F001Fu, mg);
+        p[2 * ST] = at0(u >> 10, 0x001F001Fu, mg);
+        p[3 * ST] = at0(u3, 0x001F001Fu, mg);
     }
 };
 
@@ -196,13 +216,13 @@ template <>
 struct Unpack<6> {  // 48 bits; sh in {0, 16}
     // Run bytes {0,1,3,4} and {1,2,4,5}; raw byte = run byte + sh/8 (sh = 0 or 16).
     template <int ST = 1>
-    static TF_HD void run(const uint32_t *w, uint32_t s0, uint32_t s2, uint32_t *p) {
+    static TF_HD void run(const uint32_t *w, uint32_t s0, uint32_t s2, uint32_t mg, uint32_t *p) {
         uint32_t P0 = prmt(w[0], w[1], s0);   // c0 @0, c1 @6 | c4 @16, c5 @22
         uint32_t P2 = prmt(w[0], w[1], s2);   // c2 @4, c3 @10 | c6 @20, c7 @26
-        p[0 * ST] = hfma2(mask_or(P0, 0x003F003Fu, MAGIC), ONE2, NEG128);
-        p[1 * ST] = hfma2(mask_or(P0 >> 6, 0x003F003Fu, MAGIC), ONE2, NEG128);
-        p[2 * ST] = hfma2(mask_or(P2 >> 4, 0x003F003Fu, MAGIC), ONE2, NEG128);
-        p[3 * ST] = hfma2(mask_or(P2 >> 10, 0x003F003Fu, MAGIC), ONE2, NEG128);
+        p[0 * ST] = at0(P0, 0x003F003Fu, mg);
+        p[1 * ST] = at0(P0 >> 6, 0x003F003Fu, mg);
+        p[2 * ST] = at0(P2 >> 4, 0x003F003Fu, mg);
+        p[3 * ST] = at0(P2 >> 10, 0x003F003Fu, mg);
     }
 };
 
