@@ -60,18 +60,19 @@ int check_io(const uint16_t *x, int rows, const float *y) {
 
 struct Plan {
     int nmt, nsl, sl, nchunks, stages, smem, grid, segpitch, sbpitch, stage_bytes, x_off, sx_off,
-        pb_off, z_off, st_off, rb, ctas, mt;
+        pb_off, z_off, st_off, rb, ctas, mt, cg;
     bool sb3d;
 };
 
 int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
-Plan layout(int N, int K, int bits, int group, int rows, int nsm, int ctas, bool sb3d, int mt) {
+Plan layout(int N, int K, int bits, int group, int rows, int nsm, int ctas, bool sb3d, int mt, int cg = 1) {
     Plan p{};
     p.rb = row_bucket(rows);
     p.ctas = ctas;
     p.sb3d = sb3d;
     p.mt = mt;
+    p.cg = cg;
     const int rws = TN * mt;                                // output columns (W rows) per item
     const int xs_max = ctas == 2 ? XS_MAX / 2 : XS_MAX;
     const int budget = ctas == 2 ? SMEM_PER_SM / 2 - 1024 : SMEM_MAX;
@@ -101,7 +102,7 @@ Plan layout(int N, int K, int bits, int group, int rows, int nsm, int ctas, bool
     p.stage_bytes = SEGS * rws * p.segpitch + 2 * rws * p.sbpitch;
     const int x_bytes = (lr * len * 2 + 127) & ~127;
     const int sx_bytes = ((len / group) * lr * 4 + 127) & ~127;
-    const int pb_bytes = 2 * SEGS * rws * lr * 4;
+    const int pb_bytes = cg * 2 * SEGS * rws * lr * 4;
     p.x_off = HDR_BYTES;
     p.sx_off = p.x_off + x_bytes;
     p.pb_off = p.sx_off + sx_bytes;
@@ -115,13 +116,21 @@ Plan layout(int N, int K, int bits, int group, int rows, int nsm, int ctas, bool
 
 // Two m-tiles (32 columns) per item with one CTA per SM when there are at
 // least two such items per SM (shared activation loads, half the per-stage
-// overhead); else one m-tile per item with two CTAs per SM when three stages
-// of each still fit; else one CTA per SM with a deeper ring.  The choice never
-// changes a result's bits.
+// overhead), computed by two consumer groups when the whole K fits one slice
+// and four stages fit (two computed, two in flight); else one m-tile per item
+// with two CTAs per SM when three stages of each still fit; else one CTA per
+// SM with a deeper ring.  The choice never changes a result's bits.
 Plan make_plan(int N, int K, int bits, int group, int rows, int nsm, bool sb3d) {
     if (row_bucket(rows) <= 8) {
         const Plan wide = layout(N, K, bits, group, rows, nsm, 1, sb3d, 2);
-        if (wide.stages >= 3 && (long long)wide.nmt * wide.nsl >= 2LL * nsm) return wide;
+        if (wide.stages >= 3 && (long long)wide.nmt * wide.nsl >= 2LL * nsm) {
+            // Two consumer groups when two stages can be computed with two more in flight.
+            if (wide.nsl == 1) {
+                const Plan pp = layout(N, K, bits, group, rows, nsm, 1, sb3d, 2, 2);
+                if (pp.stages >= 4 && pp.nsl == 1) return pp;
+            }
+            return wide;
+        }
     }
     const Plan two = layout(N, K, bits, group, rows, nsm, 2, sb3d, 1);
     if (two.stages >= 3) return two;
@@ -296,15 +305,15 @@ int stream_ws(cudaStream_t st, size_t floats, size_t counters, StreamWs **out) {
     return TF_OK;
 }
 
-cudaError_t launch(int bits, int group, int rb, int mt, const QmmParams &P, int grid, int smem,
+cudaError_t launch(int bits, int group, int rb, int mt, int cg, const QmmParams &P, int grid, int smem,
                    cudaStream_t st, bool pdl) {
     switch (bits) {
-        case 2: return launch_b2(group, rb, mt, P, grid, smem, st, pdl);
-        case 3: return launch_b3(group, rb, mt, P, grid, smem, st, pdl);
-        case 4: return launch_b4(group, rb, mt, P, grid, smem, st, pdl);
-        case 5: return launch_b5(group, rb, mt, P, grid, smem, st, pdl);
-        case 6: return launch_b6(group, rb, mt, P, grid, smem, st, pdl);
-        case 8: return launch_b8(group, rb, mt, P, grid, smem, st, pdl);
+        case 2: return launch_b2(group, rb, mt, cg, P, grid, smem, st, pdl);
+        case 3: return launch_b3(group, rb, mt, cg, P, grid, smem, st, pdl);
+        case 4: return launch_b4(group, rb, mt, cg, P, grid, smem, st, pdl);
+        case 5: return launch_b5(group, rb, mt, cg, P, grid, smem, st, pdl);
+        case 6: return launch_b6(group, rb, mt, cg, P, grid, smem, st, pdl);
+        case 8: return launch_b8(group, rb, mt, cg, P, grid, smem, st, pdl);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -321,6 +330,7 @@ int run_product(const uint16_t *x, int rows, int K, const uint32_t *W, const uin
     const bool bulk = aligned(s, 16) && aligned(b, 16) && K % SEG == 0 && K % (8 * group) == 0;
     const bool sb3d = bulk && K % CHUNK == 0;
     const Plan pl = make_plan(N, K, bits, group, rows, d->nsm, sb3d);
+    if (pl.cg > 1 && pl.nsl != 1) return fail(TF_EINVAL_SIZE, "internal: two consumer groups need one K slice");
     QmmParams P{};
     P.x = x;
     P.W = W;
@@ -367,7 +377,7 @@ int run_product(const uint16_t *x, int rows, int K, const uint32_t *W, const uin
     }
     const int mode = g_launch_mode.load(std::memory_order_relaxed);
     P.early_w = (mode & TF_LAUNCH_EARLY_WEIGHTS) != 0;
-    const cudaError_t e = launch(bits, group, pl.rb, pl.mt, P, pl.grid, pl.smem, st,
+    const cudaError_t e = launch(bits, group, pl.rb, pl.mt, pl.cg, P, pl.grid, pl.smem, st,
                                  (mode & (TF_LAUNCH_PDL | TF_LAUNCH_EARLY_WEIGHTS)) != 0);
     if (e != cudaSuccess) return cuda_fail(e, "qmm kernel launch");
     return TF_OK;
@@ -486,7 +496,7 @@ int tfq::product_with_scratch(const uint16_t *x, int rows, int K, const uint32_t
         P.ws = ws;
         P.counters = counters;
     }
-    e = launch(bits, group, pl.rb, pl.mt, P, pl.grid, pl.smem, st, false);
+    e = launch(bits, group, pl.rb, pl.mt, pl.cg, P, pl.grid, pl.smem, st, false);
     if (e != cudaSuccess) return cuda_fail(e, "qmm kernel launch");
     return TF_OK;
 }

@@ -10,17 +10,17 @@
 namespace tfq {
 
 // Defined in qmm_b<BITS>.cu, one translation unit per width.
-cudaError_t launch_b2(int group, int rb, int mt, const QmmParams &P, int grid, int smem,
+cudaError_t launch_b2(int group, int rb, int mt, int cg, const QmmParams &P, int grid, int smem,
                       cudaStream_t st, bool pdl);
-cudaError_t launch_b3(int group, int rb, int mt, const QmmParams &P, int grid, int smem,
+cudaError_t launch_b3(int group, int rb, int mt, int cg, const QmmParams &P, int grid, int smem,
                       cudaStream_t st, bool pdl);
-cudaError_t launch_b4(int group, int rb, int mt, const QmmParams &P, int grid, int smem,
+cudaError_t launch_b4(int group, int rb, int mt, int cg, const QmmParams &P, int grid, int smem,
                       cudaStream_t st, bool pdl);
-cudaError_t launch_b5(int group, int rb, int mt, const QmmParams &P, int grid, int smem,
+cudaError_t launch_b5(int group, int rb, int mt, int cg, const QmmParams &P, int grid, int smem,
                       cudaStream_t st, bool pdl);
-cudaError_t launch_b6(int group, int rb, int mt, const QmmParams &P, int grid, int smem,
+cudaError_t launch_b6(int group, int rb, int mt, int cg, const QmmParams &P, int grid, int smem,
                       cudaStream_t st, bool pdl);
-cudaError_t launch_b8(int group, int rb, int mt, const QmmParams &P, int grid, int smem,
+cudaError_t launch_b8(int group, int rb, int mt, int cg, const QmmParams &P, int grid, int smem,
                       cudaStream_t st, bool pdl);
 
 // Product whose split-K scratch and status word the caller provides (api.cu).

@@ -1,10 +1,10 @@
-// qmm_b8.cu -- kernel instantiations for 8-bit codes (groups 32/64/128, row buckets 1/2/4/8/16, 1 or 2 m-tiles per item).
+// qmm_b8.cu -- kernel instantiations for 8-bit codes (groups 32/64/128, row buckets 1/2/4/8/16, 1 or 2 m-tiles per item, 1 or 2 consumer groups).
 #include "internal.h"
 #include "qmm_kernel.cuh"
 
 namespace tfq {
-cudaError_t launch_b8(int group, int rb, int mt, const QmmParams &P, int grid, int smem,
+cudaError_t launch_b8(int group, int rb, int mt, int cg, const QmmParams &P, int grid, int smem,
                       cudaStream_t st, bool pdl) {
-    return launch_width<8>(group, rb, mt, P, grid, smem, st, pdl);
+    return launch_width<8>(group, rb, mt, cg, P, grid, smem, st, pdl);
 }
 }  // namespace tfq

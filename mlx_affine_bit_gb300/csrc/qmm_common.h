@@ -21,7 +21,8 @@ constexpr int CHUNK = 2048;
 constexpr int SEGS = CHUNK / SEG;          // segments per chunk = consumer warps
 constexpr int TN = 16;                     // output columns per work item (one mma m-tile)
 constexpr int NCW = SEGS;                  // consumer warps: one segment of a stage each
-constexpr int NTHREADS = (NCW + 1) * 32;   // + one producer warp
+// Threads of a CTA with `cg` consumer groups of NCW warps, plus one producer warp.
+TFQ_HD constexpr int block_threads(int cg) { return (cg * NCW + 1) * 32; }
 constexpr int MAXCOLSEG = 16;              // column-map segments (stack members) per run
 constexpr int MAX_STAGES = 8;
 constexpr int XS_MAX = 64 * 1024;          // bytes of permuted x a CTA keeps resident

@@ -139,8 +139,9 @@ __device__ __forceinline__ void mma_bf16_first(float c[4], uint32_t a0, uint32_t
 
 __device__ __forceinline__ float bf16f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
 
-__device__ __forceinline__ void named_bar_consumers() {
-    asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory");
+// Named barrier `id` over `n` threads (id 0 is __syncthreads).
+__device__ __forceinline__ void named_bar(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
 // ---------------------------------------------------------- item walking --
@@ -289,11 +290,11 @@ __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
 // first step as {(x0,x4),(x1,x5)} and its second as {(x2,x6),(x3,x7)}.
 // sum_group(x) is the sequential fp32 sum of the group's x in k order, from 0.
 template <int G, int RB>
-__device__ void load_x_slice(const QmmParams &P, const Item &I, uint4 *Bf, float *sx, int tid) {
+__device__ void load_x_slice(const QmmParams &P, const Item &I, uint4 *Bf, float *sx, int tid, int nthr) {
     static_assert(RB >= 2, "layout rows");
     const int rows = P.rows;
     const int ngs = (I.k_hi - I.k_lo) / G;
-    for (int u = tid; u < RB * ngs; u += NCW * 32) {
+    for (int u = tid; u < RB * ngs; u += nthr) {
         const int r = u / ngs, gs = u - r * ngs;
         float acc = 0.f;
         const uint16_t *src = P.x + (long long)r * P.K + I.k_lo + gs * G;
@@ -357,7 +358,7 @@ struct SegVals<2> {
 template <int BITS, int G, int RB, int MT>
 __device__ __forceinline__ void group_body(const uint32_t *const (&pr)[G / 32],
                                            const uint32_t (&ua)[G / 32], const uint32_t (&ub)[G / 32],
-                                           uint32_t mg, int woff, const uint4 *bq, const float (&sg)[MT][2],
+                                           uint32_t mg, uint32_t mq, int woff, const uint4 *bq, const float (&sg)[MT][2],
                                            const float (&bg)[MT][2], const float *sxq,
                                            float (&p)[MT][(RB > 8 ? 2 : 1)][4]) {
     constexpr int NT = RB > 8 ? 2 : 1;
@@ -374,8 +375,8 @@ __device__ __forceinline__ void group_body(const uint32_t *const (&pr)[G / 32],
         for (int t = 0; t < MT; ++t) {
             // A registers in MMA operand order: a[2i] = pair i of row g, a[2i+1] of row g+8.
             uint32_t a[8];
-            Unpack<BITS>::template run<2>(pr[m] + woff + (t * 16) * RW, ua[m], ub[m], mg, a);
-            Unpack<BITS>::template run<2>(pr[m] + woff + (t * 16 + 8) * RW, ua[m], ub[m], mg, a + 1);
+            Unpack<BITS>::template run<2>(pr[m] + woff + (t * 16) * RW, ua[m], ub[m], mg, mq, a);
+            Unpack<BITS>::template run<2>(pr[m] + woff + (t * 16 + 8) * RW, ua[m], ub[m], mg, mq, a + 1);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 if (m == 0)
@@ -423,7 +424,13 @@ __device__ __forceinline__ void store_y(const QmmParams &P, int r, int n, float 
     }
 }
 
-template <int BITS, int G, int RB, int MT>
+// Consumer group `cg` of CG (eight warps each; warp w of a group takes segment
+// w of a stage) computes every CG-th item of this CTA's walk, starting at item
+// cg, and steps the ring over the other groups' stages without waiting on
+// them; each ring slot is consumed by exactly one group.  With CG = 2 two
+// stages are computed at once (twice the warps to hide unpack latency) while
+// the activations stay shared: the plan gives CG = 2 only a single K slice.
+template <int BITS, int G, int RB, int MT, int CG>
 __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint64_t *empty,
                          volatile int *abort, volatile int *flag, const volatile uint32_t *magic) {
     constexpr int NT = RB > 8 ? 2 : 1;
@@ -435,19 +442,23 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
     constexpr int NGS = SEG / G;             // groups per segment
     constexpr int LR = layout_rows(RB);      // rows of the B / sum_group(x) layouts
     constexpr int NOUT = ROWS * LR;          // outputs of an item (padded rows)
-    constexpr int OUTS = (NOUT + NCW * 32 - 1) / (NCW * 32);   // outputs folded per thread
+    constexpr int GT = NCW * 32;             // threads of one consumer group
+    constexpr int OUTS = (NOUT + GT - 1) / GT;   // outputs folded per thread
     const int tid = threadIdx.x;
-    const int warp = tid >> 5, lane = tid & 31;
+    const int cg = CG == 1 ? 0 : tid / GT;
+    const int gtid = tid - cg * GT;          // thread within the group
+    const int warp = gtid >> 5, lane = tid & 31;
     const int g = lane >> 2, q = lane & 3;
     const int S = P.stages, rows = P.rows;
+    const int gbar = 2 + cg;                 // the group's named barrier (1: all consumers)
     uint4 *Bf = reinterpret_cast<uint4 *>(smem + P.x_off);
     float *sx = reinterpret_cast<float *>(smem + P.sx_off);
-    float *pbuf = reinterpret_cast<float *>(smem + P.pb_off);   // [2][SEGS][ROWS][LR]
+    float *pbuf = reinterpret_cast<float *>(smem + P.pb_off) + cg * (2 * SEGS * ROWS * LR);   // [2][SEGS][ROWS][LR]
     const uint8_t *zero = smem + P.z_off;
     // Lanes past the bucket's rows read a zero block instead of B / sum_group(x).
     const bool b_lane = g < LR, sx_lane = 2 * q < LR;
     if (LR < 8) {
-        for (int i = tid; i < ZERO_BYTES / 4; i += NCW * 32) reinterpret_cast<uint32_t *>(smem + P.z_off)[i] = 0u;
+        for (int i = tid; i < ZERO_BYTES / 4; i += CG * GT) reinterpret_cast<uint32_t *>(smem + P.z_off)[i] = 0u;
     }
     // This lane's runs inside any group: word offset and unpack arguments of run m.
     uint32_t wo[RUNS], ua[RUNS], ub[RUNS];
@@ -460,21 +471,27 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
     float yacc[OUTS];
 #pragma unroll
     for (int i = 0; i < OUTS; ++i) yacc[i] = 0.f;
-    const uint32_t mg = *magic;   // MAGIC, read at run time: held in one register
+    const uint32_t mg = magic[0], mq = magic[1];   // MAGIC, QP<BITS>: read at run time, held in registers
 
     // x, y and the split-K workspace may be touched by the previous kernel of
     // the stream (programmatic dependent launch): wait for it first.
     grid_dependency_wait();
     int cur_slice = -1;
-    uint32_t it = 0;
+    uint32_t it = 0;                         // stages this group has computed
     Ring ring;
-    for (ItemWalk iw(P); iw.more(P); iw.next(P)) {
+    int own = 0;                             // position of the item in this CTA's walk
+    for (ItemWalk iw(P); iw.more(P); iw.next(P), ++own) {
         const Item I = iw.get(P);
         if (I.slice != cur_slice) {
-            named_bar_consumers();
-            load_x_slice<G, LR>(P, I, Bf, sx, tid);
-            named_bar_consumers();
+            // Every group walks every item, so all consumers meet here.
+            named_bar(1, CG * GT);
+            load_x_slice<G, LR>(P, I, Bf, sx, tid, CG * GT);
+            named_bar(1, CG * GT);
             cur_slice = I.slice;
+        }
+        if (CG > 1 && (own % CG) != cg) {    // another group's item: skip its stages
+            for (int k0 = I.k_lo; k0 < I.k_hi; k0 += CHUNK) ring.next(S);
+            continue;
         }
         const int n0 = I.mt * ROWS;
         for (int k0 = I.k_lo; k0 < I.k_hi; k0 += CHUNK, ++it, ring.next(S)) {
@@ -507,26 +524,33 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                 const uint16_t *bp = reinterpret_cast<const uint16_t *>(sbase + (ROWS + g) * P.sbpitch) + gseg;
                 const int rstep = 8 * P.sbpitch / 2;                     // 8 rows, in bf16 elements
                 if (ng == NGS) {
-                    SegVals<NGS> Sv[MT][2], Bv[MT][2];
+                    // Scales and biases in vector loads of NV groups (fewer live
+                    // registers with two consumer groups).
+                    constexpr int NV = (CG == 2 && NGS == 8) ? 4 : NGS;
 #pragma unroll
-                    for (int t = 0; t < MT; ++t)
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            Sv[t][h].load(sp + (2 * t + h) * rstep);
-                            Bv[t][h].load(bp + (2 * t + h) * rstep);
-                        }
-#pragma unroll
-                    for (int gl = 0; gl < NGS; ++gl) {
-                        float sg[MT][2], bg[MT][2];
+                    for (int g0 = 0; g0 < NGS; g0 += NV) {
+                        SegVals<NV> Sv[MT][2], Bv[MT][2];
 #pragma unroll
                         for (int t = 0; t < MT; ++t)
 #pragma unroll
                             for (int h = 0; h < 2; ++h) {
-                                sg[t][h] = Sv[t][h].get(gl);
-                                bg[t][h] = Bv[t][h].get(gl);
+                                Sv[t][h].load(sp + (2 * t + h) * rstep + g0);
+                                Bv[t][h].load(bp + (2 * t + h) * rstep + g0);
                             }
-                        group_body<BITS, G, RB, MT>(pr, ua, ub, mg, gl * GW, bq + gl * RUNS * LR * 4, sg, bg,
-                                                    sxq + gl * LR, p);
+#pragma unroll
+                        for (int gv = 0; gv < NV; ++gv) {
+                            const int gl = g0 + gv;
+                            float sg[MT][2], bg[MT][2];
+#pragma unroll
+                            for (int t = 0; t < MT; ++t)
+#pragma unroll
+                                for (int h = 0; h < 2; ++h) {
+                                    sg[t][h] = Sv[t][h].get(gv);
+                                    bg[t][h] = Bv[t][h].get(gv);
+                                }
+                            group_body<BITS, G, RB, MT>(pr, ua, ub, mg, mq, gl * GW, bq + gl * RUNS * LR * 4, sg,
+                                                        bg, sxq + gl * LR, p);
+                        }
                     }
                 } else {
 #pragma unroll 1
@@ -539,7 +563,7 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                                 sg[t][h] = bf16f(sp[(2 * t + h) * rstep + gl]);
                                 bg[t][h] = bf16f(bp[(2 * t + h) * rstep + gl]);
                             }
-                        group_body<BITS, G, RB, MT>(pr, ua, ub, mg, gl * GW, bq + gl * RUNS * LR * 4, sg, bg,
+                        group_body<BITS, G, RB, MT>(pr, ua, ub, mg, mq, gl * GW, bq + gl * RUNS * LR * 4, sg, bg,
                                                     sxq + gl * LR, p);
                     }
                 }
@@ -565,13 +589,13 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                         const int c = t * 16 + g + 8 * (e >> 1);
                         if (r < LR) pw[c * LR + r] = p[t][nt][e];
                     }
-            named_bar_consumers();
+            named_bar(gbar, GT);
             // Chunk sum C = P_0 + P_1 + ... in segment order, then the chunk fold.
             const int nseg = (k1 - k0 + SEG - 1) / SEG;
             const int chunk = k0 / CHUNK;
 #pragma unroll
             for (int i = 0; i < OUTS; ++i) {
-                const int o = tid + i * NCW * 32;
+                const int o = gtid + i * GT;
                 if (o < NOUT) {
                     const int fc = o / LR, fr = o - (o / LR) * LR;
                     const float *pf = pbuf + (buf * SEGS * ROWS + fc) * LR + fr;
@@ -586,18 +610,18 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                 }
             }
         }
-        if (P.nsl > 1) {
+        if (CG == 1 && P.nsl > 1) {
             // Split K: the last CTA to finish an item folds its chunk sums in
             // chunk order (an arrival ticket; nothing waits).
             __threadfence();
-            named_bar_consumers();
-            if (tid == 0) *flag = atomicAdd(&P.counters[I.mt], 1) == P.nsl - 1;
-            named_bar_consumers();
+            named_bar(gbar, GT);
+            if (gtid == 0) *flag = atomicAdd(&P.counters[I.mt], 1) == P.nsl - 1;
+            named_bar(gbar, GT);
             if (*flag) {
                 __threadfence();
 #pragma unroll
                 for (int i = 0; i < OUTS; ++i) {
-                    const int o = tid + i * NCW * 32;
+                    const int o = gtid + i * GT;
                     if (o < NOUT) {
                         const int fc = o / LR, fr = o - (o / LR) * LR;
                         if (fr < rows && n0 + fc < P.N) {
@@ -609,8 +633,8 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                         }
                     }
                 }
-                named_bar_consumers();
-                if (tid == 0) P.counters[I.mt] = 0;
+                named_bar(gbar, GT);
+                if (gtid == 0) P.counters[I.mt] = 0;
             }
         }
     }
@@ -618,8 +642,18 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
 
 // ------------------------------------------------------------------ kernel --
 
-template <int BITS, int G, int RB, int MT>
-__global__ void __launch_bounds__(NTHREADS, MT == 1 ? 2 : 1) qmm_kernel(const __grid_constant__ QmmParams P) {
+// Register ceiling per thread.  An SM's 65,536 registers are split evenly
+// over its four schedulers and each warp draws on its scheduler's share, so
+// the busiest scheduler decides: two CTAs of nine warps (MT = 1) or one of
+// 17 warps (CG = 2) put five warps on one scheduler (16,384 / (5 * 32),
+// rounded down to a multiple of 8: 96); one CTA of nine warps puts three (168).
+template <int MT, int CG>
+struct RegCap {
+    static constexpr int value = (CG == 2 || MT == 1) ? 96 : 168;
+};
+
+template <int BITS, int G, int RB, int MT, int CG>
+__global__ void __maxnreg__((RegCap<MT, CG>::value)) qmm_kernel(const __grid_constant__ QmmParams P) {
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + MAX_STAGES;
@@ -633,26 +667,27 @@ __global__ void __launch_bounds__(NTHREADS, MT == 1 ? 2 : 1) qmm_kernel(const __
         }
         *abort = 0;
         *flag = 0;
-        *magic = MAGIC;
+        magic[0] = MAGIC;
+        magic[1] = QP<BITS>::value;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
     // The next kernel of the stream may start its prologue once every CTA of
     // this grid is resident (no effect without programmatic dependent launch).
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (threadIdx.x >= NCW * 32)
+    if (threadIdx.x >= CG * NCW * 32)
         producer<BITS, G, MT>(P, smem, full, empty, abort);
     else
-        consumer<BITS, G, RB, MT>(P, smem, full, empty, abort, flag, magic);
+        consumer<BITS, G, RB, MT, CG>(P, smem, full, empty, abort, flag, magic);
 }
 
 // Host-side launcher for one width: every group and row bucket.
 template <int BITS>
-cudaError_t launch_width(int group, int rb, int mt, const QmmParams &P, int grid, int smem,
+cudaError_t launch_width(int group, int rb, int mt, int cg, const QmmParams &P, int grid, int smem,
                          cudaStream_t st, bool pdl) {
-#define TFQ_CASE(G_, RB_, MT_)                                                                \
-    if (group == G_ && rb == RB_ && mt == MT_) {                                              \
-        auto k = qmm_kernel<BITS, G_, RB_, MT_>;                                              \
+#define TFQ_CASE(G_, RB_, MT_, CG_)                                                           \
+    if (group == G_ && rb == RB_ && mt == MT_ && cg == CG_) {                                 \
+        auto k = qmm_kernel<BITS, G_, RB_, MT_, CG_>;                                         \
         static unsigned attr_set = 0; /* one bit per device: smem limit raised */             \
         int dev = 0;                                                                          \
         cudaError_t e = cudaGetDevice(&dev);                                                  \
@@ -665,7 +700,7 @@ cudaError_t launch_width(int group, int rb, int mt, const QmmParams &P, int grid
         }                                                                                     \
         cudaLaunchConfig_t cfg = {};                                                          \
         cfg.gridDim = dim3(grid);                                                             \
-        cfg.blockDim = dim3(NTHREADS);                                                        \
+        cfg.blockDim = dim3(block_threads(CG_));                                              \
         cfg.dynamicSmemBytes = smem;                                                          \
         cfg.stream = st;                                                                      \
         cudaLaunchAttribute attr[1];                                                          \
@@ -675,8 +710,10 @@ cudaError_t launch_width(int group, int rb, int mt, const QmmParams &P, int grid
         cfg.numAttrs = pdl ? 1 : 0;                                                           \
         return cudaLaunchKernelEx(&cfg, k, P);                                                \
     }
-#define TFQ_ROWS(G_) TFQ_CASE(G_, 1, 1) TFQ_CASE(G_, 2, 1) TFQ_CASE(G_, 4, 1) TFQ_CASE(G_, 8, 1)      \
-    TFQ_CASE(G_, 16, 1) TFQ_CASE(G_, 1, 2) TFQ_CASE(G_, 2, 2) TFQ_CASE(G_, 4, 2) TFQ_CASE(G_, 8, 2)
+#define TFQ_ROWS(G_) TFQ_CASE(G_, 1, 1, 1) TFQ_CASE(G_, 2, 1, 1) TFQ_CASE(G_, 4, 1, 1) TFQ_CASE(G_, 8, 1, 1) \
+    TFQ_CASE(G_, 16, 1, 1) TFQ_CASE(G_, 1, 2, 1) TFQ_CASE(G_, 2, 2, 1) TFQ_CASE(G_, 4, 2, 1)                \
+    TFQ_CASE(G_, 8, 2, 1) TFQ_CASE(G_, 1, 2, 2) TFQ_CASE(G_, 2, 2, 2) TFQ_CASE(G_, 4, 2, 2)                \
+    TFQ_CASE(G_, 8, 2, 2)
     TFQ_ROWS(32) TFQ_ROWS(64) TFQ_ROWS(128)
 #undef TFQ_ROWS
 #undef TFQ_CASE

@@ -266,3 +266,22 @@ def test_launch_modes_bit_identical(mode):
                 assert torch.equal(a.view(torch.int32), b.view(torch.int32))
     finally:
         tf.tf_set_launch_mode(old)
+
+
+@pytest.mark.parametrize("bits,group", [(2, 128), (3, 32), (4, 64), (5, 32), (5, 128), (6, 32)])
+@pytest.mark.parametrize("rows", [1, 3, 8])
+def test_plans_bit_identical(bits, group, rows):
+    # 12304 columns take the widest plan (two m-tiles per item; two consumer
+    # groups up to 5 bits; an odd item count), slices of 1024 and 1040 columns
+    # the one-m-tile plans: the shared columns agree bit for bit.
+    N, K = 12304, 2048
+    m = synth.make_matrix(N, K, bits, group, 40 + bits, 0.001, 0.03)
+    dm = DevMatrix(m)
+    x = synth.make_x(rows, K, 41 + rows)
+    xd = dev(x)
+    y = run_qmm(dm, xd)
+    for c0, n in ((0, 1024), (N - 1040, 1040)):
+        ys = torch.full((rows, n), float("nan"), dtype=torch.float32, device=DEV)
+        tf.tf_qmm(xd, rows, K, dm.W[c0:c0 + n], dm.s[c0:c0 + n], dm.b[c0:c0 + n], n, bits, group, ys, n)
+        assert torch.equal(ys.view(torch.int32), y[:, c0:c0 + n].contiguous().view(torch.int32)), c0
+    oracle_check(m, x, y.cpu().numpy(), sample_cols(N, 48, bits))

@@ -31,9 +31,9 @@ static int check(std::mt19937 &rng, int sh) {
         uint32_t p[4];
         uint32_t ua, ub;
         tfq::lane_args<BITS>((uint32_t)sh, ua, ub);
-        tfq::Unpack<BITS>::template run<1>(w, ua, ub, tfq::MAGIC, p);
+        tfq::Unpack<BITS>::template run<1>(w, ua, ub, tfq::MAGIC, tfq::QP<BITS>::value, p);
         uint32_t p2[8];
-        tfq::Unpack<BITS>::template run<2>(w, ua, ub, tfq::MAGIC, p2);
+        tfq::Unpack<BITS>::template run<2>(w, ua, ub, tfq::MAGIC, tfq::QP<BITS>::value, p2);
         for (int i = 0; i < 4; ++i) if (p2[2 * i] != p[i]) { printf("stride mismatch\n"); ++bad; }
         for (int i = 0; i < 4; ++i) {
             int lo = bf16_int((uint16_t)(p[i] & 0xFFFF)), hi = bf16_int((uint16_t)(p[i] >> 16));
