@@ -86,8 +86,8 @@ Plan layout(int N, int K, int bits, int group, int rows, int nsm, int ctas, bool
     for (int nsl = 1; nsl <= p.nchunks; ++nsl) {
         const int cps = ceil_div(p.nchunks, nsl);
         if (cps > max_cps || (nsl - 1) * cps >= p.nchunks) continue;
-        const long long items = (long long)p.nmt * nsl;
-        const double cost = (double)ceil_div(items, slots) * (cps + (nsl > 1 ? 0.5 : 0.25)) * ctas;
+        const long long team = std::max(1LL, slots / nsl);    // CTAs per K slice
+        const double cost = (double)ceil_div(p.nmt, team) * (cps + (nsl > 1 ? 0.5 : 0.25)) * ctas;
         if (cost < best) {
             best = cost;
             best_cps = cps;
@@ -110,7 +110,8 @@ Plan layout(int N, int K, int bits, int group, int rows, int nsm, int ctas, bool
     p.st_off = p.z_off + (lr < 8 ? ZERO_BYTES : 0);
     p.stages = std::min(MAX_STAGES, (budget - p.st_off) / p.stage_bytes);
     p.smem = p.st_off + p.stages * p.stage_bytes;
-    p.grid = (int)std::min<long long>((long long)p.nmt * p.nsl, slots);
+    // Whole teams: one team of CTAs per K slice (see ItemWalk).
+    p.grid = p.nsl * (int)std::max(1LL, std::min<long long>(p.nmt, slots / p.nsl));
     return p;
 }
 

@@ -150,15 +150,17 @@ struct Item {
     int mt, slice, k_lo, k_hi;
 };
 
-// This CTA's work items blockIdx.x, blockIdx.x + gridDim.x, ... (slice-major),
-// walked without divisions.
+// This CTA's work items.  The grid is a whole number of teams of
+// gridDim.x / nsl CTAs, one team per K slice: CTA b of team s takes column
+// tiles b, b + team, ... of slice s, so its activations are loaded once.
 struct ItemWalk {
-    int item, mt, slice;
-    __device__ __forceinline__ explicit ItemWalk(const QmmParams &P) : item(blockIdx.x) {
-        slice = blockIdx.x / P.nmt;
-        mt = blockIdx.x - slice * P.nmt;
+    int team, mt, slice;
+    __device__ __forceinline__ explicit ItemWalk(const QmmParams &P) {
+        team = gridDim.x / P.nsl;
+        slice = blockIdx.x / team;
+        mt = blockIdx.x - slice * team;
     }
-    __device__ __forceinline__ bool more(const QmmParams &P) const { return item < P.n_items; }
+    __device__ __forceinline__ bool more(const QmmParams &P) const { return mt < P.nmt; }
     __device__ __forceinline__ Item get(const QmmParams &P) const {
         Item I;
         I.mt = mt;
@@ -167,14 +169,7 @@ struct ItemWalk {
         I.k_hi = min(P.K, I.k_lo + P.sl);
         return I;
     }
-    __device__ __forceinline__ void next(const QmmParams &P) {
-        item += gridDim.x;
-        mt += gridDim.x;
-        while (mt >= P.nmt) {
-            mt -= P.nmt;
-            ++slice;
-        }
-    }
+    __device__ __forceinline__ void next(const QmmParams &) { mt += team; }
 };
 
 // Ring position of the stage sequence: slot and mbarrier phase, no divisions.
