@@ -235,6 +235,9 @@ __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                         tma_2d(bst, &P.tmB, k0 / G, n0, &full[slot]);
                     }
                 }
+                // The CTA's first stage travels alone: every CTA's first stage
+                // lands before later stages compete with it for DRAM.
+                if (it == 0) mbar_wait(&full[slot], ring.phase, abort, P.status);
             } else {
                 // Odd shapes or alignments: plain copies by the warp into the same layout.
                 const int k1 = min(I.k_hi, k0 + CHUNK);
