@@ -120,7 +120,8 @@ Plan layout(int N, int K, int bits, int group, int rows, int nsm, int ctas, bool
 // overhead), computed by two consumer groups when the whole K fits one slice
 // and four stages fit (two computed, two in flight); else one m-tile per item
 // with two CTAs per SM when three stages of each still fit; else one CTA per
-// SM with a deeper ring.  The choice never changes a result's bits.
+// SM with a deeper ring, with two consumer groups for 9-16 rows over many
+// column tiles.  The choice never changes a result's bits.
 Plan make_plan(int N, int K, int bits, int group, int rows, int nsm, bool sb3d) {
     if (row_bucket(rows) <= 8) {
         const Plan wide = layout(N, K, bits, group, rows, nsm, 1, sb3d, 2);
@@ -135,7 +136,14 @@ Plan make_plan(int N, int K, int bits, int group, int rows, int nsm, bool sb3d) 
     }
     const Plan two = layout(N, K, bits, group, rows, nsm, 2, sb3d, 1);
     if (two.stages >= 3) return two;
-    return layout(N, K, bits, group, rows, nsm, 1, sb3d, 1);
+    const Plan one = layout(N, K, bits, group, rows, nsm, 1, sb3d, 1);
+    if (row_bucket(rows) == 16 && one.nsl == 1 && (long long)one.nmt >= 2LL * nsm) {
+        // Nine to sixteen rows over many column tiles: two consumer groups
+        // (their compute per stage is long enough that one stage in flight keeps up).
+        const Plan pp = layout(N, K, bits, group, rows, nsm, 1, sb3d, 1, 2);
+        if (pp.stages >= 3 && pp.nsl == 1) return pp;
+    }
+    return one;
 }
 
 // ------------------------------------------------------------ TMA maps --

@@ -269,11 +269,12 @@ def test_launch_modes_bit_identical(mode):
 
 
 @pytest.mark.parametrize("bits,group", [(2, 128), (3, 32), (4, 64), (5, 32), (5, 128), (6, 32)])
-@pytest.mark.parametrize("rows", [1, 3, 8])
+@pytest.mark.parametrize("rows", [1, 3, 8, 16])
 def test_plans_bit_identical(bits, group, rows):
-    # 12304 columns take the widest plan (two m-tiles per item; two consumer
-    # groups up to 5 bits; an odd item count), slices of 1024 and 1040 columns
-    # the one-m-tile plans: the shared columns agree bit for bit.
+    # 12304 columns take the widest plan (two m-tiles per item, or one with 16
+    # rows; two consumer groups where the stages fit; an odd item count),
+    # slices of 1024 and 1040 columns the one-m-tile, two-CTA plans: the shared
+    # columns agree bit for bit.
     N, K = 12304, 2048
     m = synth.make_matrix(N, K, bits, group, 40 + bits, 0.001, 0.03)
     dm = DevMatrix(m)
