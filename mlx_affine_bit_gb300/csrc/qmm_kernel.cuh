@@ -137,6 +137,17 @@ __device__ __forceinline__ void mma_bf16_first(float c[4], uint32_t a0, uint32_t
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
 
+// {d0, d1} = {a0 * b0 + d0, a1 * b1 + d1}: one fp32x2 FMA, each lane rounded
+// exactly as fmaf.
+__device__ __forceinline__ void fma2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+    unsigned long long A, B, D;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(B) : "f"(b0), "f"(b1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(D) : "f"(d0), "f"(d1));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(D) : "l"(A), "l"(B));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(D));
+}
+
 __device__ __forceinline__ float bf16f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
 
 // Named barrier `id` over `n` threads (id 0 is __syncthreads).
@@ -392,16 +403,16 @@ __device__ __forceinline__ void group_body(const uint32_t *const (&pr)[G / 32],
             p[t][0][0] = fmaf(bg[t][0], x0, fmaf(sg[t][0], c[t][0][0], p[t][0][0]));
             p[t][0][2] = fmaf(bg[t][1], x0, fmaf(sg[t][1], c[t][0][2], p[t][0][2]));
         }
-    } else {
+    } else {   // the two activation rows of a lane in one packed fp32x2 FMA each
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const float2 v = *reinterpret_cast<const float2 *>(sxq + nt * 8);
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
-                p[t][nt][0] = fmaf(bg[t][0], v.x, fmaf(sg[t][0], c[t][nt][0], p[t][nt][0]));
-                p[t][nt][1] = fmaf(bg[t][0], v.y, fmaf(sg[t][0], c[t][nt][1], p[t][nt][1]));
-                p[t][nt][2] = fmaf(bg[t][1], v.x, fmaf(sg[t][1], c[t][nt][2], p[t][nt][2]));
-                p[t][nt][3] = fmaf(bg[t][1], v.y, fmaf(sg[t][1], c[t][nt][3], p[t][nt][3]));
+                fma2(p[t][nt][0], p[t][nt][1], sg[t][0], sg[t][0], c[t][nt][0], c[t][nt][1]);
+                fma2(p[t][nt][0], p[t][nt][1], bg[t][0], bg[t][0], v.x, v.y);
+                fma2(p[t][nt][2], p[t][nt][3], sg[t][1], sg[t][1], c[t][nt][2], c[t][nt][3]);
+                fma2(p[t][nt][2], p[t][nt][3], bg[t][1], bg[t][1], v.x, v.y);
             }
         }
     }
