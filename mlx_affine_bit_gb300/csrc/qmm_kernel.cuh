@@ -441,7 +441,7 @@ __device__ __forceinline__ void store_y(const QmmParams &P, int r, int n, float 
 // the activations stay shared: the plan gives CG = 2 only a single K slice.
 template <int BITS, int G, int RB, int MT, int CG>
 __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint64_t *empty,
-                         volatile int *abort, volatile int *flag, const volatile uint32_t *magic) {
+                         volatile int *abort, const volatile uint32_t *magic) {
     constexpr int NT = RB > 8 ? 2 : 1;
     constexpr int ROWS = TN * MT;
     constexpr int SEGP = Pitch<BITS>::SEGP;
@@ -619,15 +619,31 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                 }
             }
         }
-        if (CG == 1 && P.nsl > 1) {
-            // Split K: the last CTA to finish an item folds its chunk sums in
-            // chunk order (an arrival ticket; nothing waits).
+    }
+    if (CG == 1 && P.nsl > 1) {
+        // Split K: once all of this CTA's chunk sums are out, one arrival ticket
+        // per item, issued together; the last CTA to arrive at an item folds its
+        // chunk sums in chunk order and rearms the counter.  Nothing waits on
+        // another CTA.  The flags reuse the partial-sum buffer.
+        int *last = reinterpret_cast<int *>(pbuf);
+        const int team = gridDim.x / P.nsl;
+        const int mt0 = blockIdx.x % team;                  // this CTA's first column tile
+        const int nmine = mt0 < P.nmt ? (P.nmt - mt0 + team - 1) / team : 0;
+        __threadfence();
+        named_bar(gbar, GT);
+        for (int b0 = 0; b0 < nmine; b0 += GT) {
+            const int nb = min(GT, nmine - b0);
+            if (gtid < nb) {
+                const int mt = mt0 + (b0 + gtid) * team;
+                const int lst = atomicAdd(&P.counters[mt], 1) == P.nsl - 1;
+                if (lst) P.counters[mt] = 0;                // no other arrival in this launch
+                last[gtid] = lst;
+            }
+            named_bar(gbar, GT);
             __threadfence();
-            named_bar(gbar, GT);
-            if (gtid == 0) *flag = atomicAdd(&P.counters[I.mt], 1) == P.nsl - 1;
-            named_bar(gbar, GT);
-            if (*flag) {
-                __threadfence();
+            for (int j = 0; j < nb; ++j) {
+                if (!last[j]) continue;                      // the same for the whole group
+                const int n0 = (mt0 + (b0 + j) * team) * ROWS;
 #pragma unroll
                 for (int i = 0; i < OUTS; ++i) {
                     const int o = gtid + i * GT;
@@ -642,9 +658,8 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                         }
                     }
                 }
-                named_bar(gbar, GT);
-                if (gtid == 0) P.counters[I.mt] = 0;
             }
+            named_bar(gbar, GT);                             // before the flags are rewritten
         }
     }
 }
@@ -667,7 +682,6 @@ __global__ void __maxnreg__((RegCap<MT, CG>::value)) qmm_kernel(const __grid_con
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + MAX_STAGES;
     volatile int *abort = reinterpret_cast<volatile int *>(empty + MAX_STAGES);
-    volatile int *flag = abort + 1;
     volatile uint32_t *magic = reinterpret_cast<volatile uint32_t *>(abort + 2);
     if (threadIdx.x == 0) {
         for (int i = 0; i < P.stages; ++i) {
@@ -675,7 +689,6 @@ __global__ void __maxnreg__((RegCap<MT, CG>::value)) qmm_kernel(const __grid_con
             mbar_init(&empty[i], NCW);
         }
         *abort = 0;
-        *flag = 0;
         magic[0] = MAGIC;
         magic[1] = QP<BITS>::value;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -687,7 +700,7 @@ __global__ void __maxnreg__((RegCap<MT, CG>::value)) qmm_kernel(const __grid_con
     if (threadIdx.x >= CG * NCW * 32)
         producer<BITS, G, MT>(P, smem, full, empty, abort);
     else
-        consumer<BITS, G, RB, MT, CG>(P, smem, full, empty, abort, flag, magic);
+        consumer<BITS, G, RB, MT, CG>(P, smem, full, empty, abort, magic);
 }
 
 // Host-side launcher for one width: every group and row bucket.
