@@ -51,9 +51,9 @@ def workload_cases(name: str):
     if name == "lmhead16":
         return [("lmhead %d/%d r16" % (b, g), synth.LMHEAD_N, synth.LMHEAD_K, b, g, s, 16)
                 for (b, g, s) in synth.LMHEAD_CASES]
-    if name == "stack":
-        return [("stack 5/64 run r%d" % r, 6192, synth.STACK_K, 5, 64, 21, r) for r in synth.STACK_ROWS] + \
-               [("stack 6/64 run r%d" % r, 48, synth.STACK_K, 6, 64, 24, r) for r in synth.STACK_ROWS]
+    if name == "stack":   # the members (the GPU arm runs them as one fused stack per row count)
+        return [("stack member %d/%d r%d" % (m.bits, m.group, r), m.n_cols, synth.STACK_K, m.bits, m.group, m.seed, r)
+                for r in synth.STACK_ROWS for m in synth.STACK_MEMBERS]
     if name == "decode":
         return [("decode %dx%d r%d" % (N, K, r), N, K, 6, 32, s, r)
                 for (N, K, s) in synth.DECODE_SHAPES for r in synth.DECODE_ROWS]
@@ -64,7 +64,9 @@ WORKLOAD_TEXT = {
     "sweep": "width sweep: N=K=4096, 1 bf16 row, bits {2,3,4,5,6,8} x group {32,64,128} (18 GEMVs a step)",
     "lmhead": "LM head: N=248320, K=2048, 1 row, 6-bit g32 and 4-bit g64 (2 GEMVs a step)",
     "lmhead16": "LM head: N=248320, K=2048, 16 rows, 6-bit g32 and 4-bit g64 (2 GEMVs a step)",
-    "stack": "fused-stack runs: 5-bit g64 6192 x 2048 and 6-bit g64 48 x 2048, rows 1 and 16 (4 GEMVs a step)",
+    "stack": "fused mixed-width stack, K=2048: members 4/g64 4096, 5/g128 2048, 5/g128 48, 6/g64 48 "
+             "widened to a 5-bit g64 run of 6192 columns and a 6-bit g64 run of 48, one tf_qmm_stack "
+             "into a 6240-column strided output; rows 1 and 16 (2 stacks a step)",
     "decode": "decode windows: 6-bit g32, 12288x2048 and 2048x12288, rows {1,2,3,8,16} (10 GEMVs a step)",
 }
 
@@ -162,6 +164,48 @@ def run_reference(args, cases):
     }))
 
 
+def stack_items(cases, dev, tf):
+    """One fused stack per row count: members 0-2 widened on the device to a
+    5-bit g64 run of 6192 columns, member 3 a 6-bit g64 run of 48 columns,
+    written through the member column map into one 6240-column output."""
+    import torch
+    K = synth.STACK_K
+    mats = synth.stack_member_matrices()
+
+    def to_dev(a, dt):
+        return torch.from_numpy(a.view(dt)).to(dev)
+
+    parts = []
+    for m in mats[:3]:
+        Wo = torch.zeros((m.N, K * 5 // 32), dtype=torch.int32, device=dev)
+        so = torch.zeros((m.N, K // 64), dtype=torch.int16, device=dev)
+        bo = torch.zeros_like(so)
+        tf.tf_widen(to_dev(m.W, np.int32), to_dev(m.scales, np.int16), to_dev(m.biases, np.int16),
+                    m.N, K, m.bits, m.group, Wo, so, bo, 5, 64)
+        parts.append((Wo, so, bo))
+    W5 = torch.cat([q[0] for q in parts]).contiguous()
+    s5 = torch.cat([q[1] for q in parts]).contiguous()
+    b5 = torch.cat([q[2] for q in parts]).contiguous()
+    m6 = mats[3]
+    runs = ((W5, s5, b5, 6192, 5, 64),
+            (to_dev(m6.W, np.int32), to_dev(m6.scales, np.int16), to_dev(m6.biases, np.int16), 48, 6, 64))
+    members = [(0, 0, 4096, 0), (0, 4096, 2048, 4096), (0, 6144, 48, 6144), (1, 0, 48, 6192)]
+    stride = 6240
+    items, per_step = [], 0
+    for rows in synth.STACK_ROWS:
+        nb = (synth.algorithmic_bytes(6192, K, 5, 64, rows) + synth.algorithmic_bytes(48, K, 6, 64, rows)
+              - rows * K * 2)                          # x is read once
+        x_h = synth.make_x(rows, K, 60 + rows)
+        items.append(dict(label="stack r%d" % rows, N=stride, K=K, rows=rows, stack=True, members=members,
+                          reps=[runs], x=torch.from_numpy(x_h.view(np.int16)).to(dev),
+                          y=torch.empty((rows, stride), dtype=torch.float32, device=dev),
+                          x_pin=torch.from_numpy(x_h.view(np.int16)).pin_memory(),
+                          y_pin=torch.empty((rows, stride), dtype=torch.float32).pin_memory(), bytes=nb))
+        per_step += nb
+    torch.cuda.synchronize()
+    return items, per_step
+
+
 def run_gpu(args, cases):
     import torch
     import torch.distributed as dist
@@ -187,9 +231,18 @@ def run_gpu(args, cases):
 
     # Device-resident inputs; enough weight copies that a buffer is reused only
     # after >= 4 L2 sizes of other traffic.
-    per_step = sum(synth.algorithmic_bytes(N, K, b, g, r) for (_, N, K, b, g, _, r) in cases)
-    copies = max(1, -(-4 * L2_BYTES // per_step))
-    items = []
+    cpu_cases = list(cases)                  # the oracle baseline runs on the members
+    if args.workload == "stack":
+        items, per_step = stack_items(cases, dev, tf)
+        copies = max(1, -(-4 * L2_BYTES // per_step))
+        for it in items:
+            it["reps"] += [tuple((W.clone(), sc.clone(), bc.clone(), N, b, g) for (W, sc, bc, N, b, g) in it["reps"][0])
+                           for _ in range(copies - 1)]
+        cases = []
+    else:
+        per_step = sum(synth.algorithmic_bytes(N, K, b, g, r) for (_, N, K, b, g, _, r) in cases)
+        copies = max(1, -(-4 * L2_BYTES // per_step))
+        items = []
     for (label, N, K, bits, group, seed, rows) in cases:
         m = synth.make_matrix(N, K, bits, group, seed, 0.001, 0.03 if N < 100000 else 0.02)
         W = torch.from_numpy(m.W.view(np.int32)).to(dev)
@@ -207,6 +260,10 @@ def run_gpu(args, cases):
     torch.cuda.synchronize()
 
     def launch(it, c, st):
+        if it.get("stack"):
+            tf.tf_qmm_stack(it["x"], it["rows"], it["K"], it["reps"][c % len(it["reps"])], it["members"],
+                            it["y"], it["N"], st)
+            return
         W, s, b = it["reps"][c % len(it["reps"])]
         tf.tf_qmm(it["x"], it["rows"], it["K"], W, s, b, it["N"], it["bits"], it["group"], it["y"],
                   it["N"], st)
@@ -323,9 +380,9 @@ def run_gpu(args, cases):
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
             cores = os.cpu_count() or 1
-            gbs, secs, nb = cpu_sample(cases, 1, cores)          # probe
+            gbs, secs, nb = cpu_sample(cpu_cases, 1, cores)      # probe
             cols = max(1, min(4096, int(12.0 / max(secs, 1e-3))))
-            gbs, secs, nb = cpu_sample(cases, cols, cores)
+            gbs, secs, nb = cpu_sample(cpu_cases, cols, cores)
             cpu = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
                    "sample": "fp64 oracle on the first %d output columns of each product (%.1f s)" % (cols, secs)}
         print(json.dumps({
@@ -346,7 +403,7 @@ def run_gpu(args, cases):
             "cpu_baseline": cpu,
             "e2e": {"value": per_step * e2e_steps / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": n * args.steps,
+            "gpu_launches": sum(len(it["reps"][0]) if it.get("stack") else 1 for it in items) * args.steps,
             "timing": "CUDA graph of %d steps replayed %d times; per-product launch time from its own graph "
                       "over >= 4 L2 sizes of weight copies" % (copies, replays),
             "clocks": clocks,

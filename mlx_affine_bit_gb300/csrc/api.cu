@@ -331,7 +331,7 @@ cudaError_t launch(int bits, int group, int rb, int mt, int cg, const QmmParams 
 int run_product(const uint16_t *x, int rows, int K, const uint32_t *W, const uint16_t *s,
                 const uint16_t *b, int N, int bits, int group, float *y, int64_t y_stride,
                 int nseg, const int *seg_src, const int *seg_len, const int *seg_dst,
-                cudaStream_t st) {
+                cudaStream_t st, int stack_pos = -1) {
     std::lock_guard<std::mutex> lk(g_mu);
     DevState *d = nullptr;
     int rc = dev_state(&d);
@@ -386,6 +386,9 @@ int run_product(const uint16_t *x, int rows, int K, const uint32_t *W, const uin
     }
     const int mode = g_launch_mode.load(std::memory_order_relaxed);
     P.early_w = (mode & TF_LAUNCH_EARLY_WEIGHTS) != 0;
+    // Runs of a stack read x and write disjoint columns: after the first, a run
+    // without split-K overlaps the runs before it (see QmmParams::dep).
+    P.dep = stack_pos < 0 ? 0 : stack_pos == 0 ? 1 : pl.nsl == 1 ? 2 : 0;
     const cudaError_t e = launch(bits, group, pl.rb, pl.mt, pl.cg, P, pl.grid, pl.smem, st,
                                  (mode & (TF_LAUNCH_PDL | TF_LAUNCH_EARLY_WEIGHTS)) != 0);
     if (e != cudaSuccess) return cuda_fail(e, "qmm kernel launch");
@@ -558,6 +561,7 @@ int tf_qmm_stack(const uint16_t *x, int rows, int K, const tf_run *runs, int n_r
                 return fail(TF_ESTACK, "members take overlapping columns of one run");
         }
     }
+    int pos = 0;                                    // launched runs so far
     for (int r = 0; r < n_runs; ++r) {
         int src[MAXCOLSEG], len[MAXCOLSEG], dst[MAXCOLSEG], n = 0;
         for (int i = 0; i < n_members; ++i) {
@@ -571,7 +575,7 @@ int tf_qmm_stack(const uint16_t *x, int rows, int K, const tf_run *runs, int n_r
         if (n == 0) continue;
         rc = run_product(x, rows, K, runs[r].W, runs[r].scales, runs[r].biases, runs[r].N,
                          runs[r].bits, runs[r].group, y, y_stride, n, src, len, dst,
-                         static_cast<cudaStream_t>(stream));
+                         static_cast<cudaStream_t>(stream), pos++);
         if (rc) return rc;
     }
     return TF_OK;

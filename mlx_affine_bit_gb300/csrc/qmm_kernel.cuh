@@ -220,7 +220,7 @@ __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
     }
     // Under programmatic dependent launch the previous kernel of the stream may
     // still run: wait for it unless the caller declared the weights unwritten by it.
-    if (!P.early_w) grid_dependency_wait();
+    if (!P.early_w && P.dep != 2) grid_dependency_wait();
     uint32_t it = 0;
     Ring ring;
     for (ItemWalk w(P); w.more(P); w.next(P)) {
@@ -483,8 +483,12 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
     const uint32_t mg = magic[0], mq = magic[1];   // MAGIC, QP<BITS>: read at run time, held in registers
 
     // x, y and the split-K workspace may be touched by the previous kernel of
-    // the stream (programmatic dependent launch): wait for it first.
-    grid_dependency_wait();
+    // the stream (programmatic dependent launch): wait for it first -- unless
+    // this is a later run of a stack, which shares nothing it writes with the
+    // runs before it.  The first run of a stack lets the later runs start only
+    // now, so that they too read x after its producer finished.
+    if (P.dep != 2) grid_dependency_wait();
+    if (P.dep == 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     int cur_slice = -1;
     uint32_t it = 0;                         // stages this group has computed
     Ring ring;
@@ -696,11 +700,14 @@ __global__ void __maxnreg__((RegCap<MT, CG>::value)) qmm_kernel(const __grid_con
     __syncthreads();
     // The next kernel of the stream may start its prologue once every CTA of
     // this grid is resident (no effect without programmatic dependent launch).
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (P.dep != 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x >= CG * NCW * 32)
         producer<BITS, G, MT>(P, smem, full, empty, abort);
     else
         consumer<BITS, G, RB, MT, CG>(P, smem, full, empty, abort, magic);
+    // A later run of a stack completes only after the run before it, so the
+    // stack's last launch completes after all of them.
+    if (P.dep == 2) grid_dependency_wait();
 }
 
 // Host-side launcher for one width: every group and row bucket.

@@ -286,3 +286,33 @@ def test_plans_bit_identical(bits, group, rows):
         tf.tf_qmm(xd, rows, K, dm.W[c0:c0 + n], dm.s[c0:c0 + n], dm.b[c0:c0 + n], n, bits, group, ys, n)
         assert torch.equal(ys.view(torch.int32), y[:, c0:c0 + n].contiguous().view(torch.int32)), c0
     oracle_check(m, x, y.cpu().numpy(), sample_cols(N, 48, bits))
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_stack_launch_modes_bit_identical(mode):
+    # Under programmatic dependent launch the runs of a stack overlap (the
+    # first releases the rest only after its dependency wait; a split-K run
+    # keeps the ordinary ordering).  Every run still equals its own product.
+    K = 8192
+    shapes = [(4096, 4, 64), (64, 5, 32), (48, 6, 64), (2000, 3, 128)]
+    mats = [synth.make_matrix(N, K, b, g, 90 + i, 0.001, 0.03) for i, (N, b, g) in enumerate(shapes)]
+    dms = [DevMatrix(m) for m in mats]
+    x = synth.make_x(3, K, 95)
+    xd = dev(x)
+    runs = [(dm.W, dm.s, dm.b, m.N, m.bits, m.group) for dm, m in zip(dms, mats)]
+    members, off = [], 0
+    for i, m in enumerate(mats):
+        members.append((i, 0, m.N, off))
+        off += m.N
+    ref = [run_qmm(dm, xd) for dm in dms]
+    old = tf.tf_set_launch_mode(mode)
+    try:
+        for _ in range(3):
+            y = torch.full((3, off), float("nan"), dtype=torch.float32, device=DEV)
+            tf.tf_qmm_stack(xd, 3, K, runs, members, y, off)
+            c = 0
+            for r, m in zip(ref, mats):
+                assert torch.equal(y[:, c:c + m.N].contiguous().view(torch.int32), r.view(torch.int32))
+                c += m.N
+    finally:
+        tf.tf_set_launch_mode(old)
