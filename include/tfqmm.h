@@ -108,7 +108,12 @@ int tf_qmm_noalloc(const uint16_t *x, int rows, int K,
  * takes n_cols consecutive columns of its run starting at src_col and writes
  * them to y columns [dst_col, dst_col + n_cols).  Members of a run need not be
  * adjacent in y.  Every member's columns equal the run's own tf_qmm result
- * bit for bit.  The table is read on the host only.
+ * bit for bit.  The table is read on the host only.  Each run is one launch;
+ * under TF_LAUNCH_PDL / TF_LAUNCH_EARLY_WEIGHTS the runs after the first
+ * overlap it (they start once the first run's dependency on the previous
+ * kernel of the stream has resolved, and a run with split K waits for the run
+ * before it), and the last launch completes after every run, so the next
+ * kernel of the stream sees the whole stack.
  */
 typedef struct tf_run {
     const uint32_t *W;
