@@ -118,7 +118,7 @@ Plan layout(int N, int K, int bits, int group, int rows, int nsm, int ctas, bool
 // Two m-tiles (32 columns) per item with one CTA per SM when there are at
 // least two such items per SM (shared activation loads, half the per-stage
 // overhead), computed by two consumer groups when the whole K fits one slice
-// and four stages fit (two computed, two in flight); else one m-tile per item
+// and three stages fit (two computed, one in flight); else one m-tile per item
 // with two CTAs per SM when three stages of each still fit; else one CTA per
 // SM with a deeper ring, with two consumer groups for 9-16 rows over many
 // column tiles.  The choice never changes a result's bits.
@@ -126,10 +126,10 @@ Plan make_plan(int N, int K, int bits, int group, int rows, int nsm, bool sb3d) 
     if (row_bucket(rows) <= 8) {
         const Plan wide = layout(N, K, bits, group, rows, nsm, 1, sb3d, 2);
         if (wide.stages >= 3 && (long long)wide.nmt * wide.nsl >= 2LL * nsm) {
-            // Two consumer groups when two stages can be computed with two more in flight.
+            // Two consumer groups (two stages computed at once) when three stages fit.
             if (wide.nsl == 1) {
                 const Plan pp = layout(N, K, bits, group, rows, nsm, 1, sb3d, 2, 2);
-                if (pp.stages >= 4 && pp.nsl == 1) return pp;
+                if (pp.stages >= 3 && pp.nsl == 1) return pp;
             }
             return wide;
         }
