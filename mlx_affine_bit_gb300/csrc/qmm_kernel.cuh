@@ -513,6 +513,14 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
             const int buf = it & 1;
             const int ks0 = k0 + warp * SEG;      // this warp's segment
             const bool active = ks0 < k1;
+            // With two consumer groups a group skips the other's stages, so the
+            // slot's previous fill may belong to the other group and may not
+            // have landed yet; a parity wait on `full` alone could then pass a
+            // phase early.  First wait, as the producer did before this fill,
+            // for the previous fill's consumers to release the slot: `full` is
+            // then exactly one phase from this fill.  (A fresh barrier passes
+            // the parity-1 wait at once.)
+            if (CG > 1) mbar_wait(&empty[slot], ring.phase ^ 1u, abort, P.status);
             mbar_wait(&full[slot], ring.phase, abort, P.status);
             float p[MT][NT][4];
 #pragma unroll

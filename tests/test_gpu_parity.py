@@ -316,3 +316,22 @@ def test_stack_launch_modes_bit_identical(mode):
                 c += m.N
     finally:
         tf.tf_set_launch_mode(old)
+
+
+@pytest.mark.parametrize("bits,group,rows", [(6, 32, 1), (4, 64, 1), (3, 32, 2), (6, 32, 16), (4, 128, 16)])
+def test_two_group_plans_repeatable(bits, group, rows):
+    # The two-consumer-group plans (three to eight ring stages; each group
+    # skips the other's stages) give the same bits on every call and never
+    # trip a bounded wait.
+    N, K = 24832, 2048
+    m = synth.make_matrix(N, K, bits, group, 110 + bits, 0.001, 0.02)
+    dm = DevMatrix(m)
+    x = synth.make_x(rows, K, 111)
+    xd = dev(x)
+    ref = run_qmm(dm, xd)
+    for _ in range(20):
+        y = run_qmm(dm, xd)
+        assert torch.equal(y.view(torch.int32), ref.view(torch.int32))
+    torch.cuda.synchronize()
+    tf.tf_device_status()
+    oracle_check(m, x, ref.cpu().numpy(), sample_cols(N, 32, bits))
