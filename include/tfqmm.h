@@ -58,6 +58,8 @@ extern "C" {
                                  destinations, a destination past y_stride, mixed K */
 #define TF_ECUDA (-10)        /* a CUDA runtime call failed; see tf_last_error_string() */
 #define TF_EDEVICE (-11)      /* a kernel reported a bounded wait that ran out (device status) */
+#define TF_EINVAL_FLAGS (-12) /* output flags other than TF_OUT_BF16 | TF_EPI_RELU2 */
+#define TF_EGATHER (-13)      /* empty slot table, or a slot naming a missing expert or x row */
 
 /*
  * tf_qmm -- one quantized product.
@@ -135,6 +137,42 @@ int tf_qmm_stack(const uint16_t *x, int rows, int K,
                  const tf_run *runs, int n_runs,
                  const tf_member *members, int n_members,
                  float *y, int64_t y_stride, void *stream);
+
+/*
+ * Output options (PR #788, row-kernel commit: the one-row / window gate covers
+ * relu2 calls and strided outputs bit for bit; tf-affine-ref commit: bf16
+ * outputs are bounded by one more bf16 ulp).
+ *   TF_OUT_BF16:  y is bf16 (uint16 bit patterns), each output rounded to
+ *                 nearest even from the fp32 result; y 2-byte aligned.
+ *   TF_EPI_RELU2: y = max(v, 0)^2 of the fp32 result v, in fp32 (then
+ *                 rounded when TF_OUT_BF16 is also set).
+ * The fp32 result v itself is the one tf_qmm computes, bit for bit.
+ */
+#define TF_OUT_BF16 1
+#define TF_EPI_RELU2 2
+
+/* tf_qmm with output options; y is float* or bf16* as flags say. */
+int tf_qmm_ex(const uint16_t *x, int rows, int K,
+              const uint32_t *W, const uint16_t *scales, const uint16_t *biases,
+              int N, int bits, int group,
+              void *y, int64_t y_stride, int flags, void *stream);
+
+/*
+ * tf_qmm_gather -- indexed slots over a set of expert matrices (PR #788,
+ * row-kernel commit: indexed slots in the bit-exact window gate; tf-affine-ref
+ * commit: a one-expert gather equals the dense product).
+ *   Slot i (0 <= i < n_slots) computes y row i = experts[slot_expert[i]] times
+ *   x row slot_row[i] (x is [x_rows][K] bf16; y rows are y_stride elements
+ *   apart, at least every used expert's N; columns past an expert's N are
+ *   untouched).  Each slot equals, bit for bit, tf_qmm_ex of its expert on its
+ *   x row alone.  The slot table is read on the host; experts may differ in
+ *   bits, group and N.  Slots of one expert run together, 16 to a launch, and
+ *   the launches may overlap under programmatic dependent launch (as stack runs).
+ */
+int tf_qmm_gather(const uint16_t *x, int x_rows, int K,
+                  const tf_run *experts, int n_experts,
+                  const int *slot_expert, const int *slot_row, int n_slots,
+                  void *y, int64_t y_stride, int flags, void *stream);
 
 /*
  * tf_widen -- exact widen / regroup on the device (PR #788, the widen commit:

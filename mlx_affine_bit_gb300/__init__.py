@@ -21,11 +21,13 @@ TF_OK = 0
 STATUS = {
     -1: "TF_EINVAL_BITS", -2: "TF_EINVAL_GROUP", -3: "TF_EINVAL_ROWS", -4: "TF_EINVAL_STRIDE",
     -5: "TF_EINVAL_PTR", -6: "TF_EINVAL_SIZE", -7: "TF_ENARROW", -8: "TF_EGROUP",
-    -9: "TF_ESTACK", -10: "TF_ECUDA", -11: "TF_EDEVICE",
+    -9: "TF_ESTACK", -10: "TF_ECUDA", -11: "TF_EDEVICE", -12: "TF_EINVAL_FLAGS", -13: "TF_EGATHER",
 }
-SYMBOLS = ("tf_qmm", "tf_qmm_noalloc", "tf_qmm_stack", "tf_widen", "tf_common_width", "tf_qmm_bytes",
-           "tf_device_status", "tf_set_launch_mode", "tf_last_error_string", "tf_version")
+SYMBOLS = ("tf_qmm", "tf_qmm_ex", "tf_qmm_gather", "tf_qmm_noalloc", "tf_qmm_stack", "tf_widen",
+           "tf_common_width", "tf_qmm_bytes", "tf_device_status", "tf_set_launch_mode",
+           "tf_last_error_string", "tf_version")
 TF_LAUNCH_PDL, TF_LAUNCH_EARLY_WEIGHTS = 1, 2
+TF_OUT_BF16, TF_EPI_RELU2 = 1, 2
 
 
 class TfError(RuntimeError):
@@ -57,6 +59,9 @@ def lib():
         P, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
         L.tf_qmm.argtypes = [P, i32, i32, P, P, P, i32, i32, i32, P, i64, P]
         L.tf_qmm_noalloc.argtypes = [P, i32, i32, P, P, P, i32, i32, i32, P, i64, P]
+        L.tf_qmm_ex.argtypes = [P, i32, i32, P, P, P, i32, i32, i32, P, i64, i32, P]
+        L.tf_qmm_gather.argtypes = [P, i32, i32, ctypes.POINTER(TfRun), i32, ctypes.POINTER(ctypes.c_int),
+                                    ctypes.POINTER(ctypes.c_int), i32, P, i64, i32, P]
         L.tf_qmm_stack.argtypes = [P, i32, i32, ctypes.POINTER(TfRun), i32,
                                    ctypes.POINTER(TfMember), i32, P, i64, P]
         L.tf_widen.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, i32, i32, P]
@@ -66,8 +71,8 @@ def lib():
         L.tf_set_launch_mode.argtypes = [i32]
         L.tf_last_error_string.restype = ctypes.c_char_p
         L.tf_version.restype = ctypes.c_char_p
-        for name in ("tf_qmm", "tf_qmm_noalloc", "tf_qmm_stack", "tf_widen", "tf_common_width", "tf_qmm_bytes",
-                     "tf_device_status", "tf_set_launch_mode"):
+        for name in ("tf_qmm", "tf_qmm_ex", "tf_qmm_gather", "tf_qmm_noalloc", "tf_qmm_stack", "tf_widen",
+                     "tf_common_width", "tf_qmm_bytes", "tf_device_status", "tf_set_launch_mode"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -104,6 +109,23 @@ def tf_qmm_noalloc(x, rows, K, W, scales, biases, N, bits, group, y, y_stride, s
     """tf_qmm with no device allocation (fixed built-in scratch; see include/tfqmm.h)."""
     _check(lib().tf_qmm_noalloc(_ptr(x), rows, K, _ptr(W), _ptr(scales), _ptr(biases), N, bits,
                                 group, _ptr(y), y_stride, _stream(stream)))
+
+
+def tf_qmm_ex(x, rows, K, W, scales, biases, N, bits, group, y, y_stride, flags, stream=None) -> None:
+    """tf_qmm with output flags (TF_OUT_BF16: y is bf16; TF_EPI_RELU2: squared ReLU)."""
+    _check(lib().tf_qmm_ex(_ptr(x), rows, K, _ptr(W), _ptr(scales), _ptr(biases), N, bits, group,
+                           _ptr(y), y_stride, flags, _stream(stream)))
+
+
+def tf_qmm_gather(x, x_rows, K, experts, slot_expert, slot_row, y, y_stride, flags=0, stream=None) -> None:
+    """experts: [(W, scales, biases, N, bits, group)]; slot i: y row i = experts[slot_expert[i]] x row slot_row[i]."""
+    ee = (TfRun * len(experts))(*[TfRun(_ptr(W), _ptr(s), _ptr(b), N, bits, g)
+                                  for (W, s, b, N, bits, g) in experts])
+    n = len(slot_expert)
+    se = (ctypes.c_int * n)(*slot_expert)
+    sr = (ctypes.c_int * len(slot_row))(*slot_row)
+    _check(lib().tf_qmm_gather(_ptr(x), x_rows, K, ee, len(experts), se, sr, n, _ptr(y), y_stride, flags,
+                               _stream(stream)))
 
 
 def tf_qmm_stack(x, rows, K, runs, members, y, y_stride, stream=None) -> None:

@@ -328,10 +328,18 @@ cudaError_t launch(int bits, int group, int rb, int mt, int cg, const QmmParams 
 }
 
 // One run (matrix) written through `nseg` column segments.
+// Output options and row maps of one launch: window row r reads x row xrow[r]
+// and writes y row yrow[r] (identity without a map).
+struct Io {
+    int out = 0;            // OUT_BF16 | OUT_RELU2
+    bool map = false;
+    int xrow[16] = {}, yrow[16] = {};
+};
+
 int run_product(const uint16_t *x, int rows, int K, const uint32_t *W, const uint16_t *s,
                 const uint16_t *b, int N, int bits, int group, float *y, int64_t y_stride,
                 int nseg, const int *seg_src, const int *seg_len, const int *seg_dst,
-                cudaStream_t st, int stack_pos = -1) {
+                cudaStream_t st, int stack_pos = -1, const Io *io = nullptr) {
     std::lock_guard<std::mutex> lk(g_mu);
     DevState *d = nullptr;
     int rc = dev_state(&d);
@@ -376,6 +384,11 @@ int run_product(const uint16_t *x, int rows, int K, const uint32_t *W, const uin
         P.cs_src[i] = seg_src[i];
         P.cs_len[i] = seg_len[i];
         P.cs_dst[i] = seg_dst[i];
+    }
+    P.out = io ? io->out : 0;
+    for (int r = 0; r < 16; ++r) {
+        P.xrow[r] = io && io->map ? io->xrow[r] : r;
+        P.yrow[r] = io && io->map ? io->yrow[r] : r;
     }
     if (pl.nsl > 1) {
         StreamWs *w = nullptr;
@@ -499,6 +512,7 @@ int tfq::product_with_scratch(const uint16_t *x, int rows, int K, const uint32_t
     P.cs_src[0] = 0;
     P.cs_len[0] = N;
     P.cs_dst[0] = 0;
+    for (int r = 0; r < 16; ++r) P.xrow[r] = P.yrow[r] = r;
     cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), st);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(scratch status)");
     if (pl.nsl > 1) {
@@ -577,6 +591,77 @@ int tf_qmm_stack(const uint16_t *x, int rows, int K, const tf_run *runs, int n_r
                          runs[r].bits, runs[r].group, y, y_stride, n, src, len, dst,
                          static_cast<cudaStream_t>(stream), pos++);
         if (rc) return rc;
+    }
+    return TF_OK;
+}
+
+int tf_qmm_ex(const uint16_t *x, int rows, int K, const uint32_t *W, const uint16_t *scales,
+              const uint16_t *biases, int N, int bits, int group, void *y, int64_t y_stride,
+              int flags, void *stream) {
+    g_err.clear();
+    if (flags & ~(TF_OUT_BF16 | TF_EPI_RELU2)) return fail(TF_EINVAL_FLAGS, "unknown output flags");
+    int rc = check_matrix(K, W, scales, biases, N, bits, group);
+    if (rc) return rc;
+    if (rows < 1 || rows > 16) return fail(TF_EINVAL_ROWS, "rows must be in [1, 16]");
+    if (!x || !y || !aligned(x, 16) || !aligned(y, (flags & TF_OUT_BF16) ? 2 : 4))
+        return fail(TF_EINVAL_PTR, "NULL pointer, x not 16-byte aligned, or y not aligned to its type");
+    if (y_stride < N) return fail(TF_EINVAL_STRIDE, "y_stride below N is refused");
+    Io io;
+    io.out = flags;
+    const int src = 0, len = N, dst = 0;
+    return run_product(x, rows, K, W, scales, biases, N, bits, group, static_cast<float *>(y), y_stride, 1,
+                       &src, &len, &dst, static_cast<cudaStream_t>(stream), -1, &io);
+}
+
+int tf_qmm_gather(const uint16_t *x, int x_rows, int K, const tf_run *experts, int n_experts,
+                  const int *slot_expert, const int *slot_row, int n_slots, void *y,
+                  int64_t y_stride, int flags, void *stream) {
+    g_err.clear();
+    if (flags & ~(TF_OUT_BF16 | TF_EPI_RELU2)) return fail(TF_EINVAL_FLAGS, "unknown output flags");
+    if (!x || !y || !aligned(x, 16) || !aligned(y, (flags & TF_OUT_BF16) ? 2 : 4))
+        return fail(TF_EINVAL_PTR, "NULL pointer, x not 16-byte aligned, or y not aligned to its type");
+    if (x_rows < 1) return fail(TF_EINVAL_ROWS, "x_rows must be at least 1");
+    if (!experts || n_experts < 1 || !slot_expert || !slot_row || n_slots < 1)
+        return fail(TF_EGATHER, "empty expert or slot table");
+    for (int i = 0; i < n_slots; ++i) {
+        if (slot_expert[i] < 0 || slot_expert[i] >= n_experts)
+            return fail(TF_EGATHER, "a slot names a missing expert");
+        if (slot_row[i] < 0 || slot_row[i] >= x_rows) return fail(TF_EGATHER, "a slot names a missing x row");
+    }
+    for (int e = 0; e < n_experts; ++e) {
+        int used = 0;
+        for (int i = 0; i < n_slots && !used; ++i) used = slot_expert[i] == e;
+        if (!used) continue;
+        const int rc = check_matrix(K, experts[e].W, experts[e].scales, experts[e].biases, experts[e].N,
+                                    experts[e].bits, experts[e].group);
+        if (rc) return rc;
+        if (y_stride < experts[e].N) return fail(TF_EINVAL_STRIDE, "y_stride below an expert's N is refused");
+    }
+    // Slots grouped by expert in slot order, at most 16 to a launch; every
+    // launch reads x and writes its own y rows, so they may overlap (as stack runs).
+    int pos = 0;
+    for (int e = 0; e < n_experts; ++e) {
+        Io io;
+        io.out = flags;
+        io.map = true;
+        int n = 0;
+        for (int i = 0; i <= n_slots; ++i) {
+            const bool take = i < n_slots && slot_expert[i] == e;
+            if (take) {
+                io.xrow[n] = slot_row[i];
+                io.yrow[n] = i;
+                ++n;
+            }
+            if (n == 16 || (i == n_slots && n > 0)) {
+                const int src = 0, len = experts[e].N, dst = 0;
+                const int rc = run_product(x, n, K, experts[e].W, experts[e].scales, experts[e].biases,
+                                           experts[e].N, experts[e].bits, experts[e].group,
+                                           static_cast<float *>(y), y_stride, 1, &src, &len, &dst,
+                                           static_cast<cudaStream_t>(stream), pos++, &io);
+                if (rc) return rc;
+                n = 0;
+            }
+        }
     }
     return TF_OK;
 }

@@ -40,8 +40,8 @@ constexpr int ZERO_BYTES = 2048;           // zero block that idle lanes of smal
 
 struct QmmParams {
     // TMA descriptors (bulk mode).  W: [K/SEG segments][N rows][SEG*bits/32
-    // words], box {segment + 4 words past its extent (zero filled), 16 rows,
-    // 8 segments}; scales/biases: one stage's groups of 16 rows.
+    // words], box {segment + 4 words past its extent (zero filled), the
+    // stage's rows, 8 segments}; scales/biases: one stage's groups of its rows.
     CUtensorMap tmW, tmS, tmB;
     const uint16_t *x;
     const uint32_t *W;
@@ -70,6 +70,12 @@ struct QmmParams {
     int x_off, sx_off, pb_off, z_off, st_off;   // smem offsets
     int ncs;            // column-map segments
     int cs_src[MAXCOLSEG], cs_len[MAXCOLSEG], cs_dst[MAXCOLSEG];
+    int out;            // OUT_* bits: bf16 output (y holds bf16), squared-ReLU epilogue
+    int xrow[16];       // window row r reads x row xrow[r] (K elements apart) ...
+    int yrow[16];       // ... and writes y row yrow[r] (y_stride elements apart)
 };
+
+constexpr int OUT_BF16 = 1;    // y is bf16, each output rounded to nearest even
+constexpr int OUT_RELU2 = 2;   // y = max(v, 0)^2 of the fp32 result v (before any bf16 rounding)
 
 }  // namespace tfq

@@ -306,7 +306,7 @@ __device__ void load_x_slice(const QmmParams &P, const Item &I, uint4 *Bf, float
     for (int u = tid; u < RB * ngs; u += nthr) {
         const int r = u / ngs, gs = u - r * ngs;
         float acc = 0.f;
-        const uint16_t *src = P.x + (long long)r * P.K + I.k_lo + gs * G;
+        const uint16_t *src = P.x + (long long)(r < rows ? P.xrow[r] : 0) * P.K + I.k_lo + gs * G;
 #pragma unroll 4
         for (int t = 0; t < G / 8; ++t) {
             const int qq = (8 * t) / (G / 4), m = ((8 * t) % (G / 4)) / 8;
@@ -426,10 +426,21 @@ __device__ __forceinline__ int dst_col(const QmmParams &P, int n) {
     return -1;
 }
 
+// Output (window row r, column n) = v: the optional squared-ReLU epilogue in
+// fp32, then an fp32 or a round-to-nearest-even bf16 store.
 __device__ __forceinline__ void store_y(const QmmParams &P, int r, int n, float v) {
     if (r < P.rows && n < P.N) {
         const int d = dst_col(P, n);
-        if (d >= 0) P.y[(long long)r * P.y_stride + d] = v;
+        if (d < 0) return;
+        if (P.out & OUT_RELU2) {
+            const float u = fmaxf(v, 0.f);
+            v = u * u;
+        }
+        const long long at = (long long)P.yrow[r] * P.y_stride + d;
+        if (P.out & OUT_BF16)
+            reinterpret_cast<__nv_bfloat16 *>(P.y)[at] = __float2bfloat16_rn(v);
+        else
+            P.y[at] = v;
     }
 }
 

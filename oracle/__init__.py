@@ -64,6 +64,8 @@ def lib():
         L.oracle_widen.argtypes = [P, P, P, i64, i64, i32, i32, P, P, P, i32, i32]
         L.oracle_common_width.restype = i32
         L.oracle_common_width.argtypes = [P, P, i32, P, P]
+        L.oracle_relu2.restype = None
+        L.oracle_relu2.argtypes = [P, i64, P]
         _lib = L
     return _lib
 
@@ -146,3 +148,33 @@ def common_width(bits_list, groups_list):
 # |y - y64| <= (K * 2**-24 + 2**-20) * sum_k |x_k * w_k|.
 def bound(absum: np.ndarray, K: int) -> np.ndarray:
     return (K * 2.0 ** -24 + 2.0 ** -20) * absum
+
+
+def relu2(y: np.ndarray) -> np.ndarray:
+    """max(y, 0)^2 elementwise, in fp64 (the squared-ReLU output epilogue)."""
+    y = _c(y, np.float64)
+    out = np.empty_like(y)
+    lib().oracle_relu2(_p(y), y.size, _p(out))
+    return out
+
+
+def bf16_ulp(a: np.ndarray) -> np.ndarray:
+    """One bf16 ulp at magnitude a (8 significant bits; 0 where a == 0)."""
+    a = np.abs(np.asarray(a, dtype=np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, np.exp2(e - 7), 0.0)
+
+
+def bound_out(y64: np.ndarray, absum: np.ndarray, K: int, relu2_epi: bool, bf16_out: bool):
+    """(target, bound) of an output with options, from the fp32 bound B of the
+    product v: squared ReLU moves the error to B*(2|v| + B) plus one fp32
+    rounding of the square; a bf16 output adds one bf16 ulp (as the pages bound
+    bf16 outputs)."""
+    B = bound(absum, K)
+    t, Bt = y64, B
+    if relu2_epi:
+        t = relu2(y64)
+        Bt = B * (2 * np.abs(y64) + B) + 2.0 ** -24 * (np.maximum(y64, 0) + B) ** 2
+    if bf16_out:
+        Bt = Bt + bf16_ulp(np.abs(t) + Bt)
+    return t, Bt

@@ -194,3 +194,10 @@ int oracle_common_width(const int *bits, const int *groups, int n,
     *group_out = g;
     return ORACLE_OK;
 }
+
+void oracle_relu2(const double *y, int64_t n, double *out) {
+    for (int64_t i = 0; i < n; ++i) {
+        const double v = y[i] > 0.0 ? y[i] : 0.0;
+        out[i] = v * v;
+    }
+}

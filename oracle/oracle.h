@@ -71,6 +71,13 @@ int oracle_widen(const uint32_t *W, const uint16_t *scales, const uint16_t *bias
                  uint32_t *W_out, uint16_t *s_out, uint16_t *b_out,
                  int bits_out, int group_out);
 
+/*
+ * Squared-ReLU output epilogue (TensorFold PR #788, row-kernel commit: relu2
+ * calls in the bit-exact window gate; the pages name it without a formula, so
+ * it is read as its name says): out[i] = max(y[i], 0)^2, in fp64.
+ */
+void oracle_relu2(const double *y, int64_t n, double *out);
+
 /* The common width of n members: the most bits and the smallest group. */
 int oracle_common_width(const int *bits, const int *groups, int n,
                         int *bits_out, int *group_out);

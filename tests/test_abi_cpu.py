@@ -95,3 +95,35 @@ def test_every_kernel_instantiated(tf):
                 for mt, cg in (((1, 1), (2, 1), (2, 2)) if rb <= 8 else ((1, 1), (1, 2))):
                     name = "tfq::qmm_kernel<%d, %d, %d, %d, %d>(" % (bits, group, rb, mt, cg)
                     assert name in out, name
+
+
+def test_output_option_refusals_on_host(tf):
+    L = tf.lib()
+    # unknown flag bits; bf16 y needs 2-byte alignment only, fp32 y 4-byte
+    assert L.tf_qmm_ex(A, 1, 1024, A, A, A, 256, 4, 64, A, 256, 4, None) == -12
+    assert L.tf_qmm_ex(A, 1, 1024, A, A, A, 256, 4, 64, A + 2, 256, 0, None) == -5
+    assert L.tf_qmm_ex(A, 17, 1024, A, A, A, 256, 4, 64, A, 256, 1, None) == -3
+    assert L.tf_qmm_ex(A, 1, 1024, A, A, A, 256, 4, 64, A, 255, 3, None) == -4
+
+
+@pytest.mark.parametrize("slot_expert,slot_row,code", [
+    ([0, 2], [0, 0], -13),        # a missing expert
+    ([0, 1], [0, 3], -13),        # a missing x row (x_rows = 3)
+    ([0, -1], [0, 0], -13),
+    ([], [], -13),                # no slots
+])
+def test_gather_refusals_on_host(tf, slot_expert, slot_row, code):
+    experts = [(A, A, A, 64, 4, 64), (A, A, A, 64, 5, 32)]
+    with pytest.raises(tf.TfError) as e:
+        tf.tf_qmm_gather(A, 3, 256, experts, slot_expert, slot_row, A, 64, 0, stream=0)
+    assert e.value.rc == code
+
+
+def test_gather_stride_and_flags_refused(tf):
+    experts = [(A, A, A, 64, 4, 64), (A, A, A, 96, 5, 32)]
+    with pytest.raises(tf.TfError) as e:      # y_stride below the used expert's N
+        tf.tf_qmm_gather(A, 3, 256, experts, [1], [0], A, 64, 0, stream=0)
+    assert e.value.rc == -4
+    with pytest.raises(tf.TfError) as e:
+        tf.tf_qmm_gather(A, 3, 256, experts, [0], [0], A, 96, 8, stream=0)
+    assert e.value.rc == -12

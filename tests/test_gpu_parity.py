@@ -335,3 +335,84 @@ def test_two_group_plans_repeatable(bits, group, rows):
     torch.cuda.synchronize()
     tf.tf_device_status()
     oracle_check(m, x, ref.cpu().numpy(), sample_cols(N, 32, bits))
+
+
+def _bf16_bits_to_f64(t: torch.Tensor) -> np.ndarray:
+    h = t.cpu().numpy().view(np.uint16).astype(np.uint32) << 16
+    return h.view(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("flags", [tf.TF_EPI_RELU2, tf.TF_OUT_BF16, tf.TF_OUT_BF16 | tf.TF_EPI_RELU2])
+@pytest.mark.parametrize("bits,group,N,K", [(4, 64, 300, 2048), (6, 32, 12304, 2048), (3, 128, 2048, 12288)])
+def test_output_options(flags, bits, group, N, K):
+    # fp32 or bf16 output, with or without the squared-ReLU epilogue: within
+    # the bound of the oracle's product passed through the same epilogue, equal
+    # to the epilogue of the fp32 result bit for bit, and each row alone equal
+    # to the same row of a 16-row window.
+    m = synth.make_matrix(N, K, bits, group, 130 + bits, 0.001, 0.03)
+    dm = DevMatrix(m)
+    x = synth.make_x(16, K, 131)
+    xd = dev(x)
+    bf = bool(flags & tf.TF_OUT_BF16)
+    dt = torch.int16 if bf else torch.float32
+
+    def call(xs):
+        y = torch.zeros((xs.shape[0], N), dtype=dt, device=DEV)
+        tf.tf_qmm_ex(xs, xs.shape[0], K, dm.W, dm.s, dm.b, N, bits, group, y, N, flags)
+        return y
+
+    y16 = call(xd)
+    v = run_qmm(dm, xd)                                     # the fp32 product
+    if flags & tf.TF_EPI_RELU2:
+        v = torch.clamp(v, min=0) * torch.clamp(v, min=0)
+    want = v.to(torch.bfloat16).view(torch.int16) if bf else v
+    assert torch.equal(y16.view(torch.int16 if bf else torch.int32), want.view(torch.int16 if bf else torch.int32))
+    for r in (0, 7, 15):
+        assert torch.equal(call(xd[r:r + 1].contiguous())[0], y16[r])
+    cols = sample_cols(N, 40, bits)
+    y64, absum = oracle.qmm(x, m.W, m.scales, m.biases, N, K, bits, group, cols=cols, nthreads=8)
+    t, B = oracle.bound_out(y64, absum, K, bool(flags & tf.TF_EPI_RELU2), bf)
+    got = _bf16_bits_to_f64(y16[:, cols]) if bf else y16[:, cols].cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - t) <= B)
+
+
+@pytest.mark.parametrize("flags", [0, tf.TF_OUT_BF16 | tf.TF_EPI_RELU2])
+def test_gather_equals_dense(flags):
+    # Indexed slots over four experts (mixed widths, one with fewer columns):
+    # every slot equals its expert's product on its x row alone, bit for bit;
+    # columns past an expert's N stay untouched.
+    K, x_rows, n_slots = 2048, 6, 37
+    shapes = [(256, 4, 64), (256, 6, 32), (256, 3, 128), (160, 5, 64)]
+    mats = [synth.make_matrix(N, K, b, g, 140 + i, 0.001, 0.03) for i, (N, b, g) in enumerate(shapes)]
+    dms = [DevMatrix(m) for m in mats]
+    x = synth.make_x(x_rows, K, 141)
+    xd = dev(x)
+    rng = np.random.default_rng(142)
+    se = rng.integers(0, 4, n_slots).tolist()
+    sr = rng.integers(0, x_rows, n_slots).tolist()
+    bf = bool(flags & tf.TF_OUT_BF16)
+    dt = torch.int16 if bf else torch.float32
+    stride = 264
+    y = torch.full((n_slots, stride), -7, dtype=torch.int16, device=DEV) if bf else \
+        torch.full((n_slots, stride), float("nan"), dtype=torch.float32, device=DEV)
+    experts = [(dm.W, dm.s, dm.b, m.N, m.bits, m.group) for dm, m in zip(dms, mats)]
+    tf.tf_qmm_gather(xd, x_rows, K, experts, se, sr, y, stride, flags)
+    for i in range(n_slots):
+        m, dm = mats[se[i]], dms[se[i]]
+        one = torch.zeros((1, m.N), dtype=dt, device=DEV)
+        tf.tf_qmm_ex(xd[sr[i]:sr[i] + 1].contiguous(), 1, K, dm.W, dm.s, dm.b, m.N, m.bits, m.group, one, m.N,
+                     flags)
+        assert torch.equal(y[i, :m.N], one[0]), i
+        tail = y[i, m.N:]
+        if bf:
+            assert torch.all(tail == -7)
+        else:
+            assert torch.all(torch.isnan(tail))
+    # and against the oracle for a few slots
+    for i in (0, 5, 36):
+        m = mats[se[i]]
+        cols = sample_cols(m.N, 24, i)
+        y64, absum = oracle.qmm(x[sr[i]:sr[i] + 1], m.W, m.scales, m.biases, m.N, K, m.bits, m.group, cols=cols)
+        t, B = oracle.bound_out(y64, absum, K, bool(flags & tf.TF_EPI_RELU2), bf)
+        got = _bf16_bits_to_f64(y[i:i + 1, cols]) if bf else y[i:i + 1, cols].cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(got - t) <= B)

@@ -241,3 +241,25 @@ def test_negative_control_exceeds_bound():
     ysq, _ = oracle.qmm(x, m.W, m.scales, zero, m.N, m.K, m.bits, m.group)
     ratio = np.abs(0.01 * ysq) / oracle.bound(absum, m.K)
     assert ratio.max() > 1.0
+
+
+def test_relu2_closed_form():
+    # max(v, 0)^2 at values whose squares are exact: negatives and zeros give 0.
+    y = np.array([-3.0, -0.0, 0.0, 0.5, 2.0, 1e-3, -1e300, 3.0])
+    assert oracle.relu2(y).tolist() == [0.0, 0.0, 0.0, 0.25, 4.0, 1e-6, 0.0, 9.0]
+
+
+def test_relu2_monotone_and_even_part():
+    v = np.linspace(-5, 5, 1001)
+    r = oracle.relu2(v)
+    assert np.all(np.diff(r) >= 0) and np.all(r[v <= 0] == 0)
+    # on v > 0 it is the square: relu2(v) * relu2(1/v) == 1 up to rounding
+    pos = v[v > 0]
+    assert np.allclose(oracle.relu2(pos) * oracle.relu2(1 / pos), 1.0, rtol=1e-15, atol=0)
+
+
+@pytest.mark.parametrize("h", [0x3F80, 0x4300, 0x3A83, 0x7F00, 0x0080])
+def test_bf16_ulp_is_the_spacing_of_adjacent_patterns(h):
+    # one ulp at a bf16 value = the gap to the next bit pattern (same exponent)
+    a, b = oracle.bf16(h), oracle.bf16(h + 1)
+    assert oracle.bf16_ulp(np.array([a]))[0] == b - a
