@@ -28,6 +28,7 @@ import numpy as np  # noqa: E402
 
 import synth  # noqa: E402
 
+GATHER_EXPERTS, GATHER_N, GATHER_K = 8, 2048, 2048
 METRIC = "achieved HBM GB/s (and % of GB300 peak) of quantized GEMV per bits/group/rows"
 L2_BYTES = 129 * 2 ** 20
 
@@ -54,6 +55,11 @@ def workload_cases(name: str):
     if name == "stack":   # the members (the GPU arm runs them as one fused stack per row count)
         return [("stack member %d/%d r%d" % (m.bits, m.group, r), m.n_cols, synth.STACK_K, m.bits, m.group, m.seed, r)
                 for r in synth.STACK_ROWS for m in synth.STACK_MEMBERS]
+    if name == "gather":   # the expert matrices (the GPU arm runs one gather call per step)
+        return [("gather expert %d" % e, GATHER_N, GATHER_K, 4, 64, 150 + e, 2) for e in range(GATHER_EXPERTS)]
+    if name == "options":
+        return [("decode 12288x2048 r%d %s" % (r, o), 12288, 2048, 6, 32, 19, r)
+                for r in (1, 16) for o in ("fp32", "bf16+relu2")]
     if name == "decode":
         return [("decode %dx%d r%d" % (N, K, r), N, K, 6, 32, s, r)
                 for (N, K, s) in synth.DECODE_SHAPES for r in synth.DECODE_ROWS]
@@ -67,6 +73,10 @@ WORKLOAD_TEXT = {
     "stack": "fused mixed-width stack, K=2048: members 4/g64 4096, 5/g128 2048, 5/g128 48, 6/g64 48 "
              "widened to a 5-bit g64 run of 6192 columns and a 6-bit g64 run of 48, one tf_qmm_stack "
              "into a 6240-column strided output; rows 1 and 16 (2 stacks a step)",
+    "gather": "expert gather: 16 slots over 8 experts of 2048 x 2048, 4-bit g64, two slots an expert "
+              "(one tf_qmm_gather a step)",
+    "options": "decode 12288 x 2048 6-bit g32, rows 1 and 16: fp32 output and bf16 output with the "
+               "squared-ReLU epilogue (tf_qmm_ex)",
     "decode": "decode windows: 6-bit g32, 12288x2048 and 2048x12288, rows {1,2,3,8,16} (10 GEMVs a step)",
 }
 
@@ -206,6 +216,70 @@ def stack_items(cases, dev, tf):
     return items, per_step
 
 
+def _dev_matrix(m, dev):
+    import torch
+    return (torch.from_numpy(m.W.view(np.int32)).to(dev), torch.from_numpy(m.scales.view(np.int16)).to(dev),
+            torch.from_numpy(m.biases.view(np.int16)).to(dev))
+
+
+def _io_item(label, rows, K, N, nbytes, dev, out_dtype, call, grow):
+    import torch
+    x_h = synth.make_x(rows, K, 150)
+    it = dict(label=label, N=N, K=K, rows=rows, bytes=nbytes, reps=[None],
+              x=torch.from_numpy(x_h.view(np.int16)).to(dev), x_pin=torch.from_numpy(x_h.view(np.int16)).pin_memory(),
+              y=torch.empty((rows, N), dtype=out_dtype, device=dev),
+              y_pin=torch.empty((rows, N), dtype=out_dtype).pin_memory())
+    it["call"] = lambda c, st: call(it, c, st)
+    it["grow"] = lambda copies: grow(it, copies)
+    return it
+
+
+def gather_items(cases, dev, tf):
+    """One tf_qmm_gather a step: 16 slots (x rows 0..15) over 8 expert matrices, two slots an expert."""
+    import torch
+    mats = [synth.make_matrix(N, K, b, g, s, 0.001, 0.03) for (_, N, K, b, g, s, _) in cases]
+    base = [_dev_matrix(m, dev) for m in mats]
+    n_slots = 2 * len(mats)
+    se = [i % len(mats) for i in range(n_slots)]
+    sr = list(range(n_slots))
+    K = GATHER_K
+    nb = sum(synth.algorithmic_bytes(m.N, K, m.bits, m.group, 2) - 2 * K * 2 for m in mats) + n_slots * K * 2
+
+    def call(it, c, st):
+        ex = [(W, s_, b_, GATHER_N, 4, 64) for (W, s_, b_) in it["reps"][c % len(it["reps"])]]
+        tf.tf_qmm_gather(it["x"], n_slots, K, ex, se, sr, it["y"], GATHER_N, 0, st)
+
+    def grow(it, copies):
+        it["reps"] = [base] + [[tuple(t.clone() for t in e) for e in base] for _ in range(copies - 1)]
+
+    it = _io_item("gather 16 slots / 8 experts", n_slots, K, GATHER_N, nb, dev, torch.float32, call, grow)
+    it["launches"] = len(mats)
+    return [it], nb
+
+
+def options_items(cases, dev, tf):
+    """tf_qmm_ex on the 12288 x 2048 decode shape: fp32 output, and bf16 output with relu2."""
+    import torch
+    m = synth.make_matrix(12288, 2048, 6, 32, 19, 0.001, 0.03)
+    base = _dev_matrix(m, dev)
+    items, per_step = [], 0
+    for (label, N, K, bits, group, seed, rows) in cases:
+        flags = 0 if label.endswith("fp32") else tf.TF_OUT_BF16 | tf.TF_EPI_RELU2
+        out_bytes = 4 if flags == 0 else 2
+        nb = synth.algorithmic_bytes(N, K, bits, group, rows) - rows * N * 4 + rows * N * out_bytes
+
+        def call(it, c, st, flags=flags):
+            W, s_, b_ = it["reps"][c % len(it["reps"])]
+            tf.tf_qmm_ex(it["x"], it["rows"], K, W, s_, b_, N, bits, group, it["y"], N, flags, st)
+
+        def grow(it, copies):
+            it["reps"] = [base] + [tuple(t.clone() for t in base) for _ in range(copies - 1)]
+
+        items.append(_io_item(label, rows, K, N, nb, dev, torch.float32 if flags == 0 else torch.int16, call, grow))
+        per_step += nb
+    return items, per_step
+
+
 def run_gpu(args, cases):
     import torch
     import torch.distributed as dist
@@ -232,7 +306,13 @@ def run_gpu(args, cases):
     # Device-resident inputs; enough weight copies that a buffer is reused only
     # after >= 4 L2 sizes of other traffic.
     cpu_cases = list(cases)                  # the oracle baseline runs on the members
-    if args.workload == "stack":
+    if args.workload in ("gather", "options"):
+        items, per_step = (gather_items if args.workload == "gather" else options_items)(cases, dev, tf)
+        copies = max(1, -(-4 * L2_BYTES // per_step))
+        for it in items:
+            it["grow"](copies)
+        cases = []
+    elif args.workload == "stack":
         items, per_step = stack_items(cases, dev, tf)
         copies = max(1, -(-4 * L2_BYTES // per_step))
         for it in items:
@@ -260,6 +340,9 @@ def run_gpu(args, cases):
     torch.cuda.synchronize()
 
     def launch(it, c, st):
+        if "call" in it:
+            it["call"](c, st)
+            return
         if it.get("stack"):
             tf.tf_qmm_stack(it["x"], it["rows"], it["K"], it["reps"][c % len(it["reps"])], it["members"],
                             it["y"], it["N"], st)
@@ -403,7 +486,8 @@ def run_gpu(args, cases):
             "cpu_baseline": cpu,
             "e2e": {"value": per_step * e2e_steps / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": sum(len(it["reps"][0]) if it.get("stack") else 1 for it in items) * args.steps,
+            "gpu_launches": sum(it.get("launches", len(it["reps"][0]) if it.get("stack") else 1)
+                                for it in items) * args.steps,
             "timing": "CUDA graph of %d steps replayed %d times; per-product launch time from its own graph "
                       "over >= 4 L2 sizes of weight copies" % (copies, replays),
             "clocks": clocks,
