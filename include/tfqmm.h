@@ -217,6 +217,16 @@ int tf_device_status(void);
 #define TF_LAUNCH_EARLY_WEIGHTS 2
 int tf_set_launch_mode(int mode);
 
+/*
+ * Test hook for the bounded waits (no GPU fault is involved): the next product
+ * launch withholds every CTA's first stage of codes, so the consumers' wait
+ * for it runs out after about 2 s; the kernel records that in the device
+ * status word, stops waiting and runs to completion (its output is then
+ * meaningless) and tf_device_status returns TF_EDEVICE.  The context stays
+ * usable.  One shot; TF_OK.
+ */
+int tf_inject_stall(void);
+
 /* Message for the last failing call on this host thread ("" if none). */
 const char *tf_last_error_string(void);
 

@@ -25,7 +25,7 @@ STATUS = {
 }
 SYMBOLS = ("tf_qmm", "tf_qmm_ex", "tf_qmm_gather", "tf_qmm_noalloc", "tf_qmm_stack", "tf_widen",
            "tf_common_width", "tf_qmm_bytes", "tf_device_status", "tf_set_launch_mode",
-           "tf_last_error_string", "tf_version")
+           "tf_inject_stall", "tf_last_error_string", "tf_version")
 TF_LAUNCH_PDL, TF_LAUNCH_EARLY_WEIGHTS = 1, 2
 TF_OUT_BF16, TF_EPI_RELU2 = 1, 2
 
@@ -69,10 +69,12 @@ def lib():
         L.tf_qmm_bytes.argtypes = [i32, i32, i32, i32, P, P]
         L.tf_device_status.argtypes = []
         L.tf_set_launch_mode.argtypes = [i32]
+        L.tf_inject_stall.argtypes = []
         L.tf_last_error_string.restype = ctypes.c_char_p
         L.tf_version.restype = ctypes.c_char_p
         for name in ("tf_qmm", "tf_qmm_ex", "tf_qmm_gather", "tf_qmm_noalloc", "tf_qmm_stack", "tf_widen",
-                     "tf_common_width", "tf_qmm_bytes", "tf_device_status", "tf_set_launch_mode"):
+                     "tf_common_width", "tf_qmm_bytes", "tf_device_status", "tf_set_launch_mode",
+                     "tf_inject_stall"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -168,6 +170,11 @@ def tf_set_launch_mode(mode: int) -> int:
     if rc < 0:
         _check(rc)
     return rc
+
+
+def tf_inject_stall() -> None:
+    """Test hook: the next product's first stage is withheld (its bounded wait runs out)."""
+    _check(lib().tf_inject_stall())
 
 
 def tf_version() -> str:

@@ -267,6 +267,7 @@ struct DevState {
 
 std::mutex g_mu;
 std::atomic<int> g_launch_mode{0};
+std::atomic<int> g_stall{0};          // test hook armed by tf_inject_stall (one launch)
 std::map<int, DevState> g_dev;
 std::map<std::pair<int, cudaStream_t>, StreamWs> g_ws;
 
@@ -399,6 +400,7 @@ int run_product(const uint16_t *x, int rows, int K, const uint32_t *W, const uin
     }
     const int mode = g_launch_mode.load(std::memory_order_relaxed);
     P.early_w = (mode & TF_LAUNCH_EARLY_WEIGHTS) != 0;
+    P.stall = g_stall.exchange(0);
     // Runs of a stack read x and write disjoint columns: after the first, a run
     // without split-K overlaps the runs before it (see QmmParams::dep).
     P.dep = stack_pos < 0 ? 0 : stack_pos == 0 ? 1 : pl.nsl == 1 ? 2 : 0;
@@ -739,6 +741,12 @@ int tf_set_launch_mode(int mode) {
     g_err.clear();
     if (mode & ~(TF_LAUNCH_PDL | TF_LAUNCH_EARLY_WEIGHTS)) return fail(TF_EINVAL_SIZE, "unknown launch mode bits");
     return g_launch_mode.exchange(mode);
+}
+
+int tf_inject_stall(void) {
+    g_err.clear();
+    g_stall.store(1);
+    return TF_OK;
 }
 
 const char *tf_last_error_string(void) { return g_err.c_str(); }

@@ -70,6 +70,7 @@ struct QmmParams {
     int x_off, sx_off, pb_off, z_off, st_off;   // smem offsets
     int ncs;            // column-map segments
     int cs_src[MAXCOLSEG], cs_len[MAXCOLSEG], cs_dst[MAXCOLSEG];
+    int stall;          // test hook: the producer withholds every CTA's first stage
     int out;            // OUT_* bits: bf16 output (y holds bf16), squared-ReLU epilogue
     int xrow[16];       // window row r reads x row xrow[r] (K elements apart) ...
     int yrow[16];       // ... and writes y row yrow[r] (y_stride elements apart)

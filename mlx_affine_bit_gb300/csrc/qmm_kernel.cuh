@@ -232,7 +232,11 @@ __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
             uint8_t *st = smem + P.st_off + slot * P.stage_bytes;
             uint8_t *sst = st + SEGS * ROWS * SEGP;
             uint8_t *bst = sst + ROWS * P.sbpitch;
-            if (P.bulk) {
+            // Test hook: the first stage is never sent, so its consumers' bounded
+            // wait runs out (recorded in the status word) and the kernel completes.
+            const bool withhold = P.stall && it == 0;
+            if (withhold) {
+            } else if (P.bulk) {
                 // Rows past N and segments past K arrive zero-filled; the full
                 // boxes count toward the transaction bytes.
                 if (lane == 0) {
@@ -248,7 +252,7 @@ __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                 }
                 // The CTA's first stage travels alone: every CTA's first stage
                 // lands before later stages compete with it for DRAM.
-                if (it == 0) mbar_wait(&full[slot], ring.phase, abort, P.status);
+                if (it == 0 && !withhold) mbar_wait(&full[slot], ring.phase, abort, P.status);
             } else {
                 // Odd shapes or alignments: plain copies by the warp into the same layout.
                 const int k1 = min(I.k_hi, k0 + CHUNK);
@@ -284,6 +288,7 @@ __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                 phase ^= 1u;
             }
             --slot;
+            if (P.stall && it - 1 - j == 0) continue;    // the withheld first stage
             mbar_wait(&full[slot], phase, abort, P.status, false);
         }
     }
