@@ -379,6 +379,28 @@ __device__ __forceinline__ void group_body(const uint32_t *const (&pr)[G / 32],
     constexpr int LR = layout_rows(RB);
     constexpr int RUNS = G / 32;
     constexpr int RW = Pitch<BITS>::SEGP / 4;     // words between rows of a segment block
+    // 4- and 8-bit runs of a lane lie in consecutive aligned words: with two or
+    // four runs a group, one vector load per row feeds them all.
+    constexpr int VW = (BITS == 4 || BITS == 8) && RUNS >= 2 ? RUNS * BITS / 4 : 0;   // words
+    uint32_t vw[MT][2][VW > 0 ? VW : 1];
+    if (VW == 2 || VW == 4 || VW == 8) {
+#pragma unroll
+        for (int t = 0; t < MT; ++t)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t *src = pr[0] + woff + (t * 16 + 8 * h) * RW;
+#pragma unroll
+                for (int v = 0; v < VW; v += (VW >= 4 ? 4 : 2)) {
+                    if (VW >= 4) {
+                        const uint4 u = *reinterpret_cast<const uint4 *>(src + v);
+                        vw[t][h][v] = u.x, vw[t][h][v + 1] = u.y, vw[t][h][v + 2] = u.z, vw[t][h][v + 3] = u.w;
+                    } else {
+                        const uint2 u = *reinterpret_cast<const uint2 *>(src + v);
+                        vw[t][h][v] = u.x, vw[t][h][v + 1] = u.y;
+                    }
+                }
+            }
+    }
     float c[MT][NT][4];
 #pragma unroll
     for (int m = 0; m < RUNS; ++m) {
@@ -389,8 +411,13 @@ __device__ __forceinline__ void group_body(const uint32_t *const (&pr)[G / 32],
         for (int t = 0; t < MT; ++t) {
             // A registers in MMA operand order: a[2i] = pair i of row g, a[2i+1] of row g+8.
             uint32_t a[8];
-            Unpack<BITS>::template run<2>(pr[m] + woff + (t * 16) * RW, ua[m], ub[m], mg, mq, a);
-            Unpack<BITS>::template run<2>(pr[m] + woff + (t * 16 + 8) * RW, ua[m], ub[m], mg, mq, a + 1);
+            if (VW > 0) {
+                Unpack<BITS>::template run<2>(&vw[t][0][m * BITS / 4], ua[m], ub[m], mg, mq, a);
+                Unpack<BITS>::template run<2>(&vw[t][1][m * BITS / 4], ua[m], ub[m], mg, mq, a + 1);
+            } else {
+                Unpack<BITS>::template run<2>(pr[m] + woff + (t * 16) * RW, ua[m], ub[m], mg, mq, a);
+                Unpack<BITS>::template run<2>(pr[m] + woff + (t * 16 + 8) * RW, ua[m], ub[m], mg, mq, a + 1);
+            }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 if (m == 0)
