@@ -7,7 +7,7 @@
  *
  *     y[r][n] = sum_k x[r][k] * (scale[n][k/G] * q[n][k] + bias[n][k/G])
  *
- * for 1..16 activation rows r.  q[n][k] is an unsigned code of `bits` bits
+ * for activation rows r (1..16 in one launch).  q[n][k] is an unsigned code of `bits` bits
  * (2, 3, 4, 5, 6 or 8), stored low code first in row n's little-endian
  * bitstream (3- and 5-bit rows hold eight codes in three or five bytes; every
  * row ends on a 32-bit word).  scale and bias are bf16, one per group of G = 32,
@@ -15,7 +15,7 @@
  *
  * Results: every output lies within (K * 2^-24 + 2^-20) * sum_k |x_k * w_k| of
  * the exact product; a row's bits depend on its own inputs only (the same in a
- * window of 1..16 rows), and a strided or stacked output equals the contiguous
+ * window of any size), and a strided or stacked output equals the contiguous
  * one bit for bit (the canonical order below fixes the arithmetic).
  *
  * Canonical order of one output y[r][n]: K is cut into segments of 256 k and
@@ -48,7 +48,7 @@ extern "C" {
 #define TF_OK 0
 #define TF_EINVAL_BITS (-1)   /* bits not in {2,3,4,5,6,8} */
 #define TF_EINVAL_GROUP (-2)  /* group not in {32,64,128}, or K % group != 0, or K < 1 */
-#define TF_EINVAL_ROWS (-3)   /* rows not in [1, 16] */
+#define TF_EINVAL_ROWS (-3)   /* rows not in [1, 16] (tf_qmm / tf_qmm_ex: [1, 65536]) */
 #define TF_EINVAL_STRIDE (-4) /* y_stride < N (a strided call writes rows at least a matrix wide) */
 #define TF_EINVAL_PTR (-5)    /* NULL pointer, or x / W not 16-byte aligned, y not 4-byte aligned */
 #define TF_EINVAL_SIZE (-6)   /* N < 1, or sizes too large for 32-bit indexing of one row */
@@ -68,6 +68,10 @@ extern "C" {
  *   scales   [N][K/group] bf16; biases likewise.
  *   y        fp32; row r, column n is y[r*y_stride + n] for n < N.  Columns
  *            N..y_stride-1 of each row are not touched.
+ *   rows     1..65536: more than 16 rows run as 16-row windows (independent
+ *            launches that overlap under programmatic dependent launch; the
+ *            weights are read once per window), each row's bits those of the
+ *            row alone -- the row / window gate of PR #788 extended past 16 rows.
  * Returns TF_OK or a negative status (checked on the host before any launch).
  */
 int tf_qmm(const uint16_t *x, int rows, int K,

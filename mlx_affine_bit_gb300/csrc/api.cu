@@ -7,6 +7,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <map>
 #include <mutex>
@@ -48,8 +49,12 @@ int check_matrix(int K, const uint32_t *W, const uint16_t *s, const uint16_t *b,
     return TF_OK;
 }
 
-int check_io(const uint16_t *x, int rows, const float *y) {
-    if (rows < 1 || rows > 16) return fail(TF_EINVAL_ROWS, "rows must be in [1, 16]");
+// Rows of one tf_qmm / tf_qmm_ex call: more than 16 run as 16-row windows.
+constexpr int MAX_ROWS = 65536;
+
+int check_io(const uint16_t *x, int rows, const float *y, int max_rows = 16) {
+    if (rows < 1 || rows > max_rows)
+        return fail(TF_EINVAL_ROWS, max_rows == 16 ? "rows must be in [1, 16]" : "rows must be in [1, 65536]");
     if (!x || !y) return fail(TF_EINVAL_PTR, "NULL x or y");
     if (!aligned(x, 16)) return fail(TF_EINVAL_PTR, "x must be 16-byte aligned");
     if (!aligned(y, 4)) return fail(TF_EINVAL_PTR, "y must be 4-byte aligned");
@@ -533,6 +538,28 @@ int tfq::fail_message(int code, const char *msg) { return fail(code, msg); }
 
 // ============================================================== C ABI ====
 
+// A product of any row count: up to 16 rows in one launch; more as 16-row
+// windows (rows r0..r0+15 read x rows and write y rows r0..), which run as
+// independent launches and overlap like the runs of a stack.  Each row's bits
+// are those of the row alone.
+int product_rows(const uint16_t *x, int rows, int K, const uint32_t *W, const uint16_t *s,
+                 const uint16_t *b, int N, int bits, int group, float *y, int64_t y_stride, int out,
+                 cudaStream_t st) {
+    const int src = 0, len = N, dst = 0;
+    Io io;
+    io.out = out;
+    if (rows <= 16) return run_product(x, rows, K, W, s, b, N, bits, group, y, y_stride, 1, &src, &len, &dst, st, -1, &io);
+    io.map = true;
+    int pos = 0;
+    for (int r0 = 0; r0 < rows; r0 += 16) {
+        const int w = std::min(16, rows - r0);
+        for (int r = 0; r < 16; ++r) io.xrow[r] = io.yrow[r] = r0 + std::min(r, w - 1);
+        const int rc = run_product(x, w, K, W, s, b, N, bits, group, y, y_stride, 1, &src, &len, &dst, st, pos++, &io);
+        if (rc) return rc;
+    }
+    return TF_OK;
+}
+
 extern "C" {
 
 int tf_qmm(const uint16_t *x, int rows, int K, const uint32_t *W, const uint16_t *scales,
@@ -541,12 +568,11 @@ int tf_qmm(const uint16_t *x, int rows, int K, const uint32_t *W, const uint16_t
     g_err.clear();
     int rc = check_matrix(K, W, scales, biases, N, bits, group);
     if (rc) return rc;
-    rc = check_io(x, rows, y);
+    rc = check_io(x, rows, y, MAX_ROWS);
     if (rc) return rc;
     if (y_stride < N) return fail(TF_EINVAL_STRIDE, "y_stride below N is refused");
-    const int src = 0, len = N, dst = 0;
-    return run_product(x, rows, K, W, scales, biases, N, bits, group, y, y_stride, 1, &src, &len,
-                       &dst, static_cast<cudaStream_t>(stream));
+    return product_rows(x, rows, K, W, scales, biases, N, bits, group, y, y_stride, 0,
+                        static_cast<cudaStream_t>(stream));
 }
 
 int tf_qmm_stack(const uint16_t *x, int rows, int K, const tf_run *runs, int n_runs,
@@ -604,15 +630,12 @@ int tf_qmm_ex(const uint16_t *x, int rows, int K, const uint32_t *W, const uint1
     if (flags & ~(TF_OUT_BF16 | TF_EPI_RELU2)) return fail(TF_EINVAL_FLAGS, "unknown output flags");
     int rc = check_matrix(K, W, scales, biases, N, bits, group);
     if (rc) return rc;
-    if (rows < 1 || rows > 16) return fail(TF_EINVAL_ROWS, "rows must be in [1, 16]");
+    if (rows < 1 || rows > MAX_ROWS) return fail(TF_EINVAL_ROWS, "rows must be in [1, 65536]");
     if (!x || !y || !aligned(x, 16) || !aligned(y, (flags & TF_OUT_BF16) ? 2 : 4))
         return fail(TF_EINVAL_PTR, "NULL pointer, x not 16-byte aligned, or y not aligned to its type");
     if (y_stride < N) return fail(TF_EINVAL_STRIDE, "y_stride below N is refused");
-    Io io;
-    io.out = flags;
-    const int src = 0, len = N, dst = 0;
-    return run_product(x, rows, K, W, scales, biases, N, bits, group, static_cast<float *>(y), y_stride, 1,
-                       &src, &len, &dst, static_cast<cudaStream_t>(stream), -1, &io);
+    return product_rows(x, rows, K, W, scales, biases, N, bits, group, static_cast<float *>(y), y_stride,
+                        flags, static_cast<cudaStream_t>(stream));
 }
 
 int tf_qmm_gather(const uint16_t *x, int x_rows, int K, const tf_run *experts, int n_experts,

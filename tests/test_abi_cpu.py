@@ -36,7 +36,7 @@ A = 4096  # a 16-byte aligned stand-in address; no call below reaches the device
 @pytest.mark.parametrize("kw,code", [
     (dict(bits=7), -1), (dict(bits=1), -1),
     (dict(group=48), -2), (dict(group=64, K=96), -2), (dict(K=16, group=32), -2),
-    (dict(rows=0), -3), (dict(rows=17), -3),
+    (dict(rows=0), -3), (dict(rows=65537), -3),
     (dict(y_stride=255), -4),
     (dict(x=0), -5), (dict(W=0), -5), (dict(x=A + 8), -5), (dict(W=A + 4), -5), (dict(y=A + 2), -5),
     (dict(N=0, y_stride=0), -6),
@@ -102,7 +102,7 @@ def test_output_option_refusals_on_host(tf):
     # unknown flag bits; bf16 y needs 2-byte alignment only, fp32 y 4-byte
     assert L.tf_qmm_ex(A, 1, 1024, A, A, A, 256, 4, 64, A, 256, 4, None) == -12
     assert L.tf_qmm_ex(A, 1, 1024, A, A, A, 256, 4, 64, A + 2, 256, 0, None) == -5
-    assert L.tf_qmm_ex(A, 17, 1024, A, A, A, 256, 4, 64, A, 256, 1, None) == -3
+    assert L.tf_qmm_ex(A, 65537, 1024, A, A, A, 256, 4, 64, A, 256, 1, None) == -3
     assert L.tf_qmm_ex(A, 1, 1024, A, A, A, 256, 4, 64, A, 255, 3, None) == -4
 
 
@@ -127,3 +127,9 @@ def test_gather_stride_and_flags_refused(tf):
     with pytest.raises(tf.TfError) as e:
         tf.tf_qmm_gather(A, 3, 256, experts, [0], [0], A, 96, 8, stream=0)
     assert e.value.rc == -12
+
+
+def test_stack_keeps_16_rows(tf):
+    with pytest.raises(tf.TfError) as e:
+        tf.tf_qmm_stack(A, 17, 256, [(A, A, A, 64, 4, 64)], [(0, 0, 64, 0)], A, 64, stream=0)
+    assert e.value.rc == -3

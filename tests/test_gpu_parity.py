@@ -416,3 +416,33 @@ def test_gather_equals_dense(flags):
         t, B = oracle.bound_out(y64, absum, K, bool(flags & tf.TF_EPI_RELU2), bf)
         got = _bf16_bits_to_f64(y[i:i + 1, cols]) if bf else y[i:i + 1, cols].cpu().numpy().astype(np.float64)
         assert np.all(np.abs(got - t) <= B)
+
+
+@pytest.mark.parametrize("rows", [17, 33, 65])
+@pytest.mark.parametrize("flags", [0, tf.TF_OUT_BF16 | tf.TF_EPI_RELU2])
+def test_rows_past_16(rows, flags):
+    # More than 16 rows run as 16-row windows: every row equals the same row
+    # computed alone, bit for bit, and the product stays within the bound.
+    m = synth.make_matrix(700, 2048, 5, 64, 170, 0.001, 0.03)
+    dm = DevMatrix(m)
+    x = synth.make_x(rows, m.K, 171 + rows)
+    xd = dev(x)
+    bf = bool(flags & tf.TF_OUT_BF16)
+    dt = torch.int16 if bf else torch.float32
+
+    def call(xs):
+        y = torch.zeros((xs.shape[0], m.N), dtype=dt, device=DEV)
+        tf.tf_qmm_ex(xs, xs.shape[0], m.K, dm.W, dm.s, dm.b, m.N, m.bits, m.group, y, m.N, flags)
+        return y
+
+    y = call(xd)
+    for r in (0, 15, 16, rows - 1):
+        assert torch.equal(call(xd[r:r + 1].contiguous())[0], y[r]), r
+    if flags == 0:
+        y2 = run_qmm(dm, xd)                                   # tf_qmm takes any row count too
+        assert torch.equal(y2.view(torch.int32), y.view(torch.int32))
+    cols = sample_cols(m.N, 24, rows)
+    y64, absum = oracle.qmm(x, m.W, m.scales, m.biases, m.N, m.K, m.bits, m.group, cols=cols, nthreads=8)
+    t, B = oracle.bound_out(y64, absum, m.K, bool(flags & tf.TF_EPI_RELU2), bf)
+    got = _bf16_bits_to_f64(y[:, cols]) if bf else y[:, cols].cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - t) <= B)
