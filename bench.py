@@ -465,9 +465,15 @@ def run_gpu(args, cases):
             cores = os.cpu_count() or 1
             gbs, secs, nb = cpu_sample(cpu_cases, 1, cores)      # probe
             cols = max(1, min(4096, int(12.0 / max(secs, 1e-3))))
-            gbs, secs, nb = cpu_sample(cpu_cases, cols, cores)
-            cpu = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                   "sample": "fp64 oracle on the first %d output columns of each product (%.1f s)" % (cols, secs)}
+            # About 10 s of oracle work: the column sample, repeated when even the
+            # whole workload takes less.
+            secs, nb, reps = 0.0, 0, 0
+            while secs < 10.0 and reps < 200:
+                _, t, b = cpu_sample(cpu_cases, cols, cores)
+                secs, nb, reps = secs + t, nb + b, reps + 1
+            cpu = {"value": nb / secs / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                   "sample": "fp64 oracle on the first %d output columns of each product, %d pass%s (%.1f s)"
+                             % (cols, reps, "" if reps == 1 else "es", secs)}
         print(json.dumps({
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
