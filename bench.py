@@ -132,13 +132,19 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+_CPU_INPUTS = {}
+
+
 def cpu_sample(cases, cols_per_case: int, nthreads: int):
     """Time the oracle on `cols_per_case` columns of every case; (GB/s, seconds, desc)."""
     import oracle
     total_bytes, t_total = 0, 0.0
     for (label, N, K, bits, group, seed, rows) in cases:
-        m = synth.make_matrix(min(N, 4096), K, bits, group, seed, 0.001, 0.03)
-        x = synth.make_x(rows, K, seed)
+        key = (N, K, bits, group, seed, rows)
+        if key not in _CPU_INPUTS:            # generated once, outside the timing
+            _CPU_INPUTS[key] = (synth.make_matrix(min(N, 4096), K, bits, group, seed, 0.001, 0.03),
+                                synth.make_x(rows, K, seed))
+        m, x = _CPU_INPUTS[key]
         cols = np.arange(min(cols_per_case, m.N), dtype=np.int64)
         t0 = time.perf_counter()
         oracle.qmm(x, m.W, m.scales, m.biases, m.N, K, bits, group, cols=cols, nthreads=nthreads)
