@@ -369,7 +369,6 @@ int run_product(const uint16_t *x, int rows, int K, const uint32_t *W, const uin
     P.nsl = pl.nsl;
     P.sl = pl.sl;
     P.nchunks = pl.nchunks;
-    P.n_items = pl.nmt * pl.nsl;
     P.stages = pl.stages;
     P.bulk = bulk;
     P.sb3d = sb3d;
@@ -377,7 +376,6 @@ int run_product(const uint16_t *x, int rows, int K, const uint32_t *W, const uin
         rc = tensor_maps(W, s, b, N, K, bits, group, pl, P);
         if (rc) return rc;
     }
-    P.segpitch = pl.segpitch;
     P.sbpitch = pl.sbpitch;
     P.stage_bytes = pl.stage_bytes;
     P.x_off = pl.x_off;
@@ -485,7 +483,6 @@ int tfq::product_with_scratch(const uint16_t *x, int rows, int K, const uint32_t
     P.nsl = pl.nsl;
     P.sl = pl.sl;
     P.nchunks = pl.nchunks;
-    P.n_items = pl.nmt * pl.nsl;
     P.stages = pl.stages;
     P.bulk = bulk;
     P.sb3d = sb3d;
@@ -507,7 +504,6 @@ int tfq::product_with_scratch(const uint16_t *x, int rows, int K, const uint32_t
         }
         if (rc) return rc;
     }
-    P.segpitch = pl.segpitch;
     P.sbpitch = pl.sbpitch;
     P.stage_bytes = pl.stage_bytes;
     P.x_off = pl.x_off;

@@ -53,10 +53,9 @@ struct QmmParams {
     int *status;        // device status word (bounded waits that ran out)
     long long y_stride;
     int rows, K, N;
-    int nmt;            // m-tiles of TN columns
+    int nmt;            // column tiles of TN * MT columns (items per K slice)
     int nsl, sl;        // K slices and slice length (multiple of CHUNK)
     int nchunks;
-    int n_items;        // nmt * nsl, slice-major
     int stages;         // pipeline depth
     int bulk;           // 1: tensor-map TMA copies; 0: copies by the producer warp
     int sb3d;           // 1: scale/bias rows padded through a 3D map (K % CHUNK == 0)
@@ -64,7 +63,6 @@ struct QmmParams {
     int dep;            // programmatic dependent launch: 0 wait before x/y, release the next
                         // launch at once; 1 release it only after that wait (first run of a
                         // stack); 2 no wait before x/y, wait before exit (later runs of a stack)
-    int segpitch;       // bytes per W row inside a segment block (SEG*bits/8 + 16)
     int sbpitch;        // bytes per scale (or bias) row in a stage
     int stage_bytes;    // W blocks + scales + biases
     int x_off, sx_off, pb_off, z_off, st_off;   // smem offsets
