@@ -4,16 +4,16 @@
 // (TensorFold PR #788, commit "every MLX affine width in the row kernel"; the
 // group-sum form with fp32 group sums, PR #774 Exactness, Precision bullet).
 //
-// One CTA = 8 consumer warps + 1 producer warp, persistent over work items
-// (16 output columns x one K slice).  A pipeline stage is those 16 rows x
-// 2048 k: one 3D tensor-map TMA copy for the codes (a contiguous 8-32 KB of
-// HBM when the slice is the whole row) and one each for scales and biases,
-// completed on mbarriers.  Each consumer warp takes one 256-k segment of the
-// stage: it unpacks 8-code runs straight into bf16 A fragments (codes exact),
-// multiplies them by the activations with mma.sync m16n8k16 (rows are the N
-// dimension: 1..8 rows cost one MMA, 9..16 two), applies each group's scale
-// and bias to the fp32 group sum in registers, and the segment partials are
-// folded in k order through shared memory.
+// One CTA = one or two consumer groups of 8 warps + 1 producer warp,
+// persistent over work items (16 or 32 output columns x one K slice).  A
+// pipeline stage is those rows x 2048 k: one 3D tensor-map TMA copy for the
+// codes (a contiguous 8-64 KB of HBM when the slice is the whole row) and one
+// each for scales and biases, completed on mbarriers.  Warp w of a group takes
+// segment w (256 k) of a stage: it unpacks 8-code runs straight into bf16 A
+// fragments (codes exact), multiplies them by the activations with mma.sync
+// m16n8k16 (rows are the N dimension: 1..8 rows cost one MMA, 9..16 two),
+// applies each group's scale and bias to the fp32 group sum in registers, and
+// the segment partials are folded in k order through shared memory.
 //
 // Every wait on an mbarrier is bounded in time; on expiry the kernel records
 // it in the device status word, stops waiting and runs to completion.
