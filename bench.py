@@ -92,9 +92,8 @@ class ClockSampler:
 
     def start(self):
         try:
-            out = os.path.join(ROOT, "gpurun_out")
-            os.makedirs(out, exist_ok=True)
-            self.path = os.path.join(out, "clocks_%d.csv" % os.getpid())
+            import tempfile
+            self.path = os.path.join(tempfile.gettempdir(), "tfqmm_clocks_%d.csv" % os.getpid())
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
                                           "--format=csv,noheader,nounits", "-lms", "50"],
