@@ -303,8 +303,17 @@ __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
 // Code i of an 8-code run is paired with code i+4, so a run x0..x7 feeds its
 // first step as {(x0,x4),(x1,x5)} and its second as {(x2,x6),(x3,x7)}.
 // sum_group(x) is the sequential fp32 sum of the group's x in k order, from 0.
+// Two forms with the same result: one thread per (group, row) loads, places
+// and sums its group (load_x_groups), or every thread places 8-value pieces and
+// one thread per (group, row) then sums its group from shared memory
+// (load_x_pieces).  With groups of 64 or 128 the first form's long per-group
+// loops leave most threads idle: the second measured 0.3-0.5 us faster per
+// 4096 x 4096 product and 0.4 us per 16-row 6192 x 2048 stack, but 0.3 us
+// slower on that stack at one row (two rows and a 2048 slice keep the first
+// form); with 32-wide groups the second pass's bank conflicts make it slower
+// (0.3-1.4 us at 8-16 rows).  Threads 0..nthr-1 run either.
 template <int G, int RB>
-__device__ void load_x_slice(const QmmParams &P, const Item &I, uint4 *Bf, float *sx, int tid, int nthr) {
+__device__ void load_x_groups(const QmmParams &P, const Item &I, uint4 *Bf, float *sx, int tid, int nthr) {
     static_assert(RB >= 2, "layout rows");
     const int rows = P.rows;
     const int ngs = (I.k_hi - I.k_lo) / G;
@@ -328,6 +337,67 @@ __device__ void load_x_slice(const QmmParams &P, const Item &I, uint4 *Bf, float
             acc += bf16f((uint16_t)(v.z >> 16));
             acc += bf16f((uint16_t)(v.w & 0xFFFF));
             acc += bf16f((uint16_t)(v.w >> 16));
+        }
+        sx[gs * RB + r] = acc;
+    }
+}
+
+// B-layout slot of piece pc (the 8 x values at slice offset 8*pc) of row r.
+template <int G, int RB>
+__device__ __forceinline__ int piece_slot(int pc, int r) {
+    constexpr int PPG = G / 8;                       // pieces of a group
+    const int gs = pc / PPG, t = pc - gs * PPG;
+    const int qq = (8 * t) / (G / 4), m = ((8 * t) % (G / 4)) / 8;
+    return ((gs * (G / 32) + m) * RB + r) * 4 + qq;
+}
+
+// Piece form; `bar` is the threads' named barrier between the two passes.
+template <int G, int RB>
+__device__ void load_x_pieces(const QmmParams &P, const Item &I, uint4 *Bf, float *sx, int tid, int nthr,
+                              int bar) {
+    static_assert(RB >= 2, "layout rows");
+    constexpr int BATCH = 4;                         // loads a thread keeps in flight
+    const int rows = P.rows;
+    const int npc = (I.k_hi - I.k_lo) / 8;           // pieces of one row
+    const int total = RB * npc;
+    for (int u0 = tid; u0 < total; u0 += BATCH * nthr) {
+        uint4 v[BATCH];
+#pragma unroll
+        for (int j = 0; j < BATCH; ++j) {
+            const int u = u0 + j * nthr;
+            const int r = u / npc, pc = u - r * npc;
+            v[j] = make_uint4(0u, 0u, 0u, 0u);
+            if (u < total && r < rows)
+                v[j] = *reinterpret_cast<const uint4 *>(P.x + (long long)P.xrow[r] * P.K + I.k_lo + 8 * pc);
+        }
+#pragma unroll
+        for (int j = 0; j < BATCH; ++j) {
+            const int u = u0 + j * nthr;
+            const int r = u / npc, pc = u - r * npc;
+            if (u < total)
+                Bf[piece_slot<G, RB>(pc, r)] = make_uint4(prmt(v[j].x, v[j].z, 0x5410u), prmt(v[j].x, v[j].z, 0x7632u),
+                                                          prmt(v[j].y, v[j].w, 0x5410u), prmt(v[j].y, v[j].w, 0x7632u));
+        }
+    }
+    named_bar(bar, nthr);
+    const int ngs = npc / (G / 8);
+    for (int u = tid; u < RB * ngs; u += nthr) {
+        const int r = u / ngs, gs = u - r * ngs;
+        float acc = 0.f;
+        if (r < rows) {
+#pragma unroll
+            for (int t = 0; t < G / 8; ++t) {
+                // Stored pairs (x0,x4) (x1,x5) (x2,x6) (x3,x7): add x0..x7 in order.
+                const uint4 w = Bf[piece_slot<G, RB>(gs * (G / 8) + t, r)];
+                acc += bf16f((uint16_t)(w.x & 0xFFFF));
+                acc += bf16f((uint16_t)(w.y & 0xFFFF));
+                acc += bf16f((uint16_t)(w.z & 0xFFFF));
+                acc += bf16f((uint16_t)(w.w & 0xFFFF));
+                acc += bf16f((uint16_t)(w.x >> 16));
+                acc += bf16f((uint16_t)(w.y >> 16));
+                acc += bf16f((uint16_t)(w.z >> 16));
+                acc += bf16f((uint16_t)(w.w >> 16));
+            }
         }
         sx[gs * RB + r] = acc;
     }
@@ -541,7 +611,10 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
         if (I.slice != cur_slice) {
             // Every group walks every item, so all consumers meet here.
             named_bar(1, CG * GT);
-            load_x_slice<G, LR>(P, I, Bf, sx, tid, CG * GT);
+            if (G >= 64 && (LR > 2 || I.k_hi - I.k_lo >= 4096))
+                load_x_pieces<G, LR>(P, I, Bf, sx, tid, CG * GT, 1);
+            else
+                load_x_groups<G, LR>(P, I, Bf, sx, tid, CG * GT);
             named_bar(1, CG * GT);
             cur_slice = I.slice;
         }
