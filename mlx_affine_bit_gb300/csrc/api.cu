@@ -102,7 +102,7 @@ Plan layout(int N, int K, int bits, int group, int rows, int nsm, int ctas, bool
     p.nsl = ceil_div(p.nchunks, best_cps);
     const int len = std::min(p.sl, K);
     const int sbg = CHUNK / group;                          // groups of one stage
-    p.segpitch = SEG * bits / 8 + 16;
+    p.segpitch = SEG * bits / 8 + 4 * seg_pad_words(bits, group);
     p.sbpitch = sb3d ? (sbg + 8) * 2 : sbg * 2;
     p.stage_bytes = SEGS * rws * p.segpitch + 2 * rws * p.sbpitch;
     const int x_bytes = (lr * len * 2 + 127) & ~127;
@@ -235,7 +235,7 @@ int tensor_maps(const uint32_t *W, const uint16_t *s, const uint16_t *b, int N, 
         // one stage lands segment-major with a row pitch of segment + 16 bytes
         // (the 4 words past each segment's extent are zero-filled, not read).
         rc = encode_3d(&ms.W, W, CU_TENSOR_MAP_DATA_TYPE_UINT32, segw, N, K / SEG, rowb, segw * 4,
-                       (int)segw + 4, TN * pl.mt, SEGS);
+                       (int)segw + seg_pad_words(bits, group), TN * pl.mt, SEGS);
         const int sbg = CHUNK / group;
         for (int i = 0; i < 2 && !rc; ++i) {
             CUtensorMap *m = i ? &ms.b : &ms.s;
@@ -491,7 +491,7 @@ int tfq::product_with_scratch(const uint16_t *x, int rows, int K, const uint32_t
         if (rc) return rc;
         const long long segw = SEG * bits / 32, rowb = (long long)K * bits / 8;
         rc = encode_3d(&P.tmW, W, CU_TENSOR_MAP_DATA_TYPE_UINT32, segw, N, K / SEG, rowb, segw * 4,
-                       (int)segw + 4, TN * pl.mt, SEGS);
+                       (int)segw + seg_pad_words(bits, group), TN * pl.mt, SEGS);
         const int sbg = CHUNK / group;
         for (int i = 0; i < 2 && !rc; ++i) {
             CUtensorMap *m = i ? &P.tmB : &P.tmS;

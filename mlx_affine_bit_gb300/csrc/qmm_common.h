@@ -36,11 +36,19 @@ TFQ_HD constexpr int row_bucket(int rows) {
     return rows == 1 ? 1 : rows <= 2 ? 2 : rows <= 4 ? 4 : rows <= 8 ? 8 : 16;
 }
 TFQ_HD constexpr int layout_rows(int rb) { return rb < 2 ? 2 : rb; }
+
+// Zero words after each row segment of a stage (the TMA box reads them past the
+// segment's extent).  Four in general; 4-bit rows with groups of 64 or 128 and
+// 8-bit rows with groups of 64 take the pad at which no two lanes of a warp's
+// code loads share a shared-memory bank (with four words they would in pairs).
+TFQ_HD constexpr int seg_pad_words(int bits, int group) {
+    return (bits == 4 && group == 64) ? 8 : ((bits == 4 && group == 128) || (bits == 8 && group == 64)) ? 16 : 4;
+}
 constexpr int ZERO_BYTES = 2048;           // zero block that idle lanes of small buckets read
 
 struct QmmParams {
     // TMA descriptors (bulk mode).  W: [K/SEG segments][N rows][SEG*bits/32
-    // words], box {segment + 4 words past its extent (zero filled), the
+    // words], box {segment + seg_pad_words past its extent (zero filled), the
     // stage's rows, 8 segments}; scales/biases: one stage's groups of its rows.
     CUtensorMap tmW, tmS, tmB;
     const uint16_t *x;

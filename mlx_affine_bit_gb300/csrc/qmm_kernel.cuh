@@ -197,17 +197,17 @@ struct Ring {
 // -------------------------------------------------------------- producer --
 
 // Stage layout: W [SEGS segments][ROWS rows][SEGP bytes], then scales and
-// biases [ROWS rows][sbpitch bytes] each.  SEGP = segment bytes + 16.
-template <int BITS>
+// biases [ROWS rows][sbpitch bytes] each.  SEGP = segment bytes + the pad.
+template <int BITS, int G>
 struct Pitch {
-    static constexpr int SEGP = SEG * BITS / 8 + 16;
+    static constexpr int SEGP = SEG * BITS / 8 + 4 * seg_pad_words(BITS, G);
 };
 
 template <int BITS, int G, int MT>
 __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint64_t *empty,
                          volatile int *abort) {
     constexpr int ROWS = TN * MT;
-    constexpr int SEGP = Pitch<BITS>::SEGP;
+    constexpr int SEGP = Pitch<BITS, G>::SEGP;
     constexpr int SEGW = SEG * BITS / 32;     // words of one row segment
     const int lane = threadIdx.x & 31;
     const int S = P.stages;
@@ -436,11 +436,13 @@ struct SegVals<2> {
 // One group of this lane's 2*MT columns (rows t*16+g and t*16+g+8 of each
 // m-tile t): T = tensor-core dot products of the group's exact codes with x,
 // then p = fma(s,T,p); p = fma(b,sum_group(x),p).  pr[m]: run m of the lane's
-// quarter in row g of m-tile 0 (other rows at compile-time offsets); woff: the
-// group's word offset in the segment row; bq: this lane's B entry of the
-// group's first run (shared by the m-tiles); sxq: the group's sum_group(x).
+// quarter in row g of m-tile 0 (other rows at compile-time offsets); for 6-bit
+// codes pr[m] / pr2[m] are the run's first / second word in this lane's load
+// order; woff: the group's word offset in the segment row; bq: this lane's B
+// entry of the group's first run (shared by the m-tiles); sxq: the group's
+// sum_group(x).
 template <int BITS, int G, int RB, int MT>
-__device__ __forceinline__ void group_body(const uint32_t *const (&pr)[G / 32],
+__device__ __forceinline__ void group_body(const uint32_t *const (&pr)[G / 32], const uint32_t *const (&pr2)[G / 32],
                                            const uint32_t (&ua)[G / 32], const uint32_t (&ub)[G / 32],
                                            uint32_t mg, uint32_t mq, int woff, const uint4 *bq, const float (&sg)[MT][2],
                                            const float (&bg)[MT][2], const float *sxq,
@@ -448,7 +450,7 @@ __device__ __forceinline__ void group_body(const uint32_t *const (&pr)[G / 32],
     constexpr int NT = RB > 8 ? 2 : 1;
     constexpr int LR = layout_rows(RB);
     constexpr int RUNS = G / 32;
-    constexpr int RW = Pitch<BITS>::SEGP / 4;     // words between rows of a segment block
+    constexpr int RW = Pitch<BITS, G>::SEGP / 4;     // words between rows of a segment block
     // 4- and 8-bit runs of a lane lie in consecutive aligned words: with two or
     // four runs a group, one vector load per row feeds them all.
     constexpr int VW = (BITS == 4 || BITS == 8) && RUNS >= 2 ? RUNS * BITS / 4 : 0;   // words
@@ -484,6 +486,10 @@ __device__ __forceinline__ void group_body(const uint32_t *const (&pr)[G / 32],
             if (VW > 0) {
                 Unpack<BITS>::template run<2>(&vw[t][0][m * BITS / 4], ua[m], ub[m], mg, mq, a);
                 Unpack<BITS>::template run<2>(&vw[t][1][m * BITS / 4], ua[m], ub[m], mg, mq, a + 1);
+            } else if constexpr (BITS == 6) {
+                const int o0 = woff + (t * 16) * RW, o1 = woff + (t * 16 + 8) * RW;
+                Unpack<6>::template run_words<2>(pr[m][o0], pr2[m][o0], ua[m], ub[m], mg, mq, a);
+                Unpack<6>::template run_words<2>(pr[m][o1], pr2[m][o1], ua[m], ub[m], mg, mq, a + 1);
             } else {
                 Unpack<BITS>::template run<2>(pr[m] + woff + (t * 16) * RW, ua[m], ub[m], mg, mq, a);
                 Unpack<BITS>::template run<2>(pr[m] + woff + (t * 16 + 8) * RW, ua[m], ub[m], mg, mq, a + 1);
@@ -557,7 +563,7 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                          volatile int *abort, const volatile uint32_t *magic) {
     constexpr int NT = RB > 8 ? 2 : 1;
     constexpr int ROWS = TN * MT;
-    constexpr int SEGP = Pitch<BITS>::SEGP;
+    constexpr int SEGP = Pitch<BITS, G>::SEGP;
     constexpr int QG = G / 4;                // codes of a group per quad lane
     constexpr int RUNS = G / 32;             // 8-code runs per quad lane per group
     constexpr int GW = G * BITS / 32;        // words per group of one row
@@ -583,12 +589,25 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
         for (int i = tid; i < ZERO_BYTES / 4; i += CG * GT) reinterpret_cast<uint32_t *>(smem + P.z_off)[i] = 0u;
     }
     // This lane's runs inside any group: word offset and unpack arguments of run m.
+    // A 6-bit run spans two words; with groups of 32 or 128 lanes whose quarter
+    // starts at words {0,1,3,4} (or {0,6,12,18}) + a multiple of 4 per row would
+    // meet in pairs on one bank, so half the lanes load the second word first
+    // (their selectors flipped to match): every load is then conflict-free.
+    // The one- and two-row kernels with two consumer groups keep the plain
+    // order: under their 96-register cap the second pointer set spills (the
+    // 6-bit LM head measured 6 % slower), and they wait least on shared memory.
+    constexpr bool SWAP6 = BITS == 6 && !(RB <= 2 && CG == 2);
+    const uint32_t d6 = (SWAP6 && ((G == 32 && !(q & 1)) || (G == 128 && q < 2))) ? 1u : 0u;
     uint32_t wo[RUNS], ua[RUNS], ub[RUNS];
 #pragma unroll
     for (int m = 0; m < RUNS; ++m) {
         const uint32_t bit = (uint32_t)(q * QG + 8 * m) * BITS;
         wo[m] = bit >> 5;
         lane_args<BITS>(bit & 31u, ua[m], ub[m]);
+        if (d6) {
+            ua[m] ^= 0x4444u;
+            ub[m] ^= 0x4444u;
+        }
     }
     float yacc[OUTS];
 #pragma unroll
@@ -646,9 +665,12 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
             if (active) {
                 const uint8_t *st = smem + P.st_off + slot * P.stage_bytes;
                 const uint32_t *wr = reinterpret_cast<const uint32_t *>(st + (warp * ROWS + g) * SEGP);
-                const uint32_t *pr[RUNS];
+                const uint32_t *pr[RUNS], *pr2[RUNS];
 #pragma unroll
-                for (int m = 0; m < RUNS; ++m) pr[m] = wr + wo[m];
+                for (int m = 0; m < RUNS; ++m) {
+                    pr[m] = wr + wo[m] + d6;
+                    pr2[m] = wr + wo[m] + (1u - d6);
+                }
                 const uint8_t *sbase = st + SEGS * ROWS * SEGP;
                 const int gseg = warp * NGS;                             // segment's first group in the stage
                 const int gs0 = (ks0 - I.k_lo) / G;                      // slice group index
@@ -685,7 +707,7 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                                     sg[t][h] = Sv[t][h].get(gv);
                                     bg[t][h] = Bv[t][h].get(gv);
                                 }
-                            group_body<BITS, G, RB, MT>(pr, ua, ub, mg, mq, gl * GW, bq + gl * RUNS * LR * 4, sg,
+                            group_body<BITS, G, RB, MT>(pr, pr2, ua, ub, mg, mq, gl * GW, bq + gl * RUNS * LR * 4, sg,
                                                         bg, sxq + gl * LR, p);
                         }
                     }
@@ -700,7 +722,7 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                                 sg[t][h] = bf16f(sp[(2 * t + h) * rstep + gl]);
                                 bg[t][h] = bf16f(bp[(2 * t + h) * rstep + gl]);
                             }
-                        group_body<BITS, G, RB, MT>(pr, ua, ub, mg, mq, gl * GW, bq + gl * RUNS * LR * 4, sg, bg,
+                        group_body<BITS, G, RB, MT>(pr, pr2, ua, ub, mg, mq, gl * GW, bq + gl * RUNS * LR * 4, sg, bg,
                                                     sxq + gl * LR, p);
                     }
                 }

@@ -224,8 +224,16 @@ struct Unpack<6> {  // 48 bits; sh in {0, 16}
     // Run bytes {0,1,3,4} and {1,2,4,5}; raw byte = run byte + sh/8 (sh = 0 or 16).
     template <int ST = 1>
     static TF_HD void run(const uint32_t *w, uint32_t s0, uint32_t s2, uint32_t mg, uint32_t mq, uint32_t *p) {
-        uint32_t P0 = prmt(w[0], w[1], s0);   // c0 @0, c1 @6 | c4 @16, c5 @22
-        uint32_t P2 = prmt(w[0], w[1], s2);   // c2 @4, c3 @10 | c6 @20, c7 @26
+        run_words<ST>(w[0], w[1], s0, s2, mg, mq, p);
+    }
+    // The run's two words passed in (a, b) = (w[0], w[1]); the same pairs come
+    // from (a, b) = (w[1], w[0]) with both selectors XOR 0x4444 (each selector
+    // byte index then names the other operand's byte).
+    template <int ST = 1>
+    static TF_HD void run_words(uint32_t a, uint32_t b, uint32_t s0, uint32_t s2, uint32_t mg, uint32_t mq,
+                                uint32_t *p) {
+        uint32_t P0 = prmt(a, b, s0);   // c0 @0, c1 @6 | c4 @16, c5 @22
+        uint32_t P2 = prmt(a, b, s2);   // c2 @4, c3 @10 | c6 @20, c7 @26
         p[0 * ST] = at0(P0, 0x003F003Fu, mg);
         p[1 * ST] = at0(P0 >> 6, 0x003F003Fu, mg);
         p[2 * ST] = at0(P2 >> 4, 0x003F003Fu, mg);

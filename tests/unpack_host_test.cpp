@@ -35,6 +35,11 @@ static int check(std::mt19937 &rng, int sh) {
         uint32_t p2[8];
         tfq::Unpack<BITS>::template run<2>(w, ua, ub, tfq::MAGIC, tfq::QP<BITS>::value, p2);
         for (int i = 0; i < 4; ++i) if (p2[2 * i] != p[i]) { printf("stride mismatch\n"); ++bad; }
+        if (BITS == 6) {   // the two words in swapped order with flipped selectors
+            uint32_t p3[4];
+            tfq::Unpack<6>::template run_words<1>(w[1], w[0], ua ^ 0x4444u, ub ^ 0x4444u, tfq::MAGIC, 0u, p3);
+            for (int i = 0; i < 4; ++i) if (p3[i] != p[i]) { printf("swapped words mismatch\n"); ++bad; }
+        }
         for (int i = 0; i < 4; ++i) {
             int lo = bf16_int((uint16_t)(p[i] & 0xFFFF)), hi = bf16_int((uint16_t)(p[i] >> 16));
             int want_lo = (int)bit_code(w, BITS, sh, i), want_hi = (int)bit_code(w, BITS, sh, i + 4);
