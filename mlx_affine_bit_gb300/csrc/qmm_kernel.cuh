@@ -736,17 +736,19 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                 __syncwarp();
                 if (lane == 0) mbar_arrive_after(&empty[slot], dep);
             }
-            // Segment partial -> pbuf[buf][warp][row][padded activation row].
+            // Segment partial -> pbuf[buf][warp][row][padded activation row];
+            // a lane's two activation rows are adjacent: one 8-byte store.
             float *pw = pbuf + ((buf * SEGS + warp) * ROWS) * LR;
 #pragma unroll
             for (int t = 0; t < MT; ++t)
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int r = nt * 8 + 2 * q + (e & 1);
-                        const int c = t * 16 + g + 8 * (e >> 1);
-                        if (r < LR) pw[c * LR + r] = p[t][nt][e];
+                    for (int h = 0; h < 2; ++h) {
+                        const int r = nt * 8 + 2 * q;
+                        const int c = t * 16 + g + 8 * h;
+                        if (r < LR)
+                            *reinterpret_cast<float2 *>(pw + c * LR + r) = make_float2(p[t][nt][2 * h], p[t][nt][2 * h + 1]);
                     }
             named_bar(gbar, GT);
             // Chunk sum C = P_0 + P_1 + ... in segment order, then the chunk fold.
