@@ -433,9 +433,19 @@ struct SegVals<2> {
     }
 };
 
+// Codes below 8 bits enter the MMA as 128 + c; 8-bit codes as c.
+__host__ __device__ constexpr bool offset_codes(int bits) { return bits != 8; }
+
+// The group's bias coefficient: b, or b - 128 s (one rounding) for offset codes.
+template <int BITS>
+__device__ __forceinline__ float bias_term(float s, float b) {
+    return offset_codes(BITS) ? fmaf(-128.f, s, b) : b;
+}
+
 // One group of this lane's 2*MT columns (rows t*16+g and t*16+g+8 of each
-// m-tile t): T = tensor-core dot products of the group's exact codes with x,
-// then p = fma(s,T,p); p = fma(b,sum_group(x),p).  pr[m]: run m of the lane's
+// m-tile t): T = tensor-core dot products of the group's codes with x (exact
+// codes c at 8 bits, offset codes 128 + c below), then p = fma(s,T,p);
+// p = fma(b',sum_group(x),p); bg holds b' = b, or b - 128 s for offset codes.  pr[m]: run m of the lane's
 // quarter in row g of m-tile 0 (other rows at compile-time offsets); for 6-bit
 // codes pr[m] / pr2[m] are the run's first / second word in this lane's load
 // order; woff: the group's word offset in the segment row; bq: this lane's B
@@ -451,6 +461,9 @@ __device__ __forceinline__ void group_body(const uint32_t *const (&pr)[G / 32], 
     constexpr int LR = layout_rows(RB);
     constexpr int RUNS = G / 32;
     constexpr int RW = Pitch<BITS, G>::SEGP / 4;     // words between rows of a segment block
+    // Below 8 bits the MMA takes the offset codes 128 + c (one instruction per
+    // pair less): T' = T + 128 sum_group(x), and bg holds b - 128 s.
+    constexpr bool OFF = offset_codes(BITS);
     // 4- and 8-bit runs of a lane lie in consecutive aligned words: with two or
     // four runs a group, one vector load per row feeds them all.
     constexpr int VW = (BITS == 4 || BITS == 8) && RUNS >= 2 ? RUNS * BITS / 4 : 0;   // words
@@ -484,15 +497,15 @@ __device__ __forceinline__ void group_body(const uint32_t *const (&pr)[G / 32], 
             // A registers in MMA operand order: a[2i] = pair i of row g, a[2i+1] of row g+8.
             uint32_t a[8];
             if (VW > 0) {
-                Unpack<BITS>::template run<2>(&vw[t][0][m * BITS / 4], ua[m], ub[m], mg, mq, a);
-                Unpack<BITS>::template run<2>(&vw[t][1][m * BITS / 4], ua[m], ub[m], mg, mq, a + 1);
+                Unpack<BITS>::template run<2, OFF>(&vw[t][0][m * BITS / 4], ua[m], ub[m], mg, mq, a);
+                Unpack<BITS>::template run<2, OFF>(&vw[t][1][m * BITS / 4], ua[m], ub[m], mg, mq, a + 1);
             } else if constexpr (BITS == 6) {
                 const int o0 = woff + (t * 16) * RW, o1 = woff + (t * 16 + 8) * RW;
-                Unpack<6>::template run_words<2>(pr[m][o0], pr2[m][o0], ua[m], ub[m], mg, mq, a);
-                Unpack<6>::template run_words<2>(pr[m][o1], pr2[m][o1], ua[m], ub[m], mg, mq, a + 1);
+                Unpack<6>::template run_words<2, OFF>(pr[m][o0], pr2[m][o0], ua[m], ub[m], mg, mq, a);
+                Unpack<6>::template run_words<2, OFF>(pr[m][o1], pr2[m][o1], ua[m], ub[m], mg, mq, a + 1);
             } else {
-                Unpack<BITS>::template run<2>(pr[m] + woff + (t * 16) * RW, ua[m], ub[m], mg, mq, a);
-                Unpack<BITS>::template run<2>(pr[m] + woff + (t * 16 + 8) * RW, ua[m], ub[m], mg, mq, a + 1);
+                Unpack<BITS>::template run<2, OFF>(pr[m] + woff + (t * 16) * RW, ua[m], ub[m], mg, mq, a);
+                Unpack<BITS>::template run<2, OFF>(pr[m] + woff + (t * 16 + 8) * RW, ua[m], ub[m], mg, mq, a + 1);
             }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
@@ -705,7 +718,7 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
 #pragma unroll
                                 for (int h = 0; h < 2; ++h) {
                                     sg[t][h] = Sv[t][h].get(gv);
-                                    bg[t][h] = Bv[t][h].get(gv);
+                                    bg[t][h] = bias_term<BITS>(sg[t][h], Bv[t][h].get(gv));
                                 }
                             group_body<BITS, G, RB, MT>(pr, pr2, ua, ub, mg, mq, gl * GW, bq + gl * RUNS * LR * 4, sg,
                                                         bg, sxq + gl * LR, p);
@@ -720,7 +733,7 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
 #pragma unroll
                             for (int h = 0; h < 2; ++h) {
                                 sg[t][h] = bf16f(sp[(2 * t + h) * rstep + gl]);
-                                bg[t][h] = bf16f(bp[(2 * t + h) * rstep + gl]);
+                                bg[t][h] = bias_term<BITS>(sg[t][h], bf16f(bp[(2 * t + h) * rstep + gl]));
                             }
                         group_body<BITS, G, RB, MT>(pr, pr2, ua, ub, mg, mq, gl * GW, bq + gl * RUNS * LR * 4, sg, bg,
                                                     sxq + gl * LR, p);

@@ -120,13 +120,21 @@ constexpr uint32_t MAGIC = 0x43004300u;            // 128.0 | 128.0
 constexpr uint32_t NEG128 = 0xC300C300u;           // -128
 constexpr uint32_t Q3 = 0x3E003E00u, NEG16 = 0xC180C180u;   // p=3: 1/8, -16
 constexpr uint32_t Q4 = 0x3D803D80u, NEG8 = 0xC100C100u;    // p=4: 1/16, -8
+constexpr uint32_t P112 = 0x42E042E0u, P120 = 0x42F042F0u;  // 128 - 16, 128 - 8
 
-// Code pair at mantissa position p = 0: (128 + c) - 128.
-TF_HD uint32_t at0(uint32_t u, uint32_t m, uint32_t mg) { return hadd2(mask_or(u, m, mg), NEG128); }
-// Code pair at position p > 0: (128 + c*2^p) * 2^-p - 128*2^-p, with q = 2^-p
-// passed in a register (QP<BITS>) like `mg`.
-TF_HD uint32_t atp(uint32_t u, uint32_t m, uint32_t mg, uint32_t q, uint32_t neg) {
-    return hfma2(mask_or(u, m, mg), q, neg);
+// Two forms of a run's pairs: exact codes c (OFF = false), or offset codes
+// 128 + c (OFF = true; every pair of the run carries the same offset, and a
+// product built on them takes 128 * sum(x) back through its bias term).
+// Code pair at mantissa position p = 0: (128 + c) - 128, or 128 + c itself.
+template <bool OFF = false>
+TF_HD uint32_t at0(uint32_t u, uint32_t m, uint32_t mg) {
+    return OFF ? mask_or(u, m, mg) : hadd2(mask_or(u, m, mg), NEG128);
+}
+// Code pair at position p > 0: (128 + c*2^p) * 2^-p + a with q = 2^-p passed
+// in a register (QP<BITS>) like `mg`, and a = -128*2^-p (exact codes) or
+// 128 - 128*2^-p (offset codes).
+TF_HD uint32_t atp(uint32_t u, uint32_t m, uint32_t mg, uint32_t q, uint32_t a) {
+    return hfma2(mask_or(u, m, mg), q, a);
 }
 
 // The 2^-p pair that Unpack<BITS> uses for its p > 0 pairs (0 when it has none).
@@ -146,28 +154,28 @@ struct Unpack;
 
 template <>
 struct Unpack<2> {  // 16 bits; sh in {0, 16}
-    template <int ST = 1>
+    template <int ST = 1, bool OFF = false>
     static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t, uint32_t mg, uint32_t mq, uint32_t *p) {
         uint32_t v = w[0] >> sh;
         uint32_t u = halves(v, v << 8);              // c0..c3 @0,2,4,6 | c4..c7 @16,18,20,22
         uint32_t u1 = u >> 2;                        // c1, c3 @0,4 | c5, c7 @16,20
-        p[0 * ST] = at0(u, 0x00030003u, mg);
-        p[1 * ST] = at0(u1, 0x00030003u, mg);
-        p[2 * ST] = atp(u, 0x00300030u, mg, mq, NEG8);
-        p[3 * ST] = atp(u1, 0x00300030u, mg, mq, NEG8);
+        p[0 * ST] = at0<OFF>(u, 0x00030003u, mg);
+        p[1 * ST] = at0<OFF>(u1, 0x00030003u, mg);
+        p[2 * ST] = atp(u, 0x00300030u, mg, mq, OFF ? P120 : NEG8);
+        p[3 * ST] = atp(u1, 0x00300030u, mg, mq, OFF ? P120 : NEG8);
     }
 };
 
 template <>
 struct Unpack<4> {  // 32 bits; sh == 0
     // A 4-bit code fits the 7-bit mantissa only at p <= 3: every pair is moved to p = 0.
-    template <int ST = 1>
+    template <int ST = 1, bool OFF = false>
     static TF_HD void run(const uint32_t *w, uint32_t, uint32_t, uint32_t mg, uint32_t mq, uint32_t *p) {
         uint32_t v = w[0];                           // c0..c3 @0,4,8,12 | c4..c7 @16,20,24,28
-        p[0 * ST] = at0(v, 0x000F000Fu, mg);
-        p[1 * ST] = at0(v >> 4, 0x000F000Fu, mg);
-        p[2 * ST] = at0(v >> 8, 0x000F000Fu, mg);
-        p[3 * ST] = at0(v >> 12, 0x000F000Fu, mg);
+        p[0 * ST] = at0<OFF>(v, 0x000F000Fu, mg);
+        p[1 * ST] = at0<OFF>(v >> 4, 0x000F000Fu, mg);
+        p[2 * ST] = at0<OFF>(v >> 8, 0x000F000Fu, mg);
+        p[3 * ST] = at0<OFF>(v >> 12, 0x000F000Fu, mg);
     }
 };
 
@@ -180,8 +188,9 @@ struct Unpack<8> {  // 64 bits; sh == 0
         uint32_t add = ~sgn & NEG128;                       // -128 if c < 128, else 0
         return hadd2(mant, add);
     }
-    template <int ST = 1>
+    template <int ST = 1, bool OFF = false>
     static TF_HD void run(const uint32_t *w, uint32_t, uint32_t, uint32_t mg, uint32_t mq, uint32_t *p) {
+        static_assert(!OFF, "8-bit codes have no offset form (128 + c needs 9 bits)");
         uint32_t lo = w[0], hi = w[1];
         p[0 * ST] = one(prmt(lo, hi, 0x0400u), mg);   // byte i of lo -> 0, byte i of hi -> 2
         p[1 * ST] = one(prmt(lo, hi, 0x0501u), mg);
@@ -192,52 +201,52 @@ struct Unpack<8> {  // 64 bits; sh == 0
 
 template <>
 struct Unpack<3> {  // 24 bits; sh in {0, 8, 16, 24}
-    template <int ST = 1>
+    template <int ST = 1, bool OFF = false>
     static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t, uint32_t mg, uint32_t mq, uint32_t *p) {
         uint32_t v = funnel(w[0], w[1], sh);
         uint32_t u = halves(v, v << 4);   // c0..c3 @0,3,6,9 | c4..c7 @16,19,22,25
         uint32_t u2 = u >> 6;             // c2 @0, c3 @3 | c6 @16, c7 @19
-        p[0 * ST] = at0(u, 0x00070007u, mg);
-        p[1 * ST] = atp(u, 0x00380038u, mg, mq, NEG16);
-        p[2 * ST] = at0(u2, 0x00070007u, mg);
-        p[3 * ST] = atp(u2, 0x00380038u, mg, mq, NEG16);
+        p[0 * ST] = at0<OFF>(u, 0x00070007u, mg);
+        p[1 * ST] = atp(u, 0x00380038u, mg, mq, OFF ? P112 : NEG16);
+        p[2 * ST] = at0<OFF>(u2, 0x00070007u, mg);
+        p[3 * ST] = atp(u2, 0x00380038u, mg, mq, OFF ? P112 : NEG16);
     }
 };
 
 template <>
 struct Unpack<5> {  // 40 bits; sh in {0, 8, 16, 24}
-    template <int ST = 1>
+    template <int ST = 1, bool OFF = false>
     static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t, uint32_t mg, uint32_t mq, uint32_t *p) {
         uint32_t lo = funnel(w[0], w[1], sh);               // run bits 0..31
         uint32_t hi = w[1] >> sh;                           // run bits 32..39 at 0..7
         uint32_t u = halves(lo, funnel(lo, hi, 4));         // c0,c1,c2 @0,5,10 | c4,c5,c6 @16,21,26
         uint32_t u3 = halves(lo >> 15, funnel(lo, hi, 19)); // c3 @0 | c7 @16
-        p[0 * ST] = at0(u, 0x001F001Fu, mg);
-        p[1 * ST] = at0(u >> 5, 0x001F001Fu, mg);
-        p[2 * ST] = at0(u >> 10, 0x001F001Fu, mg);
-        p[3 * ST] = at0(u3, 0x001F001Fu, mg);
+        p[0 * ST] = at0<OFF>(u, 0x001F001Fu, mg);
+        p[1 * ST] = at0<OFF>(u >> 5, 0x001F001Fu, mg);
+        p[2 * ST] = at0<OFF>(u >> 10, 0x001F001Fu, mg);
+        p[3 * ST] = at0<OFF>(u3, 0x001F001Fu, mg);
     }
 };
 
 template <>
 struct Unpack<6> {  // 48 bits; sh in {0, 16}
     // Run bytes {0,1,3,4} and {1,2,4,5}; raw byte = run byte + sh/8 (sh = 0 or 16).
-    template <int ST = 1>
+    template <int ST = 1, bool OFF = false>
     static TF_HD void run(const uint32_t *w, uint32_t s0, uint32_t s2, uint32_t mg, uint32_t mq, uint32_t *p) {
-        run_words<ST>(w[0], w[1], s0, s2, mg, mq, p);
+        run_words<ST, OFF>(w[0], w[1], s0, s2, mg, mq, p);
     }
     // The run's two words passed in (a, b) = (w[0], w[1]); the same pairs come
     // from (a, b) = (w[1], w[0]) with both selectors XOR 0x4444 (each selector
     // byte index then names the other operand's byte).
-    template <int ST = 1>
+    template <int ST = 1, bool OFF = false>
     static TF_HD void run_words(uint32_t a, uint32_t b, uint32_t s0, uint32_t s2, uint32_t mg, uint32_t mq,
                                 uint32_t *p) {
         uint32_t P0 = prmt(a, b, s0);   // c0 @0, c1 @6 | c4 @16, c5 @22
         uint32_t P2 = prmt(a, b, s2);   // c2 @4, c3 @10 | c6 @20, c7 @26
-        p[0 * ST] = at0(P0, 0x003F003Fu, mg);
-        p[1 * ST] = at0(P0 >> 6, 0x003F003Fu, mg);
-        p[2 * ST] = at0(P2 >> 4, 0x003F003Fu, mg);
-        p[3 * ST] = at0(P2 >> 10, 0x003F003Fu, mg);
+        p[0 * ST] = at0<OFF>(P0, 0x003F003Fu, mg);
+        p[1 * ST] = at0<OFF>(P0 >> 6, 0x003F003Fu, mg);
+        p[2 * ST] = at0<OFF>(P2 >> 4, 0x003F003Fu, mg);
+        p[3 * ST] = at0<OFF>(P2 >> 10, 0x003F003Fu, mg);
     }
 };
 

@@ -35,6 +35,18 @@ static int check(std::mt19937 &rng, int sh) {
         uint32_t p2[8];
         tfq::Unpack<BITS>::template run<2>(w, ua, ub, tfq::MAGIC, tfq::QP<BITS>::value, p2);
         for (int i = 0; i < 4; ++i) if (p2[2 * i] != p[i]) { printf("stride mismatch\n"); ++bad; }
+        if constexpr (BITS != 8) {   // offset form: every pair holds 128 + c
+            uint32_t p4[4];
+            tfq::Unpack<BITS>::template run<1, true>(w, ua, ub, tfq::MAGIC, tfq::QP<BITS>::value, p4);
+            for (int i = 0; i < 4; ++i) {
+                int lo = bf16_int((uint16_t)(p4[i] & 0xFFFF)), hi = bf16_int((uint16_t)(p4[i] >> 16));
+                int want_lo = 128 + (int)bit_code(w, BITS, sh, i), want_hi = 128 + (int)bit_code(w, BITS, sh, i + 4);
+                if (lo != want_lo || hi != want_hi) {
+                    if (bad < 5) printf("OFF BITS=%d sh=%d pair %d: got (%d,%d) want (%d,%d)\n", BITS, sh, i, lo, hi, want_lo, want_hi);
+                    ++bad;
+                }
+            }
+        }
         if (BITS == 6) {   // the two words in swapped order with flipped selectors
             uint32_t p3[4];
             tfq::Unpack<6>::template run_words<1>(w[1], w[0], ua ^ 0x4444u, ub ^ 0x4444u, tfq::MAGIC, 0u, p3);
