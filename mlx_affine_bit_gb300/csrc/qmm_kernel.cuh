@@ -696,9 +696,11 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                 const uint16_t *bp = reinterpret_cast<const uint16_t *>(sbase + (ROWS + g) * P.sbpitch) + gseg;
                 const int rstep = 8 * P.sbpitch / 2;                     // 8 rows, in bf16 elements
                 if (ng == NGS) {
-                    // Scales and biases in vector loads of NV groups (fewer live
-                    // registers with two consumer groups).
-                    constexpr int NV = (CG == 2 && NGS == 8) ? 4 : NGS;
+                    // Scales and biases in vector loads of NV groups: two for the
+                    // two-m-tile kernels with two consumer groups (wider loads spill
+                    // under their 96-register cap; the 6-bit LM head measured 5 %
+                    // faster), four for 16 rows with two groups.
+                    constexpr int NV = CG == 2 ? (MT == 2 ? (NGS >= 4 ? 2 : NGS) : (NGS == 8 ? 4 : NGS)) : NGS;
 #pragma unroll
                     for (int g0 = 0; g0 < NGS; g0 += NV) {
                         SegVals<NV> Sv[MT][2], Bv[MT][2];
