@@ -433,8 +433,11 @@ struct SegVals<2> {
     }
 };
 
-// Codes below 8 bits enter the MMA as 128 + c; 8-bit codes as c.
-__host__ __device__ constexpr bool offset_codes(int bits) { return bits != 8; }
+// 4-, 5- and 6-bit codes enter the MMA as 128 + c (every pair of their runs
+// sits at mantissa position 0, so this saves one instruction per pair); 2-,
+// 3- and 8-bit codes enter exactly (the pages enter 2-bit codes exactly, and at
+// 8 bits 128 + c does not fit the bf16 significand).
+__host__ __device__ constexpr bool offset_codes(int bits) { return bits >= 4 && bits <= 6; }
 
 // The group's bias coefficient: b, or b - 128 s (one rounding) for offset codes.
 template <int BITS>
@@ -443,8 +446,8 @@ __device__ __forceinline__ float bias_term(float s, float b) {
 }
 
 // One group of this lane's 2*MT columns (rows t*16+g and t*16+g+8 of each
-// m-tile t): T = tensor-core dot products of the group's codes with x (exact
-// codes c at 8 bits, offset codes 128 + c below), then p = fma(s,T,p);
+// m-tile t): T = tensor-core dot products of the group's codes with x (offset
+// codes 128 + c at 4-6 bits, exact codes c otherwise), then p = fma(s,T,p);
 // p = fma(b',sum_group(x),p); bg holds b' = b, or b - 128 s for offset codes.  pr[m]: run m of the lane's
 // quarter in row g of m-tile 0 (other rows at compile-time offsets); for 6-bit
 // codes pr[m] / pr2[m] are the run's first / second word in this lane's load
@@ -461,8 +464,8 @@ __device__ __forceinline__ void group_body(const uint32_t *const (&pr)[G / 32], 
     constexpr int LR = layout_rows(RB);
     constexpr int RUNS = G / 32;
     constexpr int RW = Pitch<BITS, G>::SEGP / 4;     // words between rows of a segment block
-    // Below 8 bits the MMA takes the offset codes 128 + c (one instruction per
-    // pair less): T' = T + 128 sum_group(x), and bg holds b - 128 s.
+    // With offset codes the MMA takes 128 + c (one instruction per pair less):
+    // T' = T + 128 sum_group(x), and bg holds b - 128 s.
     constexpr bool OFF = offset_codes(BITS);
     // 4- and 8-bit runs of a lane lie in consecutive aligned words: with two or
     // four runs a group, one vector load per row feeds them all.

@@ -120,21 +120,19 @@ constexpr uint32_t MAGIC = 0x43004300u;            // 128.0 | 128.0
 constexpr uint32_t NEG128 = 0xC300C300u;           // -128
 constexpr uint32_t Q3 = 0x3E003E00u, NEG16 = 0xC180C180u;   // p=3: 1/8, -16
 constexpr uint32_t Q4 = 0x3D803D80u, NEG8 = 0xC100C100u;    // p=4: 1/16, -8
-constexpr uint32_t P112 = 0x42E042E0u, P120 = 0x42F042F0u;  // 128 - 16, 128 - 8
 
-// Two forms of a run's pairs: exact codes c (OFF = false), or offset codes
-// 128 + c (OFF = true; every pair of the run carries the same offset, and a
-// product built on them takes 128 * sum(x) back through its bias term).
+// Two forms of a run's pairs: exact codes c (OFF = false), or, for the widths
+// whose pairs all sit at p = 0 (4, 5, 6 bits), offset codes 128 + c (OFF =
+// true; a product built on them takes 128 * sum(x) back through its bias).
 // Code pair at mantissa position p = 0: (128 + c) - 128, or 128 + c itself.
 template <bool OFF = false>
 TF_HD uint32_t at0(uint32_t u, uint32_t m, uint32_t mg) {
     return OFF ? mask_or(u, m, mg) : hadd2(mask_or(u, m, mg), NEG128);
 }
-// Code pair at position p > 0: (128 + c*2^p) * 2^-p + a with q = 2^-p passed
-// in a register (QP<BITS>) like `mg`, and a = -128*2^-p (exact codes) or
-// 128 - 128*2^-p (offset codes).
-TF_HD uint32_t atp(uint32_t u, uint32_t m, uint32_t mg, uint32_t q, uint32_t a) {
-    return hfma2(mask_or(u, m, mg), q, a);
+// Code pair at position p > 0: (128 + c*2^p) * 2^-p - 128*2^-p, with q = 2^-p
+// passed in a register (QP<BITS>) like `mg`.
+TF_HD uint32_t atp(uint32_t u, uint32_t m, uint32_t mg, uint32_t q, uint32_t neg) {
+    return hfma2(mask_or(u, m, mg), q, neg);
 }
 
 // The 2^-p pair that Unpack<BITS> uses for its p > 0 pairs (0 when it has none).
@@ -156,13 +154,14 @@ template <>
 struct Unpack<2> {  // 16 bits; sh in {0, 16}
     template <int ST = 1, bool OFF = false>
     static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t, uint32_t mg, uint32_t mq, uint32_t *p) {
+        static_assert(!OFF, "2-bit codes enter exactly");
         uint32_t v = w[0] >> sh;
         uint32_t u = halves(v, v << 8);              // c0..c3 @0,2,4,6 | c4..c7 @16,18,20,22
         uint32_t u1 = u >> 2;                        // c1, c3 @0,4 | c5, c7 @16,20
-        p[0 * ST] = at0<OFF>(u, 0x00030003u, mg);
-        p[1 * ST] = at0<OFF>(u1, 0x00030003u, mg);
-        p[2 * ST] = atp(u, 0x00300030u, mg, mq, OFF ? P120 : NEG8);
-        p[3 * ST] = atp(u1, 0x00300030u, mg, mq, OFF ? P120 : NEG8);
+        p[0 * ST] = at0(u, 0x00030003u, mg);
+        p[1 * ST] = at0(u1, 0x00030003u, mg);
+        p[2 * ST] = atp(u, 0x00300030u, mg, mq, NEG8);
+        p[3 * ST] = atp(u1, 0x00300030u, mg, mq, NEG8);
     }
 };
 
@@ -203,13 +202,14 @@ template <>
 struct Unpack<3> {  // 24 bits; sh in {0, 8, 16, 24}
     template <int ST = 1, bool OFF = false>
     static TF_HD void run(const uint32_t *w, uint32_t sh, uint32_t, uint32_t mg, uint32_t mq, uint32_t *p) {
+        static_assert(!OFF, "3-bit codes enter exactly");
         uint32_t v = funnel(w[0], w[1], sh);
         uint32_t u = halves(v, v << 4);   // c0..c3 @0,3,6,9 | c4..c7 @16,19,22,25
         uint32_t u2 = u >> 6;             // c2 @0, c3 @3 | c6 @16, c7 @19
-        p[0 * ST] = at0<OFF>(u, 0x00070007u, mg);
-        p[1 * ST] = atp(u, 0x00380038u, mg, mq, OFF ? P112 : NEG16);
-        p[2 * ST] = at0<OFF>(u2, 0x00070007u, mg);
-        p[3 * ST] = atp(u2, 0x00380038u, mg, mq, OFF ? P112 : NEG16);
+        p[0 * ST] = at0(u, 0x00070007u, mg);
+        p[1 * ST] = atp(u, 0x00380038u, mg, mq, NEG16);
+        p[2 * ST] = at0(u2, 0x00070007u, mg);
+        p[3 * ST] = atp(u2, 0x00380038u, mg, mq, NEG16);
     }
 };
 

@@ -35,7 +35,7 @@ static int check(std::mt19937 &rng, int sh) {
         uint32_t p2[8];
         tfq::Unpack<BITS>::template run<2>(w, ua, ub, tfq::MAGIC, tfq::QP<BITS>::value, p2);
         for (int i = 0; i < 4; ++i) if (p2[2 * i] != p[i]) { printf("stride mismatch\n"); ++bad; }
-        if constexpr (BITS != 8) {   // offset form: every pair holds 128 + c
+        if constexpr (BITS >= 4 && BITS <= 6) {   // offset form: every pair holds 128 + c
             uint32_t p4[4];
             tfq::Unpack<BITS>::template run<1, true>(w, ua, ub, tfq::MAGIC, tfq::QP<BITS>::value, p4);
             for (int i = 0; i < 4; ++i) {
