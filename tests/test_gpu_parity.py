@@ -248,6 +248,20 @@ def test_lmhead_sampled(bits, group, seed):
     oracle_check(m, x, y16.cpu().numpy(), cols)
 
 
+@pytest.mark.parametrize("bits,group", [(4, 32), (5, 32), (6, 32), (4, 128), (6, 64)])
+def test_offset_codes_keep_margin(bits, group):
+    # 4-6-bit codes enter the tensor cores as 128 + c (the bias term takes the
+    # 128 * sum(x) back), which raises the rounding of the group products.  At
+    # a short K, where the tolerance is tightest, the worst error stays well
+    # inside it (an fp32 model of the arithmetic gives about 0.02 of it).
+    N, K = 512, 256
+    m = synth.make_matrix(N, K, bits, group, 160 + bits, 0.001, 0.03)
+    x = synth.make_x(4, K, 161)
+    y = run_qmm(DevMatrix(m), dev(x)).cpu().numpy()
+    worst = oracle_check(m, x, y)
+    assert worst < 0.25, worst
+
+
 @pytest.mark.parametrize("mode", [1, 2])
 def test_launch_modes_bit_identical(mode):
     # A back-to-back sequence of products (including a split-K shape) gives the
