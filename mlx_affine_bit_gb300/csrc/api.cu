@@ -121,16 +121,19 @@ Plan layout(int N, int K, int bits, int group, int rows, int nsm, int ctas, bool
 }
 
 // Two m-tiles (32 columns) per item with one CTA per SM when there are at
-// least two such items per SM (shared activation loads, half the per-stage
-// overhead), computed by two consumer groups when the whole K fits one slice
-// and three stages fit (two computed, one in flight); else one m-tile per item
+// least two such items per SM and two stages fit (shared activation loads,
+// half the per-stage overhead), computed by two consumer groups when the whole
+// K fits one slice and three stages fit (two computed, one in flight); else one m-tile per item
 // with two CTAs per SM when three stages of each still fit; else one CTA per
 // SM with a deeper ring, with two consumer groups for 9-16 rows over many
 // column tiles.  The choice never changes a result's bits.
 Plan make_plan(int N, int K, int bits, int group, int rows, int nsm, bool sb3d) {
     if (row_bucket(rows) <= 8) {
         const Plan wide = layout(N, K, bits, group, rows, nsm, 1, sb3d, 2);
-        if (wide.stages >= 3 && (long long)wide.nmt * wide.nsl >= 2LL * nsm) {
+        // Two stages suffice for one consumer group: 6- and 8-bit codes at 4-8
+        // rows leave room for no more, and the plan still beat the one-m-tile
+        // plans there (12288 x 2048, 8 rows: 8.3 against 9.8 us).
+        if (wide.stages >= 2 && (long long)wide.nmt * wide.nsl >= 2LL * nsm) {
             // Two consumer groups (two stages computed at once) when three stages fit.
             if (wide.nsl == 1) {
                 const Plan pp = layout(N, K, bits, group, rows, nsm, 1, sb3d, 2, 2);
