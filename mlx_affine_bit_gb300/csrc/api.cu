@@ -133,7 +133,11 @@ Plan make_plan(int N, int K, int bits, int group, int rows, int nsm, bool sb3d) 
         // Two stages suffice for one consumer group: 6- and 8-bit codes at 4-8
         // rows leave room for no more, and the plan still beat the one-m-tile
         // plans there (12288 x 2048, 8 rows: 8.3 against 9.8 us).
-        if (wide.stages >= 2 && (long long)wide.nmt * wide.nsl >= 2LL * nsm) {
+        // With 4-8 rows a stage's compute is heavy enough that the wider item pays
+        // even with idle SMs (2048 x 12288, 4 rows: 128 items on 152 SMs, 10.6
+        // against 12.5 us); one or two rows want two items per SM.
+        const long long min_items = row_bucket(rows) >= 4 ? nsm / 2 : 2LL * nsm;
+        if (wide.stages >= 2 && (long long)wide.nmt * wide.nsl >= min_items) {
             // Two consumer groups (two stages computed at once) when three stages fit.
             if (wide.nsl == 1) {
                 const Plan pp = layout(N, K, bits, group, rows, nsm, 1, sb3d, 2, 2);
