@@ -907,7 +907,7 @@ cudaError_t launch_width(int group, int rb, int mt, int cg, const QmmParams &P, 
     }
 #define TFQ_ROWS(G_) TFQ_CASE(G_, 1, 1, 1) TFQ_CASE(G_, 2, 1, 1) TFQ_CASE(G_, 4, 1, 1) TFQ_CASE(G_, 8, 1, 1) \
     TFQ_CASE(G_, 16, 1, 1) TFQ_CASE(G_, 1, 2, 1) TFQ_CASE(G_, 2, 2, 1) TFQ_CASE(G_, 4, 2, 1)                \
-    TFQ_CASE(G_, 8, 2, 1) TFQ_CASE(G_, 1, 2, 2) TFQ_CASE(G_, 2, 2, 2) TFQ_CASE(G_, 4, 2, 2)                \
+    TFQ_CASE(G_, 8, 2, 1) TFQ_CASE(G_, 16, 2, 1) TFQ_CASE(G_, 1, 2, 2) TFQ_CASE(G_, 2, 2, 2) TFQ_CASE(G_, 4, 2, 2) \
     TFQ_CASE(G_, 8, 2, 2) TFQ_CASE(G_, 16, 1, 2)
     TFQ_ROWS(32) TFQ_ROWS(64) TFQ_ROWS(128)
 #undef TFQ_ROWS

@@ -87,12 +87,13 @@ def test_unpack_host_build(tmp_path):
 def test_every_kernel_instantiated(tf):
     # 6 widths x 3 groups x row buckets {1, 2, 4, 8, 16} x one m-tile per item, and
     # buckets up to 8 rows with two m-tiles and one or two consumer groups, and
-    # 16 rows with one m-tile and two groups: every host launch stub is in the library.
+    # 16 rows with one m-tile and two groups or two m-tiles and one group: every host
+    # launch stub is in the library.
     out = subprocess.check_output(["nm", "-C", "--defined-only", tf.SO]).decode()
     for bits in (2, 3, 4, 5, 6, 8):
         for group in (32, 64, 128):
             for rb in (1, 2, 4, 8, 16):
-                for mt, cg in (((1, 1), (2, 1), (2, 2)) if rb <= 8 else ((1, 1), (1, 2))):
+                for mt, cg in (((1, 1), (2, 1), (2, 2)) if rb <= 8 else ((1, 1), (1, 2), (2, 1))):
                     name = "tfq::qmm_kernel<%d, %d, %d, %d, %d>(" % (bits, group, rb, mt, cg)
                     assert name in out, name
 

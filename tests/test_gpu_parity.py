@@ -248,6 +248,23 @@ def test_lmhead_sampled(bits, group, seed):
     oracle_check(m, x, y16.cpu().numpy(), cols)
 
 
+@pytest.mark.parametrize("bits,group", [(2, 64), (3, 128), (4, 32), (5, 64), (6, 32), (8, 128)])
+def test_sixteen_rows_two_tiles(bits, group):
+    # 2048 columns over K = 8192 at 16 rows take two m-tiles per item with one
+    # consumer group (split K); every row equals the row computed alone (a
+    # one-row plan) bit for bit and meets the tolerance.
+    N, K = 2048, 8192
+    m = synth.make_matrix(N, K, bits, group, 170 + bits, 0.001, 0.03)
+    dm = DevMatrix(m)
+    x = synth.make_x(16, K, 171)
+    xd = dev(x)
+    y = run_qmm(dm, xd)
+    for r in (0, 5, 15):
+        alone = run_qmm(dm, xd[r:r + 1].contiguous())
+        assert torch.equal(y[r].view(torch.int32), alone[0].view(torch.int32)), r
+    oracle_check(m, x, y.cpu().numpy(), sample_cols(N, 24, bits))
+
+
 @pytest.mark.parametrize("bits,group", [(4, 32), (5, 32), (6, 32), (4, 128), (6, 64)])
 def test_offset_codes_keep_margin(bits, group):
     # 4-6-bit codes enter the tensor cores as 128 + c (the bias term takes the
