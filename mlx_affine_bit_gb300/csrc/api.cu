@@ -151,6 +151,10 @@ Plan make_plan(int N, int K, int bits, int group, int rows, int nsm, bool sb3d) 
     }
     const Plan two = layout(N, K, bits, group, rows, nsm, 2, sb3d, 1);
     if (two.stages >= 3) return two;
+    // Two stages suffice when they hold a whole item of two chunks (the second
+    // loads while the first computes): 8-bit 4096 x 4096 products measured
+    // 3.5-7.5 % faster than with one CTA per SM.
+    if (two.stages == 2 && two.nsl == 1 && two.nchunks == 2) return two;
     const Plan one = layout(N, K, bits, group, rows, nsm, 1, sb3d, 1);
     if (row_bucket(rows) == 16 && one.nsl == 1 && (long long)one.nmt >= 2LL * nsm) {
         // Nine to sixteen rows over many column tiles: two consumer groups
