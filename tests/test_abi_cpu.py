@@ -84,6 +84,23 @@ def test_unpack_host_build(tmp_path):
     assert "PASS" in out
 
 
+def test_planner_host(tmp_path):
+    # Every launch plan over a grid of shapes, widths, groups, row counts and SM
+    # counts fits shared memory, has a ring of 2-8 stages, uses an instantiated
+    # kernel, gives two consumer groups only one K slice and three stages, and
+    # covers K with whole teams of CTAs.  Host code only (stubbed launchers).
+    import shutil
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not available")
+    exe = str(tmp_path / "planner_test")
+    subprocess.check_call([nvcc, "-std=c++17", "-O1", "-I" + os.path.join(ROOT, "mlx_affine_bit_gb300", "csrc"),
+                           "-gencode", "arch=compute_103a,code=sm_103a",
+                           os.path.join(ROOT, "tests", "planner_host_test.cu"), "-o", exe])
+    out = subprocess.check_output([exe]).decode()
+    assert "PASS" in out, out
+
+
 def test_every_kernel_instantiated(tf):
     # 6 widths x 3 groups x row buckets {1, 2, 4, 8, 16} x one m-tile per item, and
     # buckets up to 8 rows with two m-tiles and one or two consumer groups, and
