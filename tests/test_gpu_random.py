@@ -2,6 +2,8 @@
 groups, odd column counts, K that is not a multiple of 256 (the producer's
 plain-copy path), 1-20 rows, strides and output options; one row of every
 case is also checked against the same row computed alone."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -23,7 +25,9 @@ def built():
     tf.tf_device_status()
 
 
-def _cases(n=40, seed=2024):
+def _cases(n=None, seed=2024):
+    # TFQ_RANDOM_CASES widens the sample (40 by default, so the suite stays quick).
+    n = int(os.environ.get("TFQ_RANDOM_CASES", "40")) if n is None else n
     rng = np.random.default_rng(seed)
     out = []
     for i in range(n):
