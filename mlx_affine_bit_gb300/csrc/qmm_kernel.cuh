@@ -10,7 +10,8 @@
 // codes (a contiguous 8-64 KB of HBM when the slice is the whole row) and one
 // each for scales and biases, completed on mbarriers.  Warp w of a group takes
 // segment w (256 k) of a stage: it unpacks 8-code runs straight into bf16 A
-// fragments (codes exact), multiplies them by the activations with mma.sync
+// fragments (each code exact: c, or 128 + c at 4-6 bits with the offset taken
+// back through the bias term), multiplies them by the activations with mma.sync
 // m16n8k16 (rows are the N dimension: 1..8 rows cost one MMA, 9..16 two),
 // applies each group's scale and bias to the fp32 group sum in registers, and
 // the segment partials are folded in k order through shared memory.
