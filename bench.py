@@ -152,6 +152,22 @@ def cpu_sample(cases, cols_per_case: int, nthreads: int):
     return total_bytes / t_total / 1e9, t_total, total_bytes
 
 
+def max_over_ranks(v: float, dev) -> float:
+    """The slowest rank's time (each rank times its own replica); v unchanged on one rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job GB/s: every rank's bytes over the slowest rank's time (weak scaling)."""
+    return bytes_per_rank * world / (ms * 1e-3) / 1e9
+
+
 def run_reference(args, cases):
     import oracle
     oracle.build()
@@ -417,10 +433,7 @@ def run_gpu(args, cases):
         dist.barrier()
     clocks = clk.stop()
     ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, dev)
     tf.tf_device_status()
     per_launch = [[c0.elapsed_time(c1) / nl] for (c0, c1, nl) in per_launch]
     args.steps = steps
@@ -464,14 +477,10 @@ def run_gpu(args, cases):
     e2e_ms = e0.elapsed_time(e1)
     for it, (xo, yo) in zip(items, saved):
         it["x"], it["y"] = xo, yo
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_ms, dev)
 
     peak, peak_kind = _peaks()
-    total_bytes = per_step * args.steps * world
-    value = total_bytes / (ms * 1e-3) / 1e9
+    value = job_throughput(per_step * args.steps, world, ms)
     kern_ms = sum(statistics.mean(p) for p in per_launch)   # a step's summed launch times
     achieved = per_step / (kern_ms * 1e-3) / 1e9
     case_rows = []
@@ -520,7 +529,7 @@ def run_gpu(args, cases):
                          "traffic_unit": "bytes per step (ncu, all qmm launches of one step)",
                          "kernel": "tfq::qmm_kernel (all products of the step, bytes / summed launch time)"},
             "cpu_baseline": cpu,
-            "e2e": {"value": per_step * e2e_steps / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+            "e2e": {"value": job_throughput(per_step * e2e_steps, world, e2e_ms), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": sum(it.get("launches", len(it["reps"][0]) if it.get("stack") else 1)
                                 for it in items) * args.steps,
