@@ -120,14 +120,17 @@ Plan layout(int N, int K, int bits, int group, int rows, int nsm, int ctas, bool
     return p;
 }
 
-// Two m-tiles (32 columns) per item with one CTA per SM when there are at
-// least two such items per SM and two stages fit (shared activation loads,
-// half the per-stage overhead), computed by two consumer groups when the whole
-// K fits one slice and three stages fit (two computed, one in flight); else one m-tile per item
-// with two CTAs per SM when three stages of each still fit; else one CTA per
-// SM with a deeper ring, with two consumer groups for 9-16 rows over many
-// column tiles or else two m-tiles per item.  The choice never changes a
-// result's bits.
+// The launch plan, in order of preference (every choice gives the same bits):
+//  1. up to 8 rows: two m-tiles (32 columns) per item, one CTA per SM, when two
+//     stages fit and the items fill the SMs (two per SM at 1-2 rows, one per two
+//     SMs at 3-8) -- computed by two consumer groups when the whole K is one
+//     slice, three stages fit and the items are plentiful (2+ per SM at one
+//     row, 4+ per SM from two rows on);
+//  2. one m-tile per item, two CTAs per SM, when three stages fit, or two that
+//     hold a whole item of two chunks;
+//  3. one m-tile per item, one CTA per SM with a deeper ring: two consumer
+//     groups for 9-16 rows over many column tiles, else for 9-16 rows two
+//     m-tiles per item when those fill half the SMs.
 Plan make_plan(int N, int K, int bits, int group, int rows, int nsm, bool sb3d) {
     if (row_bucket(rows) <= 8) {
         const Plan wide = layout(N, K, bits, group, rows, nsm, 1, sb3d, 2);
