@@ -73,6 +73,10 @@ extern "C" {
  *            weights are read once per window), each row's bits those of the
  *            row alone -- the row / window gate of PR #788 extended past 16 rows.
  * Returns TF_OK or a negative status (checked on the host before any launch).
+ * Allocation: the first call on a device allocates the device status word, and
+ * a call whose plan splits K allocates (or grows, with cudaFree + cudaMalloc)
+ * the split-K workspace of its (device, stream).  A caller that must not let
+ * the library allocate uses tf_qmm_noalloc instead.
  */
 int tf_qmm(const uint16_t *x, int rows, int K,
            const uint32_t *W, const uint16_t *scales, const uint16_t *biases,
@@ -86,23 +90,33 @@ int tf_qmm(const uint16_t *x, int rows, int K,
  * processes that must not grow their footprint later.  The paper has no
  * counterpart; it is a deployment variant of tf_qmm.
  *
- * Same arguments, layouts and results as tf_qmm (plain launches, whatever the
- * launch mode).  Its split-K scratch and status word come from one fixed
- * 4 MiB device array built into the library instead of a cudaMalloc: every
- * GPU that loads the library holds that array until exit, and the call
- * allocates nothing.  A product whose split-K partials need more than the
- * array holds (rows * N * ceil(K/2048) * 4 bytes, about 4 MiB, when the
- * planner splits K) is refused with TF_EINVAL_SIZE before any launch.
- * The first call on a device looks up the array's device address (set-up);
- * make that first call before any stream capture.  All calls share the
- * array: each clears what it needs at zero on its own stream, and calls that
- * overlap on the GPU race.  A bounded wait that runs out is recorded in the
- * array, not in the word tf_device_status reads.
+ * Same arguments, layouts and results as tf_qmm, bit for bit, rows 1..65536
+ * (more than 16 rows run as 16-row windows, one launch after another), with
+ * plain launches whatever the launch mode.  Its split-K scratch and status
+ * word come from one fixed 4 MiB device array built into the library instead
+ * of a cudaMalloc: every GPU that loads the library holds that array until
+ * exit, and the call allocates nothing.  A product whose split-K partials need
+ * more than the array holds (window rows * N * ceil(K/2048) * 4 bytes, about
+ * 4 MiB, when the planner splits K) is refused with TF_EINVAL_SIZE before any
+ * launch.  The first call on a device looks up the array's device address and
+ * clears its status word (set-up); make that first call before any stream
+ * capture.  All calls share the array: each clears the counters it needs at
+ * zero on its own stream, and calls that overlap on the GPU race.  A bounded
+ * wait that runs out is recorded in the array's status word, which
+ * tf_noalloc_status reads (not tf_device_status).
  */
 int tf_qmm_noalloc(const uint16_t *x, int rows, int K,
                    const uint32_t *W, const uint16_t *scales, const uint16_t *biases,
                    int N, int bits, int group,
                    float *y, int64_t y_stride, void *stream);
+
+/*
+ * Reads and clears the status word of tf_qmm_noalloc's fixed array on the
+ * current device (synchronizes the device; allocates nothing).  TF_OK, or
+ * TF_EDEVICE if a no-allocation product gave up a bounded wait since the last
+ * read.  The paper has no counterpart.
+ */
+int tf_noalloc_status(void);
 
 /*
  * Fused stack of members written through one strided output (PR #788, "a
@@ -192,6 +206,18 @@ int tf_widen(const uint32_t *W, const uint16_t *scales, const uint16_t *biases,
              int N, int K, int bits, int group,
              uint32_t *W_out, uint16_t *s_out, uint16_t *b_out,
              int bits_out, int group_out, void *stream);
+
+/*
+ * tf_widen_host -- the same widen / regroup on HOST memory, for loaders that
+ * re-pack at load time before uploading (PR #788, the widen commit: the
+ * packer writes mixed-width members as one matrix).  Same arguments, checks,
+ * status codes and output bytes as tf_widen (W 16-byte aligned), with every
+ * pointer in host memory owned by the caller; no CUDA call is made.
+ */
+int tf_widen_host(const uint32_t *W, const uint16_t *scales, const uint16_t *biases,
+                  int N, int K, int bits, int group,
+                  uint32_t *W_out, uint16_t *s_out, uint16_t *b_out,
+                  int bits_out, int group_out);
 
 /* Common width of n members: (max bits, min group).  Host only. */
 int tf_common_width(const int *bits, const int *groups, int n, int *bits_out, int *group_out);

@@ -23,8 +23,8 @@ STATUS = {
     -5: "TF_EINVAL_PTR", -6: "TF_EINVAL_SIZE", -7: "TF_ENARROW", -8: "TF_EGROUP",
     -9: "TF_ESTACK", -10: "TF_ECUDA", -11: "TF_EDEVICE", -12: "TF_EINVAL_FLAGS", -13: "TF_EGATHER",
 }
-SYMBOLS = ("tf_qmm", "tf_qmm_ex", "tf_qmm_gather", "tf_qmm_noalloc", "tf_qmm_stack", "tf_widen",
-           "tf_common_width", "tf_qmm_bytes", "tf_device_status", "tf_set_launch_mode",
+SYMBOLS = ("tf_qmm", "tf_qmm_ex", "tf_qmm_gather", "tf_qmm_noalloc", "tf_noalloc_status", "tf_qmm_stack", "tf_widen",
+           "tf_widen_host", "tf_common_width", "tf_qmm_bytes", "tf_device_status", "tf_set_launch_mode",
            "tf_inject_stall", "tf_last_error_string", "tf_version")
 TF_LAUNCH_PDL, TF_LAUNCH_EARLY_WEIGHTS = 1, 2
 TF_OUT_BF16, TF_EPI_RELU2 = 1, 2
@@ -65,16 +65,18 @@ def lib():
         L.tf_qmm_stack.argtypes = [P, i32, i32, ctypes.POINTER(TfRun), i32,
                                    ctypes.POINTER(TfMember), i32, P, i64, P]
         L.tf_widen.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, i32, i32, P]
+        L.tf_widen_host.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, i32, i32]
         L.tf_common_width.argtypes = [P, P, i32, P, P]
         L.tf_qmm_bytes.argtypes = [i32, i32, i32, i32, P, P]
         L.tf_device_status.argtypes = []
+        L.tf_noalloc_status.argtypes = []
         L.tf_set_launch_mode.argtypes = [i32]
         L.tf_inject_stall.argtypes = []
         L.tf_last_error_string.restype = ctypes.c_char_p
         L.tf_version.restype = ctypes.c_char_p
         for name in ("tf_qmm", "tf_qmm_ex", "tf_qmm_gather", "tf_qmm_noalloc", "tf_qmm_stack", "tf_widen",
-                     "tf_common_width", "tf_qmm_bytes", "tf_device_status", "tf_set_launch_mode",
-                     "tf_inject_stall"):
+                     "tf_widen_host", "tf_common_width", "tf_qmm_bytes", "tf_device_status", "tf_noalloc_status",
+                     "tf_set_launch_mode", "tf_inject_stall"):
             getattr(L, name).restype = i32
         _lib = L
     return _lib
@@ -145,6 +147,20 @@ def tf_widen(W, scales, biases, N, K, bits, group, W_out, s_out, b_out, bits_out
                           _ptr(s_out), _ptr(b_out), bits_out, group_out, _stream(stream)))
 
 
+def tf_widen_host(W, scales, biases, N, K, bits, group, bits_out, group_out):
+    """Widen / regroup on host numpy arrays (uint32 W, uint16 scales/biases); returns (W_out, s_out, b_out)."""
+    import numpy as np
+    W = np.ascontiguousarray(W, dtype=np.uint32)
+    s = np.ascontiguousarray(scales, dtype=np.uint16)
+    b = np.ascontiguousarray(biases, dtype=np.uint16)
+    Wo = np.zeros((N, K * bits_out // 32), dtype=np.uint32)
+    so = np.zeros((N, K // group_out), dtype=np.uint16)
+    bo = np.zeros((N, K // group_out), dtype=np.uint16)
+    _check(lib().tf_widen_host(W.ctypes.data, s.ctypes.data, b.ctypes.data, N, K, bits, group, Wo.ctypes.data,
+                               so.ctypes.data, bo.ctypes.data, bits_out, group_out))
+    return Wo, so, bo
+
+
 def tf_common_width(bits_list, groups_list) -> tuple[int, int]:
     n = len(bits_list)
     b = (ctypes.c_int * n)(*bits_list)
@@ -162,6 +178,11 @@ def tf_qmm_bytes(N, K, bits, group) -> tuple[int, int]:
 
 def tf_device_status() -> None:
     _check(lib().tf_device_status())
+
+
+def tf_noalloc_status() -> None:
+    """Raise TfError(TF_EDEVICE) if a tf_qmm_noalloc product gave up a bounded wait (clears it)."""
+    _check(lib().tf_noalloc_status())
 
 
 def tf_set_launch_mode(mode: int) -> int:

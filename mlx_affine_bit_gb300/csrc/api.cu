@@ -181,17 +181,19 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-EncodeTiledFn g_encode = nullptr;
+// Looked up once from the driver; read by callers on any thread (the
+// no-allocation entry point runs outside the planner's mutex).
+std::atomic<EncodeTiledFn> g_encode{nullptr};
 
 int get_encoder() {
-    if (g_encode) return TF_OK;
+    if (g_encode.load(std::memory_order_acquire)) return TF_OK;
     void *fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
                                                      cudaEnableDefault, &q);
     if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
         return fail(TF_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    g_encode.store(reinterpret_cast<EncodeTiledFn>(fn), std::memory_order_release);
     return TF_OK;
 }
 
@@ -202,7 +204,7 @@ int encode_2d(CUtensorMap *m, const void *base, CUtensorMapDataType t, int esize
     cuuint64_t strides[1] = {(cuuint64_t)(cols * esize)};
     cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(m, t, 2, const_cast<void *>(base), dims, strides, box, estr,
+    CUresult r = g_encode.load(std::memory_order_acquire)(m, t, 2, const_cast<void *>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(TF_ECUDA, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
@@ -217,7 +219,7 @@ int encode_3d(CUtensorMap *m, const void *base, CUtensorMapDataType t, long long
     cuuint64_t strides[2] = {(cuuint64_t)s1, (cuuint64_t)s2};
     cuuint32_t box[3] = {(cuuint32_t)b0, (cuuint32_t)b1, (cuuint32_t)b2};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = g_encode(m, t, 3, const_cast<void *>(base), dims, strides, box, estr,
+    CUresult r = g_encode.load(std::memory_order_acquire)(m, t, 3, const_cast<void *>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(TF_ECUDA, "cuTensorMapEncodeTiled(3D) failed (" + std::to_string((int)r) + ")");
@@ -470,27 +472,15 @@ __global__ void widen_groups(const uint16_t *s, const uint16_t *b, uint16_t *so,
     bo[t] = b[n * ngi + g / ratio];
 }
 
-}  // namespace
-
-// Product with caller-provided scratch: the split-K partials, arrival counters
-// and status word live in memory the caller owns (used by tf_qmm_noalloc).
-// Allocates nothing: tensor maps are encoded into locals, no cache is grown.
-int tfq::product_with_scratch(const uint16_t *x, int rows, int K, const uint32_t *W,
-                              const uint16_t *s, const uint16_t *b, int N, int bits, int group,
-                              float *y, int64_t y_stride, cudaStream_t st, int nsm, float *ws,
-                              size_t ws_floats, int *counters, size_t n_counters, int *status) {
-    g_err.clear();
-    int rc = check_matrix(K, W, s, b, N, bits, group);
-    if (rc) return rc;
-    rc = check_io(x, rows, y);
-    if (rc) return rc;
-    if (y_stride < N) return fail(TF_EINVAL_STRIDE, "y_stride below N is refused");
+// One launch of up to 16 rows with caller-provided scratch: window rows
+// r0 .. r0 + w - 1 of x and y (w <= 16).  Allocates nothing: the tensor maps
+// are encoded into the launch parameters, no cache is grown.
+int window_with_scratch(const uint16_t *x, int w, int r0, int K, const uint32_t *W, const uint16_t *s,
+                        const uint16_t *b, int N, int bits, int group, float *y, int64_t y_stride,
+                        cudaStream_t st, int nsm, float *ws, int *counters, int *status) {
     const bool bulk = aligned(s, 16) && aligned(b, 16) && K % SEG == 0 && K % (8 * group) == 0;
     const bool sb3d = bulk && K % CHUNK == 0;
-    const Plan pl = make_plan(N, K, bits, group, rows, nsm, sb3d);
-    if (pl.nsl > 1 && ((size_t)pl.nchunks * rows * N > ws_floats || (size_t)pl.nmt > n_counters))
-        return fail(TF_EINVAL_SIZE, "split-K partials (" + std::to_string((size_t)pl.nchunks * rows * N * 4) +
-                                        " bytes) exceed the fixed scratch of the no-allocation entry point");
+    const Plan pl = make_plan(N, K, bits, group, w, nsm, sb3d);
     QmmParams P{};
     P.x = x;
     P.W = W;
@@ -499,7 +489,7 @@ int tfq::product_with_scratch(const uint16_t *x, int rows, int K, const uint32_t
     P.y = y;
     P.status = status;
     P.y_stride = y_stride;
-    P.rows = rows;
+    P.rows = w;
     P.K = K;
     P.N = N;
     P.nmt = pl.nmt;
@@ -509,6 +499,7 @@ int tfq::product_with_scratch(const uint16_t *x, int rows, int K, const uint32_t
     P.stages = pl.stages;
     P.bulk = bulk;
     P.sb3d = sb3d;
+    int rc = TF_OK;
     if (bulk) {
         rc = get_encoder();
         if (rc) return rc;
@@ -538,9 +529,9 @@ int tfq::product_with_scratch(const uint16_t *x, int rows, int K, const uint32_t
     P.cs_src[0] = 0;
     P.cs_len[0] = N;
     P.cs_dst[0] = 0;
-    for (int r = 0; r < 16; ++r) P.xrow[r] = P.yrow[r] = r;
-    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int), st);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(scratch status)");
+    for (int r = 0; r < 16; ++r) P.xrow[r] = P.yrow[r] = r0 + std::min(r, w - 1);
+    P.stall = g_stall.exchange(0);
+    cudaError_t e;
     if (pl.nsl > 1) {
         // The scratch keeps the last call's contents: the arrival counters must start at zero.
         e = cudaMemsetAsync(counters, 0, (size_t)pl.nmt * sizeof(int), st);
@@ -550,6 +541,41 @@ int tfq::product_with_scratch(const uint16_t *x, int rows, int K, const uint32_t
     }
     e = launch(bits, group, pl.rb, pl.mt, pl.cg, P, pl.grid, pl.smem, st, false);
     if (e != cudaSuccess) return cuda_fail(e, "qmm kernel launch");
+    return TF_OK;
+}
+
+}  // namespace
+
+// Product with caller-provided scratch: the split-K partials, arrival counters
+// and status word live in memory the caller owns (used by tf_qmm_noalloc).
+// More than 16 rows run as 16-row windows, one launch after another on the
+// stream, each reusing the scratch.  Every window's need is checked before the
+// first launch.
+int tfq::product_with_scratch(const uint16_t *x, int rows, int K, const uint32_t *W,
+                              const uint16_t *s, const uint16_t *b, int N, int bits, int group,
+                              float *y, int64_t y_stride, cudaStream_t st, int nsm, float *ws,
+                              size_t ws_floats, int *counters, size_t n_counters, int *status) {
+    g_err.clear();
+    int rc = check_matrix(K, W, s, b, N, bits, group);
+    if (rc) return rc;
+    rc = check_io(x, rows, y, MAX_ROWS);
+    if (rc) return rc;
+    if (y_stride < N) return fail(TF_EINVAL_STRIDE, "y_stride below N is refused");
+    const bool bulk = aligned(s, 16) && aligned(b, 16) && K % SEG == 0 && K % (8 * group) == 0;
+    const bool sb3d = bulk && K % CHUNK == 0;
+    // Windows hold 16 rows, the last one rows % 16 if that is not zero.
+    for (int w : {std::min(16, rows), rows % 16}) {
+        if (w == 0) continue;
+        const Plan pl = make_plan(N, K, bits, group, w, nsm, sb3d);
+        if (pl.nsl > 1 && ((size_t)pl.nchunks * w * N > ws_floats || (size_t)pl.nmt > n_counters))
+            return fail(TF_EINVAL_SIZE, "split-K partials (" + std::to_string((size_t)pl.nchunks * w * N * 4) +
+                                            " bytes) exceed the fixed scratch of the no-allocation entry point");
+    }
+    for (int r0 = 0; r0 < rows; r0 += 16) {
+        rc = window_with_scratch(x, std::min(16, rows - r0), r0, K, W, s, b, N, bits, group, y, y_stride, st, nsm,
+                                 ws, counters, status);
+        if (rc) return rc;
+    }
     return TF_OK;
 }
 
@@ -733,6 +759,46 @@ int tf_widen(const uint32_t *W, const uint16_t *scales, const uint16_t *biases, 
                                                                group / group_out);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "widen_groups launch");
+    return TF_OK;
+}
+
+int tf_widen_host(const uint32_t *W, const uint16_t *scales, const uint16_t *biases, int N, int K,
+                  int bits, int group, uint32_t *W_out, uint16_t *s_out, uint16_t *b_out, int bits_out,
+                  int group_out) {
+    g_err.clear();
+    int rc = check_matrix(K, W, scales, biases, N, bits, group);
+    if (rc) return rc;
+    if (!valid_bits(bits_out)) return fail(TF_EINVAL_BITS, "bits_out must be 2, 3, 4, 5, 6 or 8");
+    if (!valid_group(group_out)) return fail(TF_EINVAL_GROUP, "group_out must be 32, 64 or 128");
+    if (bits_out < bits) return fail(TF_ENARROW, "narrowing bits is refused");
+    if (group_out > group || group % group_out != 0)
+        return fail(TF_EGROUP, "a group that does not divide the source group is refused");
+    if (!W_out || !s_out || !b_out) return fail(TF_EINVAL_PTR, "NULL output pointer");
+    // Every 32 codes of a row fill exactly `bits` words in and `bits_out` words
+    // out; each code keeps its integer value.
+    const long long wi = (long long)K * bits / 32, wo = (long long)K * bits_out / 32;
+    const uint32_t mask = (1u << bits) - 1u;
+    for (long long n = 0; n < N; ++n) {
+        const uint32_t *src = W + n * wi;
+        uint32_t *dst = W_out + n * wo;
+        for (long long w = 0; w < wo; ++w) dst[w] = 0u;
+        for (long long k = 0; k < K; ++k) {
+            const long long ib = k * bits, ob = k * bits_out;
+            const long long iw = ib >> 5, ow = ob >> 5;
+            const int ish = (int)(ib & 31), osh = (int)(ob & 31);
+            uint64_t v = src[iw];
+            if (iw + 1 < wi) v |= (uint64_t)src[iw + 1] << 32;
+            const uint64_t c = (v >> ish) & mask;
+            dst[ow] |= (uint32_t)(c << osh);
+            if (osh + bits_out > 32) dst[ow + 1] |= (uint32_t)(c >> (32 - osh));
+        }
+    }
+    const long long ngi = K / group, ngo = K / group_out, ratio = group / group_out;
+    for (long long n = 0; n < N; ++n)
+        for (long long g = 0; g < ngo; ++g) {
+            s_out[n * ngo + g] = scales[n * ngi + g / ratio];
+            b_out[n * ngo + g] = biases[n * ngi + g / ratio];
+        }
     return TF_OK;
 }
 

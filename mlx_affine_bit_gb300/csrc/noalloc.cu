@@ -10,9 +10,11 @@
 // The array holds, in order, a status word, the split-K arrival counters and
 // the split-K partial sums.  Every GPU that loads the library holds it until
 // the process exits.  Every call shares it and it keeps the last call's
-// contents, so each call clears the counters and the status word it uses on
-// its own stream first; calls that overlap on the GPU (for example on two
-// streams at once) race on it.
+// contents, so each call clears the counters it uses on its own stream first;
+// calls that overlap on the GPU (for example on two streams at once) race on
+// it.  The status word is cleared once at set-up and then only by
+// tf_noalloc_status, so a bounded wait that ran out stays recorded until the
+// caller reads it.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -54,6 +56,8 @@ int device_scratch(DeviceScratch **out) {
             return tfq::fail_message(TF_ECUDA, "cudaGetSymbolAddress(scratch) failed");
         e = cudaDeviceGetAttribute(&d.nsm, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return tfq::fail_message(TF_ECUDA, "cudaDeviceGetAttribute failed");
+        e = cudaMemset(ptr, 0, STATUS_BYTES);
+        if (e != cudaSuccess) return tfq::fail_message(TF_ECUDA, "cudaMemset(scratch status) failed");
         d.base = static_cast<unsigned char *>(ptr);
     }
     *out = &d;
@@ -75,4 +79,19 @@ extern "C" int tf_qmm_noalloc(const uint16_t *x, int rows, int K, const uint32_t
                                      static_cast<cudaStream_t>(stream), d->nsm, partials,
                                      PARTIAL_BYTES / sizeof(float), counters,
                                      COUNTER_BYTES / sizeof(int), status);
+}
+
+extern "C" int tf_noalloc_status(void) {
+    DeviceScratch *d = nullptr;
+    const int rc = device_scratch(&d);
+    if (rc) return rc;
+    int v = 0;
+    cudaError_t e = cudaMemcpy(&v, d->base, sizeof v, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return tfq::fail_message(TF_ECUDA, "cudaMemcpy(scratch status) failed");
+    if (v) {
+        e = cudaMemset(d->base, 0, sizeof v);
+        if (e != cudaSuccess) return tfq::fail_message(TF_ECUDA, "cudaMemset(scratch status) failed");
+        return tfq::fail_message(TF_EDEVICE, "a no-allocation product gave up a bounded wait");
+    }
+    return tfq::fail_message(TF_OK, "");
 }

@@ -5,6 +5,7 @@ import os
 import re
 import subprocess
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -151,3 +152,30 @@ def test_stack_keeps_16_rows(tf):
     with pytest.raises(tf.TfError) as e:
         tf.tf_qmm_stack(A, 17, 256, [(A, A, A, 64, 4, 64)], [(0, 0, 64, 0)], A, 64, stream=0)
     assert e.value.rc == -3
+
+
+WIDEN_PAIRS = [(b0, g0, b1, g1) for b0 in (2, 3, 4, 5, 6, 8) for b1 in (2, 3, 4, 5, 6, 8) if b1 >= b0
+               for g0 in (32, 64, 128) for g1 in (32, 64, 128) if g0 % g1 == 0]
+
+
+@pytest.mark.parametrize("b0,g0,b1,g1", WIDEN_PAIRS)
+def test_widen_host_equals_oracle(tf, b0, g0, b1, g1):
+    # The host widen re-packs every code at the wider width and copies scales
+    # and biases to each finer group: byte for byte the oracle's widen.
+    import oracle
+    import synth
+    N, K = 9, 384
+    m = synth.make_matrix(N, K, b0, g0, 700 + 11 * b0 + g0 + b1, 0.001, 0.03)
+    got = tf.tf_widen_host(m.W, m.scales, m.biases, N, K, b0, g0, b1, g1)
+    want = oracle.widen(m.W, m.scales, m.biases, N, K, b0, g0, b1, g1)
+    for a, b in zip(got, want):
+        assert a.dtype == b.dtype and np.array_equal(a, b)
+
+
+def test_widen_host_refusals(tf):
+    import synth
+    m = synth.make_matrix(4, 256, 5, 64, 1, 0.001, 0.03)
+    for (b1, g1, code) in ((4, 64, -7), (5, 128, -8), (7, 64, -1), (5, 48, -2)):
+        with pytest.raises(tf.TfError) as e:
+            tf.tf_widen_host(m.W, m.scales, m.biases, 4, 256, 5, 64, b1, g1)
+        assert e.value.rc == code

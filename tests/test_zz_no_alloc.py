@@ -51,10 +51,56 @@ def test_noalloc_matches_tf_qmm_twice(N, K, bits, group, rows):
 
 
 def test_noalloc_refuses_beyond_its_scratch():
-    # 16 rows x 262144 columns x 6 chunks of split-K partials is far beyond the
-    # fixed scratch: refused on the host before any launch.
-    small = torch.zeros(1024, dtype=torch.int32, device=DEV)
-    y = torch.zeros(16, dtype=torch.float32, device=DEV)
+    # 16 rows x 16384 columns x 6 chunks of split-K partials (6.3 MB) is beyond
+    # the fixed scratch: refused on the host before any launch.  The buffers
+    # are real and as large as the shape claims, so even a planner that chose
+    # not to split K here would launch on valid memory.
+    N, K, bits, group, rows = 16384, 12288, 2, 32, 16
+    W = torch.zeros((N, K * bits // 32), dtype=torch.int32, device=DEV)
+    s = torch.zeros((N, K // group), dtype=torch.int16, device=DEV)
+    x = torch.zeros((rows, K), dtype=torch.int16, device=DEV)
+    y = torch.zeros((rows, N), dtype=torch.float32, device=DEV)
     with pytest.raises(tf.TfError) as e:
-        tf.tf_qmm_noalloc(small, 16, 12288, small, small, small, 262144, 2, 32, y, 262144)
+        tf.tf_qmm_noalloc(x, rows, K, W, s, s, N, bits, group, y, N)
     assert e.value.rc == -6 and "scratch" in str(e.value)
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("rows", [17, 40])
+def test_noalloc_rows_past_16(rows):
+    # More than 16 rows run as 16-row windows over the shared scratch (split K
+    # at 2048 x 12288): the same bits as tf_qmm, twice in a row.
+    m = synth.make_matrix(2048, 12288, 5, 64, 420 + rows, 0.001, 0.03)
+    dm = DevMatrix(m)
+    x = synth.make_x(rows, m.K, 421 + rows)
+    xd = dev(x)
+    ref = run_qmm(dm, xd)
+    for _ in range(2):
+        got = _noalloc(dm, xd)
+        torch.cuda.synchronize()
+        assert torch.equal(got.view(torch.int32), ref.view(torch.int32))
+    oracle_check(m, x, got.cpu().numpy(), sample_cols(m.N, 16, rows))
+
+
+def test_noalloc_reports_a_bounded_wait_that_ran_out():
+    # A withheld first stage (test hook) makes the kernel's bounded wait run
+    # out: tf_noalloc_status reports TF_EDEVICE once, and the next call is right.
+    m = synth.make_matrix(256, 1024, 4, 64, 430, 0.001, 0.03)
+    dm = DevMatrix(m)
+    x = synth.make_x(2, m.K, 431)
+    xd = dev(x)
+    torch.cuda.synchronize()
+    tf.tf_noalloc_status()                     # starts clean
+    tf.tf_inject_stall()
+    _noalloc(dm, xd)                           # about 2 s: the first stage never arrives
+    torch.cuda.synchronize()
+    with pytest.raises(tf.TfError) as e:
+        tf.tf_noalloc_status()
+    assert e.value.rc == -11
+    tf.tf_noalloc_status()                     # reading cleared it
+    ref = run_qmm(dm, xd)
+    got = _noalloc(dm, xd)
+    torch.cuda.synchronize()
+    tf.tf_noalloc_status()
+    assert torch.equal(got.view(torch.int32), ref.view(torch.int32))
+    oracle_check(m, x, got.cpu().numpy())
