@@ -175,16 +175,17 @@ def run_reference(args, cases):
     if rank != 0:
         return
     cores = os.cpu_count() or 1
+    cols = 64                                 # output columns of each product per step
     for _ in range(args.warmup):
-        cpu_sample(cases, 1, cores)
+        cpu_sample(cases, cols, cores)
     gbs_list, secs, nbytes = [], 0.0, 0
     for _ in range(args.steps):
-        g, t, b = cpu_sample(cases, 1, cores)
+        g, t, b = cpu_sample(cases, cols, cores)
         gbs_list.append(g)
         secs += t
         nbytes += b
     value = nbytes / secs / 1e9
-    sample = "fp64 oracle, one output column of each of the %d products per step" % len(cases)
+    sample = "fp64 oracle, the first %d output columns of each of the %d products per step" % (cols, len(cases))
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
@@ -227,11 +228,19 @@ def stack_items(cases, dev, tf):
         nb = (synth.algorithmic_bytes(6192, K, 5, 64, rows) + synth.algorithmic_bytes(48, K, 6, 64, rows)
               - rows * K * 2)                          # x is read once
         x_h = synth.make_x(rows, K, 60 + rows)
+
+        def grow(it, copies):
+            it["reps"] += [tuple((W.clone(), sc.clone(), bc.clone(), N, b, g) for (W, sc, bc, N, b, g) in it["reps"][0])
+                           for _ in range(copies - 1)]
+
+        offs = [0, 4096, 6144, 6192]                   # member columns in the output
         items.append(dict(label="stack r%d" % rows, N=stride, K=K, rows=rows, stack=True, members=members,
                           reps=[runs], x=torch.from_numpy(x_h.view(np.int16)).to(dev),
                           y=torch.empty((rows, stride), dtype=torch.float32, device=dev),
                           x_pin=torch.from_numpy(x_h.view(np.int16)).pin_memory(),
-                          y_pin=torch.empty((rows, stride), dtype=torch.float32).pin_memory(), bytes=nb))
+                          y_pin=torch.empty((rows, stride), dtype=torch.float32).pin_memory(), bytes=nb,
+                          check=[(m, x_h, o) for m, o in zip(mats, offs)]))
+        items[-1]["grow"] = lambda copies, it=items[-1]: grow(it, copies)
         per_step += nb
     torch.cuda.synchronize()
     return items, per_step
@@ -301,6 +310,162 @@ def options_items(cases, dev, tf):
     return items, per_step
 
 
+def kernel_source_sha() -> str:
+    """SHA-256 (16 hex digits) of the library's CUDA sources and headers: a
+    committed traffic figure counts only for the source it was captured on."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    pat = [os.path.join(ROOT, "mlx_affine_bit_gb300", "csrc", e) for e in ("*.cu", "*.cuh", "*.h")]
+    for f in sorted(sum((glob.glob(x) for x in pat), [])):
+        h.update(os.path.basename(f).encode())
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload: str):
+    """(bytes per step, note) from profiles/traffic_<workload>.txt, or (None, why)."""
+    path = os.path.join(ROOT, "profiles", "traffic_%s.txt" % workload)
+    if not os.path.exists(path):
+        return None, "no ncu capture of this workload is committed"
+    vals = {}
+    for line in open(path):
+        f = line.split()
+        if len(f) == 2 and not line.startswith("#"):
+            vals[f[0]] = f[1]
+    if vals.get("kernel_source_sha") != kernel_source_sha():
+        return None, "the committed ncu capture predates the current kernel source"
+    return int(vals["dram_bytes_per_step"]), "ncu dram__bytes_read.sum + dram__bytes_write.sum, " + \
+        vals.get("captured", "date not recorded")
+
+
+def _host_matrix(N, K, bits, group, seed):
+    return synth.make_matrix(N, K, bits, group, seed, 0.001, 0.03 if N < 100000 else 0.02)
+
+
+def product_items(cases, dev, min_bytes):
+    """Device inputs of one tf_qmm per case; each case rotates over enough weight
+    copies that a buffer is reused only after `min_bytes` of other traffic."""
+    import torch
+    items = []
+    for (label, N, K, bits, group, seed, rows) in cases:
+        m = _host_matrix(N, K, bits, group, seed)
+        W = torch.from_numpy(m.W.view(np.int32)).to(dev)
+        s = torch.from_numpy(m.scales.view(np.int16)).to(dev)
+        b = torch.from_numpy(m.biases.view(np.int16)).to(dev)
+        nb = synth.algorithmic_bytes(N, K, bits, group, rows)
+        pc = max(1, -(-min_bytes // nb))
+        reps = [(W, s, b)] + [(W.clone(), s.clone(), b.clone()) for _ in range(pc - 1)]
+        x_h = synth.make_x(rows, K, seed)
+        items.append(dict(label=label, N=N, K=K, bits=bits, group=group, rows=rows, reps=reps,
+                          x=torch.from_numpy(x_h.view(np.int16)).to(dev),
+                          y=torch.empty((rows, N), dtype=torch.float32, device=dev),
+                          x_pin=torch.from_numpy(x_h.view(np.int16)).pin_memory(),
+                          y_pin=torch.empty((rows, N), dtype=torch.float32).pin_memory(), bytes=nb,
+                          check=[(m, x_h, 0)]))
+    return items
+
+
+def launch_item(tf, it, c, st):
+    """Launch copy c of an item on stream st (one product, stack, gather or options call)."""
+    if "call" in it:
+        it["call"](c, st)
+        return
+    if it.get("stack"):
+        tf.tf_qmm_stack(it["x"], it["rows"], it["K"], it["reps"][c % len(it["reps"])], it["members"],
+                        it["y"], it["N"], st)
+        return
+    W, s, b = it["reps"][c % len(it["reps"])]
+    tf.tf_qmm(it["x"], it["rows"], it["K"], W, s, b, it["N"], it["bits"], it["group"], it["y"], it["N"], st)
+
+
+def item_launches(it) -> int:
+    """Kernel launches of one call of the item."""
+    return it.get("launches", len(it["reps"][0]) if it.get("stack") else 1)
+
+
+def time_item(tf, it, stream, warmup, replays=7):
+    """Per-call device time (us): a CUDA graph of one call on every weight copy
+    (>= 4 L2 sizes of weights), replayed `replays` times, each replay timed with
+    CUDA events on the replay stream; the median over replays of time / calls."""
+    import torch
+    n = len(it["reps"])
+    with torch.cuda.stream(stream):
+        for w in range(max(1, warmup)):
+            launch_item(tf, it, w, stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for c in range(n):
+            launch_item(tf, it, c, stream)
+    torch.cuda.synchronize()
+    per = []
+    with torch.cuda.stream(stream):
+        g.replay()
+        for _ in range(replays):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            per.append((e0, e1))
+    torch.cuda.synchronize()
+    del g
+    return statistics.median(e0.elapsed_time(e1) * 1e3 / n for e0, e1 in per)
+
+
+def case_row(label, nbytes, us, peak):
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"case": label, "bytes": nbytes, "median_us": round(us, 3), "gbs": round(gbs, 1),
+            "frac_of_peak": round(gbs / peak, 4), "frac_of_8tbs": round(gbs / 8000.0, 4)}
+
+
+# Target configurations timed in every default run beside the headline sweep.
+EXTRA_WORKLOADS = ("lmhead", "lmhead16", "decode", "stack")
+
+
+def build_items(workload, cases, dev, tf, min_bytes):
+    if workload == "gather":
+        items, per_step = gather_items(cases, dev, tf)
+    elif workload == "options":
+        items, per_step = options_items(cases, dev, tf)
+    elif workload == "stack":
+        items, per_step = stack_items(cases, dev, tf)
+    else:
+        items = product_items(cases, dev, min_bytes)
+        return items, sum(it["bytes"] for it in items)
+    copies = max(1, -(-min_bytes // per_step))
+    for it in items:
+        it["grow"](copies)
+    return items, per_step
+
+
+def oracle_checks(items, cols_per_case, nthreads):
+    """CPU-baseline leg: the fp64 oracle on a column sample of each case's last GPU
+    output.  Per case: worst |y - y64| / bound and the 1%-off control (max over
+    the sampled outputs of |y - y64(scales * 1.01)| / bound)."""
+    import oracle
+    out = {}
+    for it in items:
+        y_gpu = it["y_host"]
+        worst, ctrl = 0.0, float("inf")
+        for (m, x_h, col0) in it.get("check", []):
+            rng = np.random.default_rng(m.seed)
+            cols = np.unique(np.concatenate([[0, m.N - 1], rng.choice(m.N, min(cols_per_case, m.N), replace=False)]))
+            y64, absum = oracle.qmm(x_h, m.W, m.scales, m.biases, m.N, m.K, m.bits, m.group, cols=cols,
+                                    nthreads=nthreads)
+            B = oracle.bound(absum, m.K)
+            yg = y_gpu[:x_h.shape[0], col0 + cols].astype(np.float64)
+            xf = synth.bf16_bits_to_f32(x_h).astype(np.float64)
+            sx = xf.reshape(x_h.shape[0], m.K // m.group, m.group).sum(axis=2)
+            bias_part = sx @ synth.bf16_bits_to_f32(m.biases[cols]).astype(np.float64).T
+            worst = max(worst, float(np.max(np.abs(yg - y64) / B)))
+            ctrl = min(ctrl, float(np.max(np.abs(yg - (y64 + 0.01 * (y64 - bias_part))) / B)))
+        if it.get("check"):
+            out[it["label"]] = (worst, ctrl)
+    return out
+
+
 def run_gpu(args, cases):
     import torch
     import torch.distributed as dist
@@ -323,89 +488,43 @@ def run_gpu(args, cases):
     tf.tf_set_launch_mode({"plain": 0, "pdl": tf.TF_LAUNCH_PDL,
                            "early": tf.TF_LAUNCH_EARLY_WEIGHTS}[args.launch])
     stream = torch.cuda.current_stream()
+    cap = torch.cuda.Stream(device=dev)
+    min_bytes = 4 * L2_BYTES
 
     # Device-resident inputs; enough weight copies that a buffer is reused only
     # after >= 4 L2 sizes of other traffic.
-    cpu_cases = list(cases)                  # the oracle baseline runs on the members
-    if args.workload in ("gather", "options"):
-        items, per_step = (gather_items if args.workload == "gather" else options_items)(cases, dev, tf)
-        copies = max(1, -(-4 * L2_BYTES // per_step))
-        for it in items:
-            it["grow"](copies)
-        cases = []
-    elif args.workload == "stack":
-        items, per_step = stack_items(cases, dev, tf)
-        copies = max(1, -(-4 * L2_BYTES // per_step))
-        for it in items:
-            it["reps"] += [tuple((W.clone(), sc.clone(), bc.clone(), N, b, g) for (W, sc, bc, N, b, g) in it["reps"][0])
-                           for _ in range(copies - 1)]
-        cases = []
-    else:
-        per_step = sum(synth.algorithmic_bytes(N, K, b, g, r) for (_, N, K, b, g, _, r) in cases)
-        copies = max(1, -(-4 * L2_BYTES // per_step))
-        items = []
-    for (label, N, K, bits, group, seed, rows) in cases:
-        m = synth.make_matrix(N, K, bits, group, seed, 0.001, 0.03 if N < 100000 else 0.02)
-        W = torch.from_numpy(m.W.view(np.int32)).to(dev)
-        s = torch.from_numpy(m.scales.view(np.int16)).to(dev)
-        b = torch.from_numpy(m.biases.view(np.int16)).to(dev)
-        pc = max(copies, -(-4 * L2_BYTES // synth.algorithmic_bytes(N, K, bits, group, rows)))
-        reps = [(W, s, b)] + [(W.clone(), s.clone(), b.clone()) for _ in range(pc - 1)]
-        x_h = synth.make_x(rows, K, seed)
-        x = torch.from_numpy(x_h.view(np.int16)).to(dev)
-        y = torch.empty((rows, N), dtype=torch.float32, device=dev)
-        x_pin = torch.from_numpy(x_h.view(np.int16)).pin_memory()
-        y_pin = torch.empty((rows, N), dtype=torch.float32).pin_memory()
-        items.append(dict(label=label, N=N, K=K, bits=bits, group=group, rows=rows, reps=reps, x=x, y=y,
-                          x_pin=x_pin, y_pin=y_pin, bytes=synth.algorithmic_bytes(N, K, bits, group, rows)))
+    items, per_step = build_items(args.workload, cases, dev, tf, min_bytes)
+    copies = max(1, -(-min_bytes // per_step))
     torch.cuda.synchronize()
 
-    def launch(it, c, st):
-        if "call" in it:
-            it["call"](c, st)
-            return
-        if it.get("stack"):
-            tf.tf_qmm_stack(it["x"], it["rows"], it["K"], it["reps"][c % len(it["reps"])], it["members"],
-                            it["y"], it["N"], st)
-            return
-        W, s, b = it["reps"][c % len(it["reps"])]
-        tf.tf_qmm(it["x"], it["rows"], it["K"], W, s, b, it["N"], it["bits"], it["group"], it["y"],
-                  it["N"], st)
-
     # The timed region replays CUDA graphs, so host launch overhead does not
-    # enter the device timing.  The step graph holds `copies` consecutive steps
-    # (every product once per step, each step on the next weight copy); each
-    # product also has its own graph over its copies (>= 4 L2 sizes of weights)
-    # for its per-launch device time.
-    n = len(items)
-    cap = torch.cuda.Stream(device=dev)
+    # enter the device timing: a graph of `copies` consecutive steps (every
+    # call once per step, each step on the next weight copy) and one of the
+    # remaining steps % copies steps, so that exactly --steps steps are timed.
     with torch.cuda.stream(cap):
         for w in range(args.warmup):
             for it in items:
-                launch(it, w, cap)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=cap):
-        for c in range(copies):
-            for it in items:
-                launch(it, c, cap)
-    case_graphs = []
-    for it in items:
-        gph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gph, stream=cap):
-            for c in range(len(it["reps"])):
-                launch(it, c, cap)
-        case_graphs.append(gph)
-    torch.cuda.synchronize()
-    with torch.cuda.stream(cap):
-        for _ in range(max(1, args.warmup // copies)):
-            graph.replay()
-        for gph in case_graphs:
-            gph.replay()
+                launch_item(tf, it, w, cap)
     torch.cuda.synchronize()
 
-    replays = max(1, -(-args.steps // copies))
-    steps = replays * copies
+    def step_graph(nsteps, first):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            for c in range(first, first + nsteps):
+                for it in items:
+                    launch_item(tf, it, c, cap)
+        return g
+
+    full = step_graph(min(copies, args.steps), 0)
+    n_full, rem = divmod(args.steps, min(copies, args.steps))
+    rest = step_graph(rem, 0) if rem else None
+    torch.cuda.synchronize()
+    with torch.cuda.stream(cap):
+        full.replay()
+        if rest is not None:
+            rest.replay()
+    torch.cuda.synchronize()
+
     clk = ClockSampler(local)
     clk.start()
     if world > 1:
@@ -413,34 +532,31 @@ def run_gpu(args, cases):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    per_launch = []
-    with torch.cuda.stream(cap):          # graph replays run on the current stream
+    with torch.cuda.stream(cap):
         t0.record(cap)
-        for _ in range(replays):
-            graph.replay()
+        for _ in range(n_full):
+            full.replay()
+        if rest is not None:
+            rest.replay()
         t1.record(cap)
-        for it, gph in zip(items, case_graphs):
-            reps = max(1, -(-args.steps // len(it["reps"])))
-            c0 = torch.cuda.Event(enable_timing=True)
-            c1 = torch.cuda.Event(enable_timing=True)
-            c0.record(cap)
-            for _ in range(reps):
-                gph.replay()
-            c1.record(cap)
-            per_launch.append((c0, c1, reps * len(it["reps"])))
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clocks = clk.stop()
-    ms = t0.elapsed_time(t1)
-    ms = max_over_ranks(ms, dev)
+    ms = max_over_ranks(t0.elapsed_time(t1), dev)
     tf.tf_device_status()
-    per_launch = [[c0.elapsed_time(c1) / nl] for (c0, c1, nl) in per_launch]
-    args.steps = steps
+    del full, rest
+
+    # Per-call device times of the headline's calls (each its own graph).
+    peak, peak_kind = _peaks()
+    case_us = [time_item(tf, it, cap, 2) for it in items]
+    case_rows = [case_row(it["label"], it["bytes"], us, peak) for it, us in zip(items, case_us)]
+    for it in items:
+        it["y_host"] = it["y"].float().cpu().numpy() if it["y"].dtype == torch.float32 else None
 
     # ---- end to end: pinned host x in, host y out, through the C ABI ----
     # A step's activations arrive in one host-to-device copy and its results
-    # leave in one device-to-host copy (every product's x and y are views of one
+    # leave in one device-to-host copy (every call's x and y are views of one
     # device buffer each, 256-byte aligned).
     def joint(key, pin_key):
         offs, total = [], 0
@@ -470,49 +586,62 @@ def run_gpu(args, cases):
     for k in range(e2e_steps):
         x_dev.copy_(x_pin, non_blocking=True)
         for it in items:
-            launch(it, k, stream)
+            launch_item(tf, it, k, stream)
         y_pin.copy_(y_dev, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
     for it, (xo, yo) in zip(items, saved):
         it["x"], it["y"] = xo, yo
-    e2e_ms = max_over_ranks(e2e_ms, dev)
+    h2d, d2h = x_pin.numel(), y_pin.numel()
+    del x_dev, x_pin, y_dev, y_pin, x_views, y_views
 
-    peak, peak_kind = _peaks()
+    # ---- the other target configurations: each timed in its own graph ----
+    checked = list(items)
+    if args.workload == "sweep" and not args.no_extra:
+        for wl in EXTRA_WORKLOADS:
+            ex_items, _ = build_items(wl, workload_cases(wl), dev, tf, min_bytes)
+            for it in ex_items:
+                us = time_item(tf, it, cap, 2)
+                case_rows.append(case_row(it["label"], it["bytes"], us, peak))
+                it["y_host"] = it["y"].cpu().numpy()
+                for k in ("reps", "x", "y", "x_pin", "y_pin"):
+                    it.pop(k, None)
+                checked.append(it)
+            del ex_items
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+    tf.tf_device_status()
+
     value = job_throughput(per_step * args.steps, world, ms)
-    kern_ms = sum(statistics.mean(p) for p in per_launch)   # a step's summed launch times
+    kern_ms = sum(case_us) * 1e-3                            # a step's summed per-call times
     achieved = per_step / (kern_ms * 1e-3) / 1e9
-    case_rows = []
-    for i, it in enumerate(items):
-        med = statistics.median(per_launch[i])
-        case_rows.append({"case": it["label"], "bytes": it["bytes"], "median_us": round(med * 1e3, 3),
-                          "gbs": round(it["bytes"] / (med * 1e-3) / 1e9, 1),
-                          "frac_of_peak": round(it["bytes"] / (med * 1e-3) / 1e9 / peak, 4)})
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic_%s.txt" % args.workload)
-    if os.path.exists(tpath):
-        for line in open(tpath):
-            f = line.split()
-            if len(f) == 2 and f[0] == "dram_bytes_per_step":
-                traffic = int(f[1])
+    traffic, traffic_note = committed_traffic(args.workload)
     if rank == 0:
-        h2d = x_pin.numel()
-        d2h = y_pin.numel()
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
             cores = os.cpu_count() or 1
-            gbs, secs, nb = cpu_sample(cpu_cases, 1, cores)      # probe
+            gbs, secs, nb = cpu_sample(cases, 1, cores)      # probe
             cols = max(1, min(4096, int(12.0 / max(secs, 1e-3))))
             # About 10 s of oracle work: the column sample, repeated when even the
             # whole workload takes less.
             secs, nb, reps = 0.0, 0, 0
             while secs < 10.0 and reps < 200:
-                _, t, b = cpu_sample(cpu_cases, cols, cores)
+                _, t, b = cpu_sample(cases, cols, cores)
                 secs, nb, reps = secs + t, nb + b, reps + 1
             cpu = {"value": nb / secs / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
                    "sample": "fp64 oracle on the first %d output columns of each product, %d pass%s (%.1f s)"
                              % (cols, reps, "" if reps == 1 else "es", secs)}
+            # The same oracle checks each timed case's GPU output on 256 sampled columns.
+            checks = oracle_checks(checked, 256, cores)
+            for row in case_rows:
+                if row["case"] in checks:
+                    w, c = checks[row["case"]]
+                    row["oracle_worst_err_over_bound"] = round(w, 4)
+                    row["control_1pct_over_bound"] = round(c, 3)
+            cpu["checks"] = "each case's last GPU output against the fp64 oracle on 256 sampled columns " \
+                            "(+ first and last): worst err/bound, and the max ratio of the 1%-off-scales " \
+                            "control (must exceed 1); full-column checks are in the GPU tests"
         print(json.dumps({
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
@@ -525,16 +654,19 @@ def run_gpu(args, cases):
                              % (copies, per_step / 1e6)},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
-                         "traffic": traffic,
-                         "traffic_unit": "bytes per step (ncu, all qmm launches of one step)",
-                         "kernel": "tfq::qmm_kernel (all products of the step, bytes / summed launch time)"},
+                         "frac_of_8tbs_nominal": achieved / 8000.0,
+                         "traffic": traffic, "traffic_note": traffic_note,
+                         "traffic_unit": "bytes per step (all qmm launches of one step)",
+                         "kernel": "tfq::qmm_kernel (all products of the step, bytes / summed per-call time)"},
             "cpu_baseline": cpu,
             "e2e": {"value": job_throughput(per_step * e2e_steps, world, e2e_ms), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": sum(it.get("launches", len(it["reps"][0]) if it.get("stack") else 1)
-                                for it in items) * args.steps,
-            "timing": "CUDA graph of %d steps replayed %d times; per-product launch time from its own graph "
-                      "over >= 4 L2 sizes of weight copies" % (copies, replays),
+            "gpu_launches": sum(item_launches(it) for it in items) * args.steps,
+            "timing": "exactly %d steps: a CUDA graph of %d steps replayed %d times%s; per-case time: the median "
+                      "over 7 replays of a graph of one call per weight copy (>= 4 L2 sizes of weights)"
+                      % (args.steps, min(copies, args.steps), n_full,
+                         " plus one of %d steps" % rem if rem else ""),
+            "kernel_source_sha": kernel_source_sha(),
             "clocks": clocks,
             "cases": case_rows,
         }))
@@ -550,6 +682,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="sweep", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time only the headline workload (no LM head / decode / stack cases)")
     ap.add_argument("--launch", default="early", choices=["plain", "pdl", "early"])
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)

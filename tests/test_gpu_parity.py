@@ -5,7 +5,12 @@ Bars (TensorFold PR #788 row-kernel and tf-affine-ref commits):
   (ii)  each row alone equals the same row in 2-, 3-, 8- and 16-row windows,
         bit for bit, at every window position;
   (iii) strided and stacked outputs equal the contiguous result bit for bit,
-        with the gap columns untouched.
+        with the gap columns untouched;
+  and the negative control: the oracle with scales 1 % off lies outside the
+  bound on some column, asserted for every full-size workload.
+
+Full-size workloads are checked on every output column (TFQ_PARITY_COLS=n
+samples n columns instead, for quick runs).
 """
 import numpy as np
 import pytest
@@ -14,7 +19,7 @@ import torch
 import oracle
 import synth
 import mlx_affine_bit_gb300 as tf
-from tests.gpu_util import DEV, DevMatrix, control_ratio, dev, oracle_check, run_qmm, sample_cols
+from tests.gpu_util import DEV, DevMatrix, dev, full_cols, oracle_check, run_qmm, sample_cols
 
 pytestmark = pytest.mark.gpu
 
@@ -34,9 +39,8 @@ def built():
 def test_single_matrix_full():
     m, x = synth.single_matrix()
     y = run_qmm(DevMatrix(m), dev(x)).cpu().numpy()
-    worst = oracle_check(m, x, y)
-    assert control_ratio(m, x, y) > 1.0          # scales 1% off must exceed the bound
-    print("single matrix worst err/bound %.4f" % worst)
+    worst, ctrl = oracle_check(m, x, y, control=True)
+    print("single matrix worst err/bound %.4f, 1%%-off control %.2f" % (worst, ctrl))
 
 
 @pytest.mark.parametrize("bits", BITS)
@@ -52,13 +56,12 @@ def test_widths_small_full(bits, group, N, K, rows):
 
 
 @pytest.mark.parametrize("bits,group,seed", synth.width_sweep_cases())
-def test_width_sweep_4096_sampled(bits, group, seed):
+def test_width_sweep_4096(bits, group, seed):
     m = synth.width_sweep_matrix(bits, group, seed)
     x = synth.make_x(1, m.K, seed)
     y = run_qmm(DevMatrix(m), dev(x)).cpu().numpy()
-    cols = sample_cols(m.N, 96, seed)
-    oracle_check(m, x, y, cols)
-    control_ratio(m, x, y, cols)   # reported by the bench; here only computed
+    worst, ctrl = oracle_check(m, x, y, full_cols(m.N, seed), control=True)
+    print("sweep %d/g%d worst err/bound %.4f, control %.2f" % (bits, group, worst, ctrl))
 
 
 @pytest.mark.parametrize("N,K,seed", synth.DECODE_SHAPES)
@@ -73,8 +76,13 @@ def test_decode_windows_bit_exact(N, K, seed):
             yw = run_qmm(dm, xd[p0:p0 + w].contiguous())
             for i in range(w):
                 assert torch.equal(yw[i].view(torch.int32), alone[p0 + i][0].view(torch.int32)), (w, p0, i)
+    # Rows of every window equal the rows alone (above), so the 16-row output
+    # covers the 1-, 2-, 3- and 8-row cases too: every column against the oracle.
     y16 = run_qmm(dm, xd).cpu().numpy()
-    oracle_check(m, x, y16, sample_cols(N, 48, seed))
+    assert torch.equal(torch.from_numpy(y16[0:1]).view(torch.int32), alone[0].cpu().view(torch.int32))
+    worst, ctrl = oracle_check(m, x, y16, full_cols(N, seed), control=True)
+    _, ctrl1 = oracle_check(m, x[0:1], y16[0:1], full_cols(N, seed), control=True)
+    print("decode %dx%d worst err/bound %.4f, control r16 %.2f r1 %.2f" % (N, K, worst, ctrl, ctrl1))
 
 
 @pytest.mark.parametrize("rows", list(range(1, 17)))
@@ -202,12 +210,13 @@ def test_fused_stack(rows):
     tf.tf_qmm(xd, rows, K, m6.W, m6.s, m6.b, 48, 6, 64, y6, 48)
     assert torch.equal(y[:, :6192].view(torch.int32), y5.view(torch.int32))
     assert torch.equal(y[:, 6192:].view(torch.int32), y6.view(torch.int32))
-    # and every member is within the bound of the oracle on its unwidened matrix
+    # and every member is within the bound of the oracle on its unwidened
+    # matrix, on every column, with the 1%-off control outside it
     yn = y.cpu().numpy()
     off = 0
     for m in mats:
-        cols = sample_cols(m.N, 40, m.seed)
-        oracle_check(m, x, yn[:, off:off + m.N], cols)
+        worst, ctrl = oracle_check(m, x, yn[:, off:off + m.N], full_cols(m.N, m.seed), control=True)
+        print("stack r%d member %d/g%d (%d cols) worst %.4f, control %.2f" % (rows, m.bits, m.group, m.N, worst, ctrl))
         off += m.N
     # non-adjacent destinations through the column map
     members2 = [(0, 4096, 2048, 0), (1, 0, 48, 2048), (0, 0, 4096, 2096), (0, 6144, 48, 6192)]
@@ -235,7 +244,7 @@ def test_stack_refusals():
 # ------------------------------------------------------------------- LM head --
 
 @pytest.mark.parametrize("bits,group,seed", synth.LMHEAD_CASES)
-def test_lmhead_sampled(bits, group, seed):
+def test_lmhead(bits, group, seed):
     m = synth.lmhead_matrix(bits, group, seed)
     dm = DevMatrix(m)
     x = synth.make_x(16, m.K, seed)
@@ -243,9 +252,11 @@ def test_lmhead_sampled(bits, group, seed):
     y1 = run_qmm(dm, xd[0:1].contiguous())
     y16 = run_qmm(dm, xd)
     assert torch.equal(y16[0].view(torch.int32), y1[0].view(torch.int32))
-    cols = sample_cols(m.N, 64, seed)
-    oracle_check(m, x[0:1], y1.cpu().numpy(), cols)
-    oracle_check(m, x, y16.cpu().numpy(), cols)
+    cols = full_cols(m.N, seed)
+    y1n = y1.cpu().numpy()
+    w1, c1 = oracle_check(m, x[0:1], y1n, cols, control=True)
+    w16, c16 = oracle_check(m, x, y16.cpu().numpy(), cols, control=True)
+    print("LM head %d/g%d worst r1 %.4f r16 %.4f, control r1 %.2f r16 %.2f" % (bits, group, w1, w16, c1, c16))
 
 
 @pytest.mark.parametrize("bits,group", [(2, 64), (3, 128), (4, 32), (5, 64), (6, 32), (8, 128)])
@@ -368,13 +379,28 @@ def test_two_group_plans_repeatable(bits, group, rows):
     oracle_check(m, x, ref.cpu().numpy(), sample_cols(N, 32, bits))
 
 
+OPTION_SHAPES = [(4, 64, 300, 2048), (6, 32, 12304, 2048), (3, 128, 2048, 12288)]
+
+
+@pytest.mark.parametrize("bits,group,N,K", OPTION_SHAPES)
+def test_output_options_product_full(bits, group, N, K):
+    # The output options apply their epilogue to this fp32 product bit for bit
+    # (test_output_options): every column of it against the oracle, with the
+    # 1%-off control outside the bound.
+    m = synth.make_matrix(N, K, bits, group, 130 + bits, 0.001, 0.03)
+    x = synth.make_x(16, K, 131)
+    v = run_qmm(DevMatrix(m), dev(x)).cpu().numpy()
+    worst, ctrl = oracle_check(m, x, v, full_cols(N, bits), control=True)
+    print("options product %d/g%d %dx%d worst %.4f, control %.2f" % (bits, group, N, K, worst, ctrl))
+
+
 def _bf16_bits_to_f64(t: torch.Tensor) -> np.ndarray:
     h = t.cpu().numpy().view(np.uint16).astype(np.uint32) << 16
     return h.view(np.float32).astype(np.float64)
 
 
 @pytest.mark.parametrize("flags", [tf.TF_EPI_RELU2, tf.TF_OUT_BF16, tf.TF_OUT_BF16 | tf.TF_EPI_RELU2])
-@pytest.mark.parametrize("bits,group,N,K", [(4, 64, 300, 2048), (6, 32, 12304, 2048), (3, 128, 2048, 12288)])
+@pytest.mark.parametrize("bits,group,N,K", OPTION_SHAPES)
 def test_output_options(flags, bits, group, N, K):
     # fp32 or bf16 output, with or without the squared-ReLU epilogue: within
     # the bound of the oracle's product passed through the same epilogue, equal
@@ -439,7 +465,13 @@ def test_gather_equals_dense(flags):
             assert torch.all(tail == -7)
         else:
             assert torch.all(torch.isnan(tail))
-    # and against the oracle for a few slots
+    # every expert's dense product on every x row and column against the
+    # oracle, with the 1%-off control (each slot equals one of these rows)
+    for e, (m, dm) in enumerate(zip(mats, dms)):
+        yd = torch.zeros((x_rows, m.N), dtype=torch.float32, device=DEV)
+        tf.tf_qmm(xd, x_rows, K, dm.W, dm.s, dm.b, m.N, m.bits, m.group, yd, m.N)
+        oracle_check(m, x, yd.cpu().numpy(), control=True)
+    # and the slots themselves (with their output options) for a few slots
     for i in (0, 5, 36):
         m = mats[se[i]]
         cols = sample_cols(m.N, 24, i)
