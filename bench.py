@@ -485,8 +485,9 @@ def run_gpu(args, cases):
     if world > 1:
         dist.barrier()
     tf.lib()
-    tf.tf_set_launch_mode({"plain": 0, "pdl": tf.TF_LAUNCH_PDL,
-                           "early": tf.TF_LAUNCH_EARLY_WEIGHTS}[args.launch])
+    modes = {"plain": 0, "pdl": tf.TF_LAUNCH_PDL, "early": tf.TF_LAUNCH_EARLY_WEIGHTS,
+             "indep": tf.TF_LAUNCH_EARLY_WEIGHTS | tf.TF_LAUNCH_EARLY_X}
+    tf.tf_set_launch_mode(modes[args.launch])
     stream = torch.cuda.current_stream()
     cap = torch.cuda.Stream(device=dev)
     min_bytes = 4 * L2_BYTES
@@ -551,6 +552,18 @@ def run_gpu(args, cases):
     peak, peak_kind = _peaks()
     case_us = [time_item(tf, it, cap, 2) for it in items]
     case_rows = [case_row(it["label"], it["bytes"], us, peak) for it, us in zip(items, case_us)]
+    # The same calls when every product waits for the one before it before it
+    # reads x (early weights only): the order a chain of dependent layers needs.
+    dependent = None
+    if args.launch == "indep":
+        tf.tf_set_launch_mode(modes["early"])
+        dep_us = [time_item(tf, it, cap, 2) for it in items]
+        tf.tf_set_launch_mode(modes[args.launch])
+        dep_gbs = per_step / (sum(dep_us) * 1e-6) / 1e9
+        dependent = {"launch": "programmatic dependent launch, weights streamed before the dependency wait, x "
+                               "read after it (each product waits for the previous one)",
+                     "achieved": dep_gbs, "frac": dep_gbs / peak, "unit": "GB/s",
+                     "per_case_us": [round(u, 3) for u in dep_us]}
     for it in items:
         it["y_host"] = it["y"].float().cpu().numpy() if it["y"].dtype == torch.float32 else None
 
@@ -650,7 +663,11 @@ def run_gpu(args, cases):
             "config": {"workload": WORKLOAD_TEXT[args.workload], "parallelism": "replicas" if world > 1 else "1 GPU",
                        "launch": {"plain": "plain launches", "pdl": "programmatic dependent launch",
                                   "early": "programmatic dependent launch; weights streamed before the "
-                                           "dependency wait (weights are never written in the step)"}[args.launch],
+                                           "dependency wait (weights are never written in the step)",
+                                  "indep": "programmatic dependent launch; the step's products are independent "
+                                           "(no call writes any weights or x of the step), so each streams its "
+                                           "weights and reads x before its dependency wait and waits only before "
+                                           "writing y (TF_LAUNCH_EARLY_WEIGHTS | TF_LAUNCH_EARLY_X)"}[args.launch],
                        "l2": "weights rotate over %d copies (%.0f MB a step, >= 4x L2 between reuses)"
                              % (copies, per_step / 1e6)},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -659,6 +676,7 @@ def run_gpu(args, cases):
                          "traffic": traffic, "traffic_note": traffic_note,
                          "traffic_unit": "bytes per step (all qmm launches of one step)",
                          "kernel": "tfq::qmm_kernel (all products of the step, bytes / summed per-call time)"},
+            "dependent_x": dependent,
             "cpu_baseline": cpu,
             "e2e": {"value": job_throughput(per_step * e2e_steps, world, e2e_ms), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -685,7 +703,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="time only the headline workload (no LM head / decode / stack cases)")
-    ap.add_argument("--launch", default="early", choices=["plain", "pdl", "early"])
+    ap.add_argument("--launch", default="indep", choices=["plain", "pdl", "early", "indep"])
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     cases = workload_cases(args.workload)

@@ -241,10 +241,18 @@ int tf_device_status(void);
  *     weights, scales and biases before that wait.  Only valid when the kernel
  *     just before it in the stream does not write them (e.g. a decode step whose
  *     weights are fixed).
+ *   TF_LAUNCH_EARLY_X: as TF_LAUNCH_EARLY_WEIGHTS, and the product also reads
+ *     x and computes before that wait; it waits only before its first write
+ *     of y (or of split-K partials), so consecutive independent products
+ *     overlap.  Only valid when the kernel just before it in the stream writes
+ *     neither x nor the weights (products that share an activation, or a
+ *     sequence of independent products).  Stack runs and the windows of a
+ *     call with more than 16 rows keep their own ordering.
  * 0 (the default) launches plainly.  Negative status for unknown bits.
  */
 #define TF_LAUNCH_PDL 1
 #define TF_LAUNCH_EARLY_WEIGHTS 2
+#define TF_LAUNCH_EARLY_X 4
 int tf_set_launch_mode(int mode);
 
 /*

@@ -26,7 +26,7 @@ STATUS = {
 SYMBOLS = ("tf_qmm", "tf_qmm_ex", "tf_qmm_gather", "tf_qmm_noalloc", "tf_noalloc_status", "tf_qmm_stack", "tf_widen",
            "tf_widen_host", "tf_common_width", "tf_qmm_bytes", "tf_device_status", "tf_set_launch_mode",
            "tf_inject_stall", "tf_last_error_string", "tf_version")
-TF_LAUNCH_PDL, TF_LAUNCH_EARLY_WEIGHTS = 1, 2
+TF_LAUNCH_PDL, TF_LAUNCH_EARLY_WEIGHTS, TF_LAUNCH_EARLY_X = 1, 2, 4
 TF_OUT_BF16, TF_EPI_RELU2 = 1, 2
 
 

@@ -68,6 +68,8 @@ struct QmmParams {
     int bulk;           // 1: tensor-map TMA copies; 0: copies by the producer warp
     int sb3d;           // 1: scale/bias rows padded through a 3D map (K % CHUNK == 0)
     int early_w;        // 1: the producer may read W/scales/biases before the grid dependency resolves
+    int early_x;        // 1: x is read and the product computed before the grid dependency
+                        //    resolves; only the first write (y or split-K partials) waits for it
     int dep;            // programmatic dependent launch: 0 wait before x/y, release the next
                         // launch at once; 1 release it only after that wait (first run of a
                         // stack); 2 no wait before x/y, wait before exit (later runs of a stack)

@@ -634,10 +634,14 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
     // x, y and the split-K workspace may be touched by the previous kernel of
     // the stream (programmatic dependent launch): wait for it first -- unless
     // this is a later run of a stack, which shares nothing it writes with the
-    // runs before it.  The first run of a stack lets the later runs start only
-    // now, so that they too read x after its producer finished.
-    if (P.dep != 2) grid_dependency_wait();
+    // runs before it, or the caller declared that the previous kernel writes
+    // neither x nor the weights (early x): then only the first write below
+    // waits.  The first run of a stack lets the later runs start only now, so
+    // that they too read x after its producer finished.
+    const bool early_x = P.early_x && P.dep == 0;
+    if (P.dep != 2 && !early_x) grid_dependency_wait();
     if (P.dep == 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    bool waited = !early_x;                  // this thread has passed the dependency wait
     int cur_slice = -1;
     uint32_t it = 0;                         // stages this group has computed
     Ring ring;
@@ -770,6 +774,12 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                             *reinterpret_cast<float2 *>(pw + c * LR + r) = make_float2(p[t][nt][2 * h], p[t][nt][2 * h + 1]);
                     }
             named_bar(gbar, GT);
+            // Early x: every thread passes the dependency wait before the first
+            // write of y or of split-K partials (the fold below).
+            if (!waited && (P.nsl > 1 || k0 + CHUNK >= I.k_hi)) {
+                grid_dependency_wait();
+                waited = true;
+            }
             // Chunk sum C = P_0 + P_1 + ... in segment order, then the chunk fold.
             const int nseg = (k1 - k0 + SEG - 1) / SEG;
             const int chunk = k0 / CHUNK;
@@ -779,8 +789,15 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                 if (o < NOUT) {
                     const int fc = o / LR, fr = o - (o / LR) * LR;
                     const float *pf = pbuf + (buf * SEGS * ROWS + fc) * LR + fr;
-                    float C = pf[0];
-                    for (int j = 1; j < nseg; ++j) C = C + pf[j * ROWS * LR];
+                    // All segment partials are loaded first (independent loads in
+                    // flight together), then added in segment order.
+                    float v[SEGS];
+#pragma unroll
+                    for (int j = 0; j < SEGS; ++j) v[j] = j < nseg ? pf[j * ROWS * LR] : 0.f;
+                    float C = v[0];
+#pragma unroll
+                    for (int j = 1; j < SEGS; ++j)
+                        if (j < nseg) C = C + v[j];
                     if (P.nsl == 1) {
                         yacc[i] = chunk == 0 ? C : yacc[i] + C;
                         if (k0 + CHUNK >= I.k_hi) store_y(P, fr, n0 + fc, yacc[i]);
@@ -791,6 +808,10 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
             }
         }
     }
+    // Every thread passes the dependency wait before it exits, so that this
+    // grid never completes before the one it depends on (a later kernel's
+    // wait on this grid then covers every kernel before it).
+    if (!waited) grid_dependency_wait();
     if (CG == 1 && P.nsl > 1) {
         // Split K: once all of this CTA's chunk sums are out, one arrival ticket
         // per item, issued together; the last CTA to arrive at an item folds its

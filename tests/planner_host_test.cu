@@ -37,11 +37,17 @@ int main() {
                 for (int bits : bitss)
                     for (int group : groups) {
                         if (K % group) continue;
-                        for (int rows = 1; rows <= 16; ++rows) {
+                        for (int rows = 1; rows <= 16; ++rows)
+                        for (int overlap = 0; overlap < 2; ++overlap) {
                             const bool sb3d = K % CHUNK == 0;
-                            const Plan p = make_plan(N, K, bits, group, rows, nsm, sb3d);
+                            const Plan p = make_plan(N, K, bits, group, rows, nsm, sb3d, overlap != 0);
                             ++n;
-                            const int budget = p.ctas == 2 ? SMEM_PER_SM / 2 - 1024 : SMEM_MAX;
+                            const int budget = (p.ctas == 2 || p.half) ? SMEM_PER_SM / 2 - 1024 : SMEM_MAX;
+                            // A half-SM plan leaves room for the next product's CTA: the
+                            // 96-register one-m-tile kernel, one CTA per SM, only when asked.
+                            check(!p.half || (overlap && p.mt == 1 && p.cg == 1 && p.ctas == 1 && p.grid <= nsm &&
+                                              p.rb <= 2),
+                                  "half-SM plan", N, K, bits, group, rows, p);
                             check(p.rb == row_bucket(rows), "row bucket", N, K, bits, group, rows, p);
                             check(p.ctas == 1 || p.ctas == 2, "CTAs per SM", N, K, bits, group, rows, p);
                             check(p.mt == 1 || p.mt == 2, "m-tiles", N, K, bits, group, rows, p);

@@ -87,9 +87,11 @@ def test_unpack_host_build(tmp_path):
 
 def test_planner_host(tmp_path):
     # Every launch plan over a grid of shapes, widths, groups, row counts and SM
-    # counts fits shared memory, has a ring of 2-8 stages, uses an instantiated
-    # kernel, gives two consumer groups only one K slice and three stages, and
-    # covers K with whole teams of CTAs.  Host code only (stubbed launchers).
+    # counts, with and without overlapping products, fits shared memory (half
+    # the SM for the overlap plans), has a ring of 2-8 stages, uses an
+    # instantiated kernel, gives two consumer groups only one K slice and three
+    # stages, and covers K with whole teams of CTAs.  Host code only (stubbed
+    # launchers).
     import shutil
     nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
     if not os.path.exists(nvcc):

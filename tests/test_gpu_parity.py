@@ -290,7 +290,7 @@ def test_offset_codes_keep_margin(bits, group):
     assert worst < 0.25, worst
 
 
-@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("mode", [1, 2, 6])
 def test_launch_modes_bit_identical(mode):
     # A back-to-back sequence of products (including a split-K shape) gives the
     # same bits with programmatic dependent launch as with plain launches.
@@ -330,7 +330,7 @@ def test_plans_bit_identical(bits, group, rows):
     oracle_check(m, x, y.cpu().numpy(), sample_cols(N, 48, bits))
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("mode", [0, 1, 2, 6])
 def test_stack_launch_modes_bit_identical(mode):
     # Under programmatic dependent launch the runs of a stack overlap (the
     # first releases the rest only after its dependency wait; a split-K run
@@ -358,6 +358,31 @@ def test_stack_launch_modes_bit_identical(mode):
                 c += m.N
     finally:
         tf.tf_set_launch_mode(old)
+
+
+def test_early_x_writes_wait_for_the_previous_product():
+    # Under early-x launches a product computes before the previous kernel
+    # finishes but writes only after it: products that write the same output
+    # back to back leave the last one's result (write-after-write order), also
+    # when the later product is much smaller (it would otherwise finish first).
+    shapes = [(4096, 4096, 8, 32), (4096, 256, 2, 128), (4096, 2048, 4, 64)]
+    mats = [synth.make_matrix(N, K, b, g, 190 + i, 0.001, 0.03) for i, (N, K, b, g) in enumerate(shapes)]
+    dms = [DevMatrix(m) for m in mats]
+    xs = [dev(synth.make_x(1, m.K, 191 + i)) for i, m in enumerate(mats)]
+    refs = [run_qmm(dm, x) for dm, x in zip(dms, xs)]
+    old = tf.tf_set_launch_mode(tf.TF_LAUNCH_EARLY_WEIGHTS | tf.TF_LAUNCH_EARLY_X)
+    try:
+        y = torch.zeros((1, 4096), dtype=torch.float32, device=DEV)
+        for rep in range(30):
+            order = [0, 1, 2] if rep % 2 == 0 else [2, 0, 1]
+            for i in order:
+                m = mats[i]
+                tf.tf_qmm(xs[i], 1, m.K, dms[i].W, dms[i].s, dms[i].b, m.N, m.bits, m.group, y, m.N)
+            torch.cuda.synchronize()
+            assert torch.equal(y.view(torch.int32), refs[order[-1]].view(torch.int32)), rep
+    finally:
+        tf.tf_set_launch_mode(old)
+    tf.tf_device_status()
 
 
 @pytest.mark.parametrize("bits,group,rows", [(6, 32, 1), (4, 64, 1), (3, 32, 2), (6, 32, 16), (4, 128, 16)])
