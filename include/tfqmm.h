@@ -246,8 +246,9 @@ int tf_device_status(void);
  *     of y (or of split-K partials), so consecutive independent products
  *     overlap.  Only valid when the kernel just before it in the stream writes
  *     neither x nor the weights (products that share an activation, or a
- *     sequence of independent products).  Stack runs and the windows of a
- *     call with more than 16 rows keep their own ordering.
+ *     sequence of independent products).  The runs of a stack, the windows of
+ *     a call with more than 16 rows and the launches of a gather then overlap
+ *     the same way.
  * 0 (the default) launches plainly.  Negative status for unknown bits.
  */
 #define TF_LAUNCH_PDL 1

@@ -126,7 +126,7 @@ Plan layout(int N, int K, int bits, int group, int rows, int nsm, int ctas, bool
 
 // The launch plan, in order of preference (every choice gives the same bits):
 //  0. when consecutive products may overlap (early-x launches), 1-2 rows and at
-//     most four column tiles per SM: one m-tile per item, one CTA per SM within
+//     most eight column tiles per SM: one m-tile per item, one CTA per SM within
 //     half of the SM, so that the next product's CTA is resident beside it and
 //     computes while this one finishes (4096 x 4096 width sweep: 82 -> 69 us
 //     for the 18 products);
@@ -144,7 +144,7 @@ Plan make_plan(int N, int K, int bits, int group, int rows, int nsm, bool sb3d, 
     if (overlap && row_bucket(rows) <= 2) {
         // The one-m-tile kernel is capped at 96 registers: two CTAs of nine warps fit an SM.
         Plan h = layout(N, K, bits, group, rows, nsm, 1, sb3d, 1, 1, true);
-        if (h.nsl == 1 && h.stages >= 2 && (long long)h.nmt <= 4LL * nsm) {
+        if (h.nsl == 1 && h.stages >= 2 && (long long)h.nmt <= 8LL * nsm) {
             h.grid = std::min(h.grid, nsm);
             return h;
         }
@@ -394,8 +394,12 @@ int run_product(const uint16_t *x, int rows, int K, const uint32_t *W, const uin
     if (rc) return rc;
     const bool bulk = aligned(s, 16) && aligned(b, 16) && K % SEG == 0 && K % (8 * group) == 0;
     const bool sb3d = bulk && K % CHUNK == 0;
+    // Early x: the kernel before this launch writes neither x nor the weights.
+    // That holds for every run of a stack, window of a long call or gather
+    // launch too (they only share x), so each launch then computes before its
+    // dependency wait and waits only before its first write and at its exit.
     const int mode = g_launch_mode.load(std::memory_order_relaxed);
-    const bool overlap = (mode & TF_LAUNCH_EARLY_X) != 0 && stack_pos < 0;
+    const bool overlap = (mode & TF_LAUNCH_EARLY_X) != 0;
     const Plan pl = make_plan(N, K, bits, group, rows, d->nsm, sb3d, overlap);
     if (pl.cg > 1 && pl.nsl != 1) return fail(TF_EINVAL_SIZE, "internal: two consumer groups need one K slice");
     QmmParams P{};
@@ -450,7 +454,7 @@ int run_product(const uint16_t *x, int rows, int K, const uint32_t *W, const uin
     P.stall = g_stall.exchange(0);
     // Runs of a stack read x and write disjoint columns: after the first, a run
     // without split-K overlaps the runs before it (see QmmParams::dep).
-    P.dep = stack_pos < 0 ? 0 : stack_pos == 0 ? 1 : pl.nsl == 1 ? 2 : 0;
+    P.dep = stack_pos < 0 || overlap ? 0 : stack_pos == 0 ? 1 : pl.nsl == 1 ? 2 : 0;
     const cudaError_t e = launch(bits, group, pl.rb, pl.mt, pl.cg, P, pl.grid, pl.smem, st,
                                  (mode & (TF_LAUNCH_PDL | TF_LAUNCH_EARLY_WEIGHTS | TF_LAUNCH_EARLY_X)) != 0);
     if (e != cudaSuccess) return cuda_fail(e, "qmm kernel launch");
