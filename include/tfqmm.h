@@ -60,6 +60,8 @@ extern "C" {
 #define TF_EDEVICE (-11)      /* a kernel reported a bounded wait that ran out (device status) */
 #define TF_EINVAL_FLAGS (-12) /* output flags other than TF_OUT_BF16 | TF_EPI_RELU2 */
 #define TF_EGATHER (-13)      /* empty slot table, or a slot naming a missing expert or x row */
+#define TF_EBOUNDS (-14)      /* the bounds-checking debug build (libtfqmm_debug.so) found an index
+                                 outside its buffer (device status; the access was skipped) */
 
 /*
  * tf_qmm -- one quantized product.
@@ -227,7 +229,8 @@ int tf_qmm_bytes(int N, int K, int bits, int group, int64_t *w_bytes, int64_t *s
 
 /*
  * Reads and clears the device status word of the current device (synchronizes
- * the device).  TF_OK, or TF_EDEVICE if a kernel gave up a bounded wait.
+ * the device).  TF_OK, TF_EDEVICE if a kernel gave up a bounded wait, or (debug
+ * build only) TF_EBOUNDS if a kernel found an index outside its buffer.
  */
 int tf_device_status(void);
 

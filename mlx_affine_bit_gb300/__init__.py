@@ -16,12 +16,14 @@ import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 SO = os.path.join(HERE, "_build", "libtfqmm.so")
+SO_DEBUG = os.path.join(HERE, "_build", "libtfqmm_debug.so")   # bounds-checking build (tfqmm_debug.h)
 
 TF_OK = 0
 STATUS = {
     -1: "TF_EINVAL_BITS", -2: "TF_EINVAL_GROUP", -3: "TF_EINVAL_ROWS", -4: "TF_EINVAL_STRIDE",
     -5: "TF_EINVAL_PTR", -6: "TF_EINVAL_SIZE", -7: "TF_ENARROW", -8: "TF_EGROUP",
     -9: "TF_ESTACK", -10: "TF_ECUDA", -11: "TF_EDEVICE", -12: "TF_EINVAL_FLAGS", -13: "TF_EGATHER",
+    -14: "TF_EBOUNDS",
 }
 SYMBOLS = ("tf_qmm", "tf_qmm_ex", "tf_qmm_gather", "tf_qmm_noalloc", "tf_noalloc_status", "tf_qmm_stack", "tf_widen",
            "tf_widen_host", "tf_common_width", "tf_qmm_bytes", "tf_device_status", "tf_set_launch_mode",
@@ -47,39 +49,55 @@ class TfMember(ctypes.Structure):
 
 
 _lib = None
+_debug_lib = None
 
 
 def lib():
     """The loaded libtfqmm (raises if it has not been built)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(SO):
-            raise ImportError("libtfqmm.so is not built (%s); run mlx_affine_bit_gb300.build.build()" % SO)
-        L = ctypes.CDLL(SO)
-        P, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
-        L.tf_qmm.argtypes = [P, i32, i32, P, P, P, i32, i32, i32, P, i64, P]
-        L.tf_qmm_noalloc.argtypes = [P, i32, i32, P, P, P, i32, i32, i32, P, i64, P]
-        L.tf_qmm_ex.argtypes = [P, i32, i32, P, P, P, i32, i32, i32, P, i64, i32, P]
-        L.tf_qmm_gather.argtypes = [P, i32, i32, ctypes.POINTER(TfRun), i32, ctypes.POINTER(ctypes.c_int),
-                                    ctypes.POINTER(ctypes.c_int), i32, P, i64, i32, P]
-        L.tf_qmm_stack.argtypes = [P, i32, i32, ctypes.POINTER(TfRun), i32,
-                                   ctypes.POINTER(TfMember), i32, P, i64, P]
-        L.tf_widen.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, i32, i32, P]
-        L.tf_widen_host.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, i32, i32]
-        L.tf_common_width.argtypes = [P, P, i32, P, P]
-        L.tf_qmm_bytes.argtypes = [i32, i32, i32, i32, P, P]
-        L.tf_device_status.argtypes = []
-        L.tf_noalloc_status.argtypes = []
-        L.tf_set_launch_mode.argtypes = [i32]
-        L.tf_inject_stall.argtypes = []
-        L.tf_last_error_string.restype = ctypes.c_char_p
-        L.tf_version.restype = ctypes.c_char_p
-        for name in ("tf_qmm", "tf_qmm_ex", "tf_qmm_gather", "tf_qmm_noalloc", "tf_qmm_stack", "tf_widen",
-                     "tf_widen_host", "tf_common_width", "tf_qmm_bytes", "tf_device_status", "tf_noalloc_status",
-                     "tf_set_launch_mode", "tf_inject_stall"):
-            getattr(L, name).restype = i32
-        _lib = L
+        _lib = _load(SO)
     return _lib
+
+
+def debug_lib():
+    """The loaded bounds-checking build, libtfqmm_debug.so (same entry points, plus tf_debug_shrink_y)."""
+    global _debug_lib
+    if _debug_lib is None:
+        _debug_lib = _load(SO_DEBUG)
+        _debug_lib.tf_debug_shrink_y.argtypes = [ctypes.c_int]
+        _debug_lib.tf_debug_shrink_y.restype = ctypes.c_int
+    return _debug_lib
+
+
+def _load(path):
+    """Open one build of the library and declare its entry points' argument types."""
+    if not os.path.exists(path):
+        raise ImportError("%s is not built; run mlx_affine_bit_gb300.build.build()" % path)
+    L = ctypes.CDLL(path)
+    P, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    L.tf_qmm.argtypes = [P, i32, i32, P, P, P, i32, i32, i32, P, i64, P]
+    L.tf_qmm_noalloc.argtypes = [P, i32, i32, P, P, P, i32, i32, i32, P, i64, P]
+    L.tf_qmm_ex.argtypes = [P, i32, i32, P, P, P, i32, i32, i32, P, i64, i32, P]
+    L.tf_qmm_gather.argtypes = [P, i32, i32, ctypes.POINTER(TfRun), i32, ctypes.POINTER(ctypes.c_int),
+                                ctypes.POINTER(ctypes.c_int), i32, P, i64, i32, P]
+    L.tf_qmm_stack.argtypes = [P, i32, i32, ctypes.POINTER(TfRun), i32,
+                               ctypes.POINTER(TfMember), i32, P, i64, P]
+    L.tf_widen.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, i32, i32, P]
+    L.tf_widen_host.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P, i32, i32]
+    L.tf_common_width.argtypes = [P, P, i32, P, P]
+    L.tf_qmm_bytes.argtypes = [i32, i32, i32, i32, P, P]
+    L.tf_device_status.argtypes = []
+    L.tf_noalloc_status.argtypes = []
+    L.tf_set_launch_mode.argtypes = [i32]
+    L.tf_inject_stall.argtypes = []
+    L.tf_last_error_string.restype = ctypes.c_char_p
+    L.tf_version.restype = ctypes.c_char_p
+    for name in ("tf_qmm", "tf_qmm_ex", "tf_qmm_gather", "tf_qmm_noalloc", "tf_qmm_stack", "tf_widen",
+                 "tf_widen_host", "tf_common_width", "tf_qmm_bytes", "tf_device_status", "tf_noalloc_status",
+                 "tf_set_launch_mode", "tf_inject_stall"):
+        getattr(L, name).restype = i32
+    return L
 
 
 def _ptr(t) -> int | None:

@@ -1,4 +1,10 @@
-"""Build libtfqmm.so in-tree with nvcc for sm_103a (one -gencode, parallel units)."""
+"""Build libtfqmm.so in-tree with nvcc for sm_103a (one -gencode, parallel units).
+
+Two libraries come out of the same sources: libtfqmm.so (the product) and
+libtfqmm_debug.so, built with TF_DEBUG_BOUNDS, whose kernels check every shared-
+and global-memory index against its buffer and report a violation through the
+device status word (TF_EBOUNDS) instead of making the access.
+"""
 from __future__ import annotations
 
 import glob
@@ -12,9 +18,11 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 SO = os.path.join(OUT, "libtfqmm.so")
+SO_DEBUG = os.path.join(OUT, "libtfqmm_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
+VARIANTS = ((SO, OUT, []), (SO_DEBUG, os.path.join(OUT, "debug"), ["-DTF_DEBUG_BOUNDS"]))
 
 
 def _nvcc() -> str:
@@ -32,27 +40,34 @@ def _stale(target: str, deps: list[str]) -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(OUT, exist_ok=True)
     nvcc = _nvcc()
     units = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + \
         glob.glob(os.path.join(ROOT, "include", "*.h"))
+    jobs = []
+    for (_, out, defs) in VARIANTS:
+        os.makedirs(out, exist_ok=True)
+        for src in units:
+            jobs.append((src, os.path.join(out, os.path.basename(src)[:-3] + ".o"), defs))
 
-    def compile_unit(src: str) -> str:
-        obj = os.path.join(OUT, os.path.basename(src)[:-3] + ".o")
+    def compile_unit(job) -> str:
+        src, obj, defs = job
         if force or _stale(obj, [src] + headers):
-            cmd = [nvcc, *ARCH, *FLAGS, "-c", src, "-o", obj]
+            cmd = [nvcc, *ARCH, *FLAGS, *defs, "-c", src, "-o", obj]
             if verbose:
                 print(" ".join(cmd))
             subprocess.check_call(cmd)
         return obj
 
-    with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
-        objs = list(ex.map(compile_unit, units))
-    if force or _stale(SO, objs):
-        tmp = SO + ".tmp%d" % os.getpid()
-        subprocess.check_call([nvcc, *ARCH, "-shared", "-o", tmp, *objs])
-        os.replace(tmp, SO)
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4)) as ex:
+        objs = list(ex.map(compile_unit, jobs))
+    for i, (so, _, _) in enumerate(VARIANTS):
+        mine = objs[i * len(units):(i + 1) * len(units)]
+        if force or _stale(so, mine):
+            tmp = so + ".tmp%d" % os.getpid()
+            # -Bsymbolic: each library binds its own symbols first (both may share a process).
+            subprocess.check_call([nvcc, *ARCH, "-shared", "-Xlinker", "-Bsymbolic", "-o", tmp, *mine])
+            os.replace(tmp, so)
     return SO
 
 

@@ -315,6 +315,9 @@ struct DevState {
 std::mutex g_mu;
 std::atomic<int> g_launch_mode{0};
 std::atomic<int> g_stall{0};          // test hook armed by tf_inject_stall (one launch)
+#ifdef TF_DEBUG_BOUNDS
+std::atomic<int> g_shrink{0};         // debug hook: rows to drop from the next launch's y extent
+#endif
 std::map<int, DevState> g_dev;
 std::map<std::pair<int, cudaStream_t>, StreamWs> g_ws;
 
@@ -382,6 +385,7 @@ struct Io {
     int out = 0;            // OUT_BF16 | OUT_RELU2
     bool map = false;
     int xrow[16] = {}, yrow[16] = {};
+    int x_rows = 0, y_rows = 0;   // rows of the call's x and y (0: the launch's rows)
 };
 
 int run_product(const uint16_t *x, int rows, int K, const uint32_t *W, const uint16_t *s,
@@ -442,12 +446,19 @@ int run_product(const uint16_t *x, int rows, int K, const uint32_t *W, const uin
         P.xrow[r] = io && io->map ? io->xrow[r] : r;
         P.yrow[r] = io && io->map ? io->yrow[r] : r;
     }
+    P.x_rows = io && io->x_rows ? io->x_rows : rows;
+    P.y_rows = io && io->y_rows ? io->y_rows : rows;
+#ifdef TF_DEBUG_BOUNDS
+    P.y_rows -= g_shrink.exchange(0);
+#endif
     if (pl.nsl > 1) {
         StreamWs *w = nullptr;
         rc = stream_ws(st, (size_t)pl.nchunks * rows * N, (size_t)pl.nmt, &w);
         if (rc) return rc;
         P.ws = w->ws;
         P.counters = w->cnt;
+        P.ws_elems = (long long)pl.nchunks * rows * N;
+        P.n_counters = pl.nmt;
     }
     P.early_x = overlap;
     P.early_w = (mode & TF_LAUNCH_EARLY_WEIGHTS) != 0 || P.early_x;
@@ -498,9 +509,9 @@ __global__ void widen_groups(const uint16_t *s, const uint16_t *b, uint16_t *so,
 // One launch of up to 16 rows with caller-provided scratch: window rows
 // r0 .. r0 + w - 1 of x and y (w <= 16).  Allocates nothing: the tensor maps
 // are encoded into the launch parameters, no cache is grown.
-int window_with_scratch(const uint16_t *x, int w, int r0, int K, const uint32_t *W, const uint16_t *s,
-                        const uint16_t *b, int N, int bits, int group, float *y, int64_t y_stride,
-                        cudaStream_t st, int nsm, float *ws, int *counters, int *status) {
+int window_with_scratch(const uint16_t *x, int w, int r0, int total_rows, int K, const uint32_t *W,
+                        const uint16_t *s, const uint16_t *b, int N, int bits, int group, float *y,
+                        int64_t y_stride, cudaStream_t st, int nsm, float *ws, int *counters, int *status) {
     const bool bulk = aligned(s, 16) && aligned(b, 16) && K % SEG == 0 && K % (8 * group) == 0;
     const bool sb3d = bulk && K % CHUNK == 0;
     const Plan pl = make_plan(N, K, bits, group, w, nsm, sb3d);
@@ -553,6 +564,7 @@ int window_with_scratch(const uint16_t *x, int w, int r0, int K, const uint32_t 
     P.cs_len[0] = N;
     P.cs_dst[0] = 0;
     for (int r = 0; r < 16; ++r) P.xrow[r] = P.yrow[r] = r0 + std::min(r, w - 1);
+    P.x_rows = P.y_rows = total_rows;
     P.stall = g_stall.exchange(0);
     cudaError_t e;
     if (pl.nsl > 1) {
@@ -561,6 +573,8 @@ int window_with_scratch(const uint16_t *x, int w, int r0, int K, const uint32_t 
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(scratch counters)");
         P.ws = ws;
         P.counters = counters;
+        P.ws_elems = (long long)pl.nchunks * w * N;
+        P.n_counters = pl.nmt;
     }
     e = launch(bits, group, pl.rb, pl.mt, pl.cg, P, pl.grid, pl.smem, st, false);
     if (e != cudaSuccess) return cuda_fail(e, "qmm kernel launch");
@@ -595,8 +609,8 @@ int tfq::product_with_scratch(const uint16_t *x, int rows, int K, const uint32_t
                                             " bytes) exceed the fixed scratch of the no-allocation entry point");
     }
     for (int r0 = 0; r0 < rows; r0 += 16) {
-        rc = window_with_scratch(x, std::min(16, rows - r0), r0, K, W, s, b, N, bits, group, y, y_stride, st, nsm,
-                                 ws, counters, status);
+        rc = window_with_scratch(x, std::min(16, rows - r0), r0, rows, K, W, s, b, N, bits, group, y, y_stride, st,
+                                 nsm, ws, counters, status);
         if (rc) return rc;
     }
     return TF_OK;
@@ -618,6 +632,7 @@ int product_rows(const uint16_t *x, int rows, int K, const uint32_t *W, const ui
     io.out = out;
     if (rows <= 16) return run_product(x, rows, K, W, s, b, N, bits, group, y, y_stride, 1, &src, &len, &dst, st, -1, &io);
     io.map = true;
+    io.x_rows = io.y_rows = rows;
     int pos = 0;
     for (int r0 = 0; r0 < rows; r0 += 16) {
         const int w = std::min(16, rows - r0);
@@ -737,6 +752,8 @@ int tf_qmm_gather(const uint16_t *x, int x_rows, int K, const tf_run *experts, i
         Io io;
         io.out = flags;
         io.map = true;
+        io.x_rows = x_rows;
+        io.y_rows = n_slots;
         int n = 0;
         for (int i = 0; i <= n_slots; ++i) {
             const bool take = i < n_slots && slot_expert[i] == e;
@@ -863,6 +880,7 @@ int tf_device_status(void) {
     if (v) {
         e = cudaMemset(d->status, 0, sizeof v);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
+        if (v & STATUS_BOUNDS) return fail(TF_EBOUNDS, "the debug build found an index outside its buffer");
         return fail(TF_EDEVICE, "a kernel gave up a bounded wait");
     }
     return TF_OK;
@@ -880,6 +898,15 @@ int tf_inject_stall(void) {
     g_stall.store(1);
     return TF_OK;
 }
+
+#ifdef TF_DEBUG_BOUNDS
+int tf_debug_shrink_y(int rows) {
+    g_err.clear();
+    if (rows < 0 || rows > 16) return fail(TF_EINVAL_ROWS, "rows must be in [0, 16]");
+    g_shrink.store(rows);
+    return TF_OK;
+}
+#endif
 
 const char *tf_last_error_string(void) { return g_err.c_str(); }
 

@@ -91,6 +91,8 @@ extern "C" int tf_noalloc_status(void) {
     if (v) {
         e = cudaMemset(d->base, 0, sizeof v);
         if (e != cudaSuccess) return tfq::fail_message(TF_ECUDA, "cudaMemset(scratch status) failed");
+        if (v & tfq::STATUS_BOUNDS)
+            return tfq::fail_message(TF_EBOUNDS, "the debug build found an index outside its buffer");
         return tfq::fail_message(TF_EDEVICE, "a no-allocation product gave up a bounded wait");
     }
     return tfq::fail_message(TF_OK, "");

@@ -2,6 +2,13 @@
 // the kernel template (qmm_kernel.cuh).  Internal to libtfqmm.
 #pragma once
 #include <cuda.h>   // CUtensorMap (type only; the encoder is fetched at run time)
+
+// The bounds-checking debug build puts its internals in a namespace of its
+// own, so that its symbols (kernels, launchers) never meet the product's when
+// a process loads both libraries.
+#ifdef TF_DEBUG_BOUNDS
+#define tfq tfq_debug
+#endif
 #include <stdint.h>
 
 #if defined(__CUDACC__)
@@ -82,7 +89,16 @@ struct QmmParams {
     int out;            // OUT_* bits: bf16 output (y holds bf16), squared-ReLU epilogue
     int xrow[16];       // window row r reads x row xrow[r] (K elements apart) ...
     int yrow[16];       // ... and writes y row yrow[r] (y_stride elements apart)
+    // Extents the call's arguments give each buffer, for the bounds checks of
+    // the debug build: x rows, y rows, split-K partial floats, arrival counters.
+    int x_rows, y_rows;
+    long long ws_elems;
+    int n_counters;
 };
+
+// Bits of the device status word.
+constexpr int STATUS_WAIT = 1;      // a bounded wait ran out
+constexpr int STATUS_BOUNDS = 2;    // the debug build found an index outside its buffer
 
 constexpr int OUT_BF16 = 1;    // y is bf16, each output rounded to nearest even
 constexpr int OUT_RELU2 = 2;   // y = max(v, 0)^2 of the fp32 result v (before any bf16 rounding)

@@ -18,6 +18,11 @@
 //
 // Every wait on an mbarrier is bounded in time; on expiry the kernel records
 // it in the device status word, stops waiting and runs to completion.
+//
+// Built with TF_DEBUG_BOUNDS, every shared- and global-memory index the kernel
+// computes is checked against its buffer before the access; an index outside
+// it sets a bit of the device status word and the access is skipped (reads
+// give zero).  The release build compiles each check to `true`.
 #pragma once
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -28,6 +33,35 @@
 namespace tfq {
 
 // ------------------------------------------------------------ primitives --
+
+#ifdef TF_DEBUG_BOUNDS
+static __device__ __noinline__ bool bounds_fail(int *status) {
+    atomicOr(status, STATUS_BOUNDS);
+    return false;
+}
+#define TFQ_IN(P, cond) ((cond) ? true : ::tfq::bounds_fail((P).status))
+#else
+#define TFQ_IN(P, cond) true
+#endif
+
+// [p, p + bytes) lies inside [lo, hi) of this CTA's shared memory.
+__device__ __forceinline__ bool in_smem(const uint8_t *smem, const void *p, int bytes, int lo, int hi) {
+    const long long off = reinterpret_cast<const uint8_t *>(p) - smem;
+    return off >= lo && off + bytes <= hi;
+}
+// The stage ring, and the activation (or zero-block) and partial-sum regions.
+__device__ __forceinline__ bool in_stages(const QmmParams &P, const uint8_t *smem, const void *p, int bytes) {
+    return in_smem(smem, p, bytes, P.st_off, P.st_off + P.stages * P.stage_bytes);
+}
+__device__ __forceinline__ bool in_b(const QmmParams &P, const uint8_t *smem, const void *p, int bytes) {
+    return in_smem(smem, p, bytes, P.x_off, P.sx_off) || in_smem(smem, p, bytes, P.z_off, P.z_off + ZERO_BYTES);
+}
+__device__ __forceinline__ bool in_sx(const QmmParams &P, const uint8_t *smem, const void *p, int bytes) {
+    return in_smem(smem, p, bytes, P.sx_off, P.pb_off) || in_smem(smem, p, bytes, P.z_off, P.z_off + ZERO_BYTES);
+}
+__device__ __forceinline__ bool in_pbuf(const QmmParams &P, const uint8_t *smem, const void *p, int bytes) {
+    return in_smem(smem, p, bytes, P.pb_off, P.z_off);
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -92,7 +126,7 @@ __device__ __forceinline__ void mbar_wait(uint64_t *bar, uint32_t parity, volati
             if (honor_abort && *abort) return;
             if (global_ns() - t0 > WAIT_LIMIT_NS) {
                 *abort = 1;
-                atomicOr(status, 1);
+                atomicOr(status, STATUS_WAIT);
                 return;
             }
         }
@@ -233,6 +267,7 @@ __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
             uint8_t *st = smem + P.st_off + slot * P.stage_bytes;
             uint8_t *sst = st + SEGS * ROWS * SEGP;
             uint8_t *bst = sst + ROWS * P.sbpitch;
+            if (!TFQ_IN(P, in_stages(P, smem, st, P.stage_bytes))) continue;
             // Test hook: the first stage is never sent, so its consumers' bounded
             // wait runs out (recorded in the status word) and the kernel completes.
             const bool withhold = P.stall && it == 0;
@@ -262,15 +297,22 @@ __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                 for (int e = lane; e < nrows * kw; e += 32) {
                     const int r = e / kw, wd = e - r * kw;
                     const int seg = wd / SEGW, sw = wd - seg * SEGW;
-                    reinterpret_cast<uint32_t *>(st + (seg * ROWS + r) * SEGP)[sw] =
-                        __ldg(P.W + (long long)(n0 + r) * row_words + (long long)k0 * BITS / 32 + wd);
+                    uint32_t *d = reinterpret_cast<uint32_t *>(st + (seg * ROWS + r) * SEGP) + sw;
+                    const long long src = (long long)(n0 + r) * row_words + (long long)k0 * BITS / 32 + wd;
+                    if (TFQ_IN(P, in_stages(P, smem, d, 4) && n0 + r < P.N && (long long)k0 * BITS / 32 + wd < row_words))
+                        *d = __ldg(P.W + src);
                 }
                 const int ng = (k1 - k0) / G;
                 for (int e = lane; e < nrows * ng; e += 32) {
                     const int r = e / ng, gg = e - r * ng;
                     const long long src = (long long)(n0 + r) * ngK + k0 / G + gg;
-                    reinterpret_cast<uint16_t *>(sst + r * P.sbpitch)[gg] = __ldg(P.s + src);
-                    reinterpret_cast<uint16_t *>(bst + r * P.sbpitch)[gg] = __ldg(P.b + src);
+                    uint16_t *ds = reinterpret_cast<uint16_t *>(sst + r * P.sbpitch) + gg;
+                    uint16_t *db = reinterpret_cast<uint16_t *>(bst + r * P.sbpitch) + gg;
+                    if (TFQ_IN(P, in_stages(P, smem, ds, 2) && in_stages(P, smem, db, 2) && n0 + r < P.N &&
+                                      k0 / G + gg < ngK)) {
+                        *ds = __ldg(P.s + src);
+                        *db = __ldg(P.b + src);
+                    }
                 }
                 __threadfence_block();
                 __syncwarp();
@@ -318,18 +360,23 @@ __device__ void load_x_groups(const QmmParams &P, const Item &I, uint4 *Bf, floa
     static_assert(RB >= 2, "layout rows");
     const int rows = P.rows;
     const int ngs = (I.k_hi - I.k_lo) / G;
+    [[maybe_unused]] const uint8_t *smem = reinterpret_cast<const uint8_t *>(Bf) - P.x_off;
     for (int u = tid; u < RB * ngs; u += nthr) {
         const int r = u / ngs, gs = u - r * ngs;
         float acc = 0.f;
-        const uint16_t *src = P.x + (long long)(r < rows ? P.xrow[r] : 0) * P.K + I.k_lo + gs * G;
+        const int xr = r < rows ? P.xrow[r] : 0;
+        const uint16_t *src = P.x + (long long)xr * P.K + I.k_lo + gs * G;
 #pragma unroll 4
         for (int t = 0; t < G / 8; ++t) {
             const int qq = (8 * t) / (G / 4), m = ((8 * t) % (G / 4)) / 8;
             const int run = gs * (G / 32) + m;
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (r < rows) v = *reinterpret_cast<const uint4 *>(src + 8 * t);
-            Bf[(run * RB + r) * 4 + qq] = make_uint4(prmt(v.x, v.z, 0x5410u), prmt(v.x, v.z, 0x7632u),
-                                                     prmt(v.y, v.w, 0x5410u), prmt(v.y, v.w, 0x7632u));
+            if (r < rows && TFQ_IN(P, xr >= 0 && xr < P.x_rows && I.k_lo + gs * G + 8 * t + 8 <= P.K))
+                v = *reinterpret_cast<const uint4 *>(src + 8 * t);
+            uint4 *d = Bf + (run * RB + r) * 4 + qq;
+            if (TFQ_IN(P, in_b(P, smem, d, 16)))
+                *d = make_uint4(prmt(v.x, v.z, 0x5410u), prmt(v.x, v.z, 0x7632u), prmt(v.y, v.w, 0x5410u),
+                                prmt(v.y, v.w, 0x7632u));
             acc += bf16f((uint16_t)(v.x & 0xFFFF));
             acc += bf16f((uint16_t)(v.x >> 16));
             acc += bf16f((uint16_t)(v.y & 0xFFFF));
@@ -339,7 +386,7 @@ __device__ void load_x_groups(const QmmParams &P, const Item &I, uint4 *Bf, floa
             acc += bf16f((uint16_t)(v.w & 0xFFFF));
             acc += bf16f((uint16_t)(v.w >> 16));
         }
-        sx[gs * RB + r] = acc;
+        if (TFQ_IN(P, in_sx(P, smem, sx + gs * RB + r, 4))) sx[gs * RB + r] = acc;
     }
 }
 
@@ -359,6 +406,7 @@ __device__ void load_x_pieces(const QmmParams &P, const Item &I, uint4 *Bf, floa
     static_assert(RB >= 2, "layout rows");
     constexpr int BATCH = 4;                         // loads a thread keeps in flight
     const int rows = P.rows;
+    [[maybe_unused]] const uint8_t *smem = reinterpret_cast<const uint8_t *>(Bf) - P.x_off;
     const int npc = (I.k_hi - I.k_lo) / 8;           // pieces of one row
     const int total = RB * npc;
     for (int u0 = tid; u0 < total; u0 += BATCH * nthr) {
@@ -368,16 +416,18 @@ __device__ void load_x_pieces(const QmmParams &P, const Item &I, uint4 *Bf, floa
             const int u = u0 + j * nthr;
             const int r = u / npc, pc = u - r * npc;
             v[j] = make_uint4(0u, 0u, 0u, 0u);
-            if (u < total && r < rows)
+            if (u < total && r < rows &&
+                TFQ_IN(P, P.xrow[r] >= 0 && P.xrow[r] < P.x_rows && I.k_lo + 8 * pc + 8 <= P.K))
                 v[j] = *reinterpret_cast<const uint4 *>(P.x + (long long)P.xrow[r] * P.K + I.k_lo + 8 * pc);
         }
 #pragma unroll
         for (int j = 0; j < BATCH; ++j) {
             const int u = u0 + j * nthr;
             const int r = u / npc, pc = u - r * npc;
-            if (u < total)
-                Bf[piece_slot<G, RB>(pc, r)] = make_uint4(prmt(v[j].x, v[j].z, 0x5410u), prmt(v[j].x, v[j].z, 0x7632u),
-                                                          prmt(v[j].y, v[j].w, 0x5410u), prmt(v[j].y, v[j].w, 0x7632u));
+            uint4 *d = Bf + piece_slot<G, RB>(pc, r);
+            if (u < total && TFQ_IN(P, in_b(P, smem, d, 16)))
+                *d = make_uint4(prmt(v[j].x, v[j].z, 0x5410u), prmt(v[j].x, v[j].z, 0x7632u),
+                                prmt(v[j].y, v[j].w, 0x5410u), prmt(v[j].y, v[j].w, 0x7632u));
         }
     }
     named_bar(bar, nthr);
@@ -389,7 +439,9 @@ __device__ void load_x_pieces(const QmmParams &P, const Item &I, uint4 *Bf, floa
 #pragma unroll
             for (int t = 0; t < G / 8; ++t) {
                 // Stored pairs (x0,x4) (x1,x5) (x2,x6) (x3,x7): add x0..x7 in order.
-                const uint4 w = Bf[piece_slot<G, RB>(gs * (G / 8) + t, r)];
+                const uint4 *pw = Bf + piece_slot<G, RB>(gs * (G / 8) + t, r);
+                uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                if (TFQ_IN(P, in_b(P, smem, pw, 16))) w = *pw;
                 acc += bf16f((uint16_t)(w.x & 0xFFFF));
                 acc += bf16f((uint16_t)(w.y & 0xFFFF));
                 acc += bf16f((uint16_t)(w.z & 0xFFFF));
@@ -400,7 +452,7 @@ __device__ void load_x_pieces(const QmmParams &P, const Item &I, uint4 *Bf, floa
                 acc += bf16f((uint16_t)(w.w >> 16));
             }
         }
-        sx[gs * RB + r] = acc;
+        if (TFQ_IN(P, in_sx(P, smem, sx + gs * RB + r, 4))) sx[gs * RB + r] = acc;
     }
 }
 
@@ -456,7 +508,8 @@ __device__ __forceinline__ float bias_term(float s, float b) {
 // entry of the group's first run (shared by the m-tiles); sxq: the group's
 // sum_group(x).
 template <int BITS, int G, int RB, int MT>
-__device__ __forceinline__ void group_body(const uint32_t *const (&pr)[G / 32], const uint32_t *const (&pr2)[G / 32],
+__device__ __forceinline__ void group_body(const QmmParams &P, const uint8_t *smem,
+                                           const uint32_t *const (&pr)[G / 32], const uint32_t *const (&pr2)[G / 32],
                                            const uint32_t (&ua)[G / 32], const uint32_t (&ub)[G / 32],
                                            uint32_t mg, uint32_t mq, int woff, const uint4 *bq, const float (&sg)[MT][2],
                                            const float (&bg)[MT][2], const float *sxq,
@@ -478,13 +531,16 @@ __device__ __forceinline__ void group_body(const uint32_t *const (&pr)[G / 32], 
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const uint32_t *src = pr[0] + woff + (t * 16 + 8 * h) * RW;
+                const bool ok = TFQ_IN(P, in_stages(P, smem, src, 4 * (VW > 0 ? VW : 1)));
 #pragma unroll
                 for (int v = 0; v < VW; v += (VW >= 4 ? 4 : 2)) {
                     if (VW >= 4) {
-                        const uint4 u = *reinterpret_cast<const uint4 *>(src + v);
+                        uint4 u = make_uint4(0u, 0u, 0u, 0u);
+                        if (ok) u = *reinterpret_cast<const uint4 *>(src + v);
                         vw[t][h][v] = u.x, vw[t][h][v + 1] = u.y, vw[t][h][v + 2] = u.z, vw[t][h][v + 3] = u.w;
                     } else {
-                        const uint2 u = *reinterpret_cast<const uint2 *>(src + v);
+                        uint2 u = make_uint2(0u, 0u);
+                        if (ok) u = *reinterpret_cast<const uint2 *>(src + v);
                         vw[t][h][v] = u.x, vw[t][h][v + 1] = u.y;
                     }
                 }
@@ -495,7 +551,11 @@ __device__ __forceinline__ void group_body(const uint32_t *const (&pr)[G / 32], 
     for (int m = 0; m < RUNS; ++m) {
         uint4 bb[NT];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) bb[nt] = bq[(m * LR + nt * 8) * 4];
+        for (int nt = 0; nt < NT; ++nt) {
+            const uint4 *pb = bq + (m * LR + nt * 8) * 4;
+            bb[nt] = make_uint4(0u, 0u, 0u, 0u);
+            if (TFQ_IN(P, in_b(P, smem, pb, 16))) bb[nt] = *pb;
+        }
 #pragma unroll
         for (int t = 0; t < MT; ++t) {
             // A registers in MMA operand order: a[2i] = pair i of row g, a[2i+1] of row g+8.
@@ -505,11 +565,20 @@ __device__ __forceinline__ void group_body(const uint32_t *const (&pr)[G / 32], 
                 Unpack<BITS>::template run<2, OFF>(&vw[t][1][m * BITS / 4], ua[m], ub[m], mg, mq, a + 1);
             } else if constexpr (BITS == 6) {
                 const int o0 = woff + (t * 16) * RW, o1 = woff + (t * 16 + 8) * RW;
-                Unpack<6>::template run_words<2, OFF>(pr[m][o0], pr2[m][o0], ua[m], ub[m], mg, mq, a);
-                Unpack<6>::template run_words<2, OFF>(pr[m][o1], pr2[m][o1], ua[m], ub[m], mg, mq, a + 1);
+                uint32_t w00 = 0u, w01 = 0u, w10 = 0u, w11 = 0u;
+                if (TFQ_IN(P, in_stages(P, smem, pr[m] + o0, 4) && in_stages(P, smem, pr2[m] + o0, 4) &&
+                                  in_stages(P, smem, pr[m] + o1, 4) && in_stages(P, smem, pr2[m] + o1, 4))) {
+                    w00 = pr[m][o0], w01 = pr2[m][o0], w10 = pr[m][o1], w11 = pr2[m][o1];
+                }
+                Unpack<6>::template run_words<2, OFF>(w00, w01, ua[m], ub[m], mg, mq, a);
+                Unpack<6>::template run_words<2, OFF>(w10, w11, ua[m], ub[m], mg, mq, a + 1);
             } else {
-                Unpack<BITS>::template run<2, OFF>(pr[m] + woff + (t * 16) * RW, ua[m], ub[m], mg, mq, a);
-                Unpack<BITS>::template run<2, OFF>(pr[m] + woff + (t * 16 + 8) * RW, ua[m], ub[m], mg, mq, a + 1);
+                // A run reads at most two words from its first.
+                const uint32_t *r0 = pr[m] + woff + (t * 16) * RW, *r1 = pr[m] + woff + (t * 16 + 8) * RW;
+                if (!TFQ_IN(P, in_stages(P, smem, r0, 8) && in_stages(P, smem, r1, 8)))
+                    r0 = r1 = reinterpret_cast<const uint32_t *>(smem + P.st_off);
+                Unpack<BITS>::template run<2, OFF>(r0, ua[m], ub[m], mg, mq, a);
+                Unpack<BITS>::template run<2, OFF>(r1, ua[m], ub[m], mg, mq, a + 1);
             }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
@@ -522,7 +591,8 @@ __device__ __forceinline__ void group_body(const uint32_t *const (&pr)[G / 32], 
         }
     }
     if (RB == 1) {   // a single activation row: only row 0 of the tile is live
-        const float x0 = *sxq;
+        float x0 = 0.f;
+        if (TFQ_IN(P, in_sx(P, smem, sxq, 4))) x0 = *sxq;
 #pragma unroll
         for (int t = 0; t < MT; ++t) {
             p[t][0][0] = fmaf(bg[t][0], x0, fmaf(sg[t][0], c[t][0][0], p[t][0][0]));
@@ -531,7 +601,8 @@ __device__ __forceinline__ void group_body(const uint32_t *const (&pr)[G / 32], 
     } else {   // the two activation rows of a lane in one packed fp32x2 FMA each
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            const float2 v = *reinterpret_cast<const float2 *>(sxq + nt * 8);
+            float2 v = make_float2(0.f, 0.f);
+            if (TFQ_IN(P, in_sx(P, smem, sxq + nt * 8, 8))) v = *reinterpret_cast<const float2 *>(sxq + nt * 8);
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
                 fma2(p[t][nt][0], p[t][nt][1], sg[t][0], sg[t][0], c[t][nt][0], c[t][nt][1]);
@@ -562,6 +633,7 @@ __device__ __forceinline__ void store_y(const QmmParams &P, int r, int n, float 
             v = u * u;
         }
         const long long at = (long long)P.yrow[r] * P.y_stride + d;
+        if (!TFQ_IN(P, P.yrow[r] >= 0 && P.yrow[r] < P.y_rows && d < P.y_stride)) return;
         if (P.out & OUT_BF16)
             reinterpret_cast<__nv_bfloat16 *>(P.y)[at] = __float2bfloat16_rn(v);
         else
@@ -716,8 +788,14 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                         for (int t = 0; t < MT; ++t)
 #pragma unroll
                             for (int h = 0; h < 2; ++h) {
-                                Sv[t][h].load(sp + (2 * t + h) * rstep + g0);
-                                Bv[t][h].load(bp + (2 * t + h) * rstep + g0);
+                                const uint16_t *ps = sp + (2 * t + h) * rstep + g0, *pb = bp + (2 * t + h) * rstep + g0;
+                                if (TFQ_IN(P, in_stages(P, smem, ps, 2 * NV) && in_stages(P, smem, pb, 2 * NV))) {
+                                    Sv[t][h].load(ps);
+                                    Bv[t][h].load(pb);
+                                } else {
+                                    Sv[t][h].load(reinterpret_cast<const uint16_t *>(smem + P.st_off));
+                                    Bv[t][h].load(reinterpret_cast<const uint16_t *>(smem + P.st_off));
+                                }
                             }
 #pragma unroll
                         for (int gv = 0; gv < NV; ++gv) {
@@ -730,8 +808,8 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                                     sg[t][h] = Sv[t][h].get(gv);
                                     bg[t][h] = bias_term<BITS>(sg[t][h], Bv[t][h].get(gv));
                                 }
-                            group_body<BITS, G, RB, MT>(pr, pr2, ua, ub, mg, mq, gl * GW, bq + gl * RUNS * LR * 4, sg,
-                                                        bg, sxq + gl * LR, p);
+                            group_body<BITS, G, RB, MT>(P, smem, pr, pr2, ua, ub, mg, mq, gl * GW,
+                                                        bq + gl * RUNS * LR * 4, sg, bg, sxq + gl * LR, p);
                         }
                     }
                 } else {
@@ -742,11 +820,13 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                         for (int t = 0; t < MT; ++t)
 #pragma unroll
                             for (int h = 0; h < 2; ++h) {
-                                sg[t][h] = bf16f(sp[(2 * t + h) * rstep + gl]);
-                                bg[t][h] = bias_term<BITS>(sg[t][h], bf16f(bp[(2 * t + h) * rstep + gl]));
+                                const uint16_t *ps = sp + (2 * t + h) * rstep + gl, *pb = bp + (2 * t + h) * rstep + gl;
+                                const bool ok = TFQ_IN(P, in_stages(P, smem, ps, 2) && in_stages(P, smem, pb, 2));
+                                sg[t][h] = ok ? bf16f(*ps) : 0.f;
+                                bg[t][h] = bias_term<BITS>(sg[t][h], ok ? bf16f(*pb) : 0.f);
                             }
-                        group_body<BITS, G, RB, MT>(pr, pr2, ua, ub, mg, mq, gl * GW, bq + gl * RUNS * LR * 4, sg, bg,
-                                                    sxq + gl * LR, p);
+                        group_body<BITS, G, RB, MT>(P, smem, pr, pr2, ua, ub, mg, mq, gl * GW,
+                                                    bq + gl * RUNS * LR * 4, sg, bg, sxq + gl * LR, p);
                     }
                 }
             }
@@ -770,7 +850,7 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                     for (int h = 0; h < 2; ++h) {
                         const int r = nt * 8 + 2 * q;
                         const int c = t * 16 + g + 8 * h;
-                        if (r < LR)
+                        if (r < LR && TFQ_IN(P, in_pbuf(P, smem, pw + c * LR + r, 8)))
                             *reinterpret_cast<float2 *>(pw + c * LR + r) = make_float2(p[t][nt][2 * h], p[t][nt][2 * h + 1]);
                     }
             named_bar(gbar, GT);
@@ -793,7 +873,8 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                     // flight together), then added in segment order.
                     float v[SEGS];
 #pragma unroll
-                    for (int j = 0; j < SEGS; ++j) v[j] = j < nseg ? pf[j * ROWS * LR] : 0.f;
+                    for (int j = 0; j < SEGS; ++j)
+                        v[j] = j < nseg && TFQ_IN(P, in_pbuf(P, smem, pf + j * ROWS * LR, 4)) ? pf[j * ROWS * LR] : 0.f;
                     float C = v[0];
 #pragma unroll
                     for (int j = 1; j < SEGS; ++j)
@@ -802,7 +883,8 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                         yacc[i] = chunk == 0 ? C : yacc[i] + C;
                         if (k0 + CHUNK >= I.k_hi) store_y(P, fr, n0 + fc, yacc[i]);
                     } else if (fr < rows && n0 + fc < P.N) {
-                        P.ws[((long long)chunk * rows + fr) * P.N + n0 + fc] = C;
+                        const long long at = ((long long)chunk * rows + fr) * P.N + n0 + fc;
+                        if (TFQ_IN(P, at < P.ws_elems)) P.ws[at] = C;
                     }
                 }
             }
@@ -827,14 +909,17 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
             const int nb = min(GT, nmine - b0);
             if (gtid < nb) {
                 const int mt = mt0 + (b0 + gtid) * team;
-                const int lst = atomicAdd(&P.counters[mt], 1) == P.nsl - 1;
-                if (lst) P.counters[mt] = 0;                // no other arrival in this launch
-                last[gtid] = lst;
+                int lst = 0;
+                if (TFQ_IN(P, mt < P.n_counters)) {
+                    lst = atomicAdd(&P.counters[mt], 1) == P.nsl - 1;
+                    if (lst) P.counters[mt] = 0;            // no other arrival in this launch
+                }
+                if (TFQ_IN(P, in_pbuf(P, smem, last + gtid, 4))) last[gtid] = lst;
             }
             named_bar(gbar, GT);
             __threadfence();
             for (int j = 0; j < nb; ++j) {
-                if (!last[j]) continue;                      // the same for the whole group
+                if (!TFQ_IN(P, in_pbuf(P, smem, last + j, 4)) || !last[j]) continue;   // the same for the whole group
                 const int n0 = (mt0 + (b0 + j) * team) * ROWS;
 #pragma unroll
                 for (int i = 0; i < OUTS; ++i) {
@@ -843,9 +928,12 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                         const int fc = o / LR, fr = o - (o / LR) * LR;
                         if (fr < rows && n0 + fc < P.N) {
                             const long long n = n0 + fc;
-                            float v = __ldcg(P.ws + (long long)fr * P.N + n);
-                            for (int ch = 1; ch < P.nchunks; ++ch)
-                                v = v + __ldcg(P.ws + ((long long)ch * rows + fr) * P.N + n);
+                            float v = 0.f;
+                            if (TFQ_IN(P, (long long)fr * P.N + n < P.ws_elems)) v = __ldcg(P.ws + (long long)fr * P.N + n);
+                            for (int ch = 1; ch < P.nchunks; ++ch) {
+                                const long long at = ((long long)ch * rows + fr) * P.N + n;
+                                if (TFQ_IN(P, at < P.ws_elems)) v = v + __ldcg(P.ws + at);
+                            }
                             store_y(P, fr, (int)n, v);
                         }
                     }

@@ -31,6 +31,19 @@ def test_exports_every_declared_symbol(tf):
         getattr(tf.lib(), name)
 
 
+def test_debug_build_exports(tf):
+    # The bounds-checking build exports every entry point of both headers.
+    names = set()
+    for h in ("tfqmm.h", "tfqmm_debug.h"):
+        names |= set(re.findall(r"^(?:int|const char \*)\s*(tf_\w+)\s*\(",
+                                open(os.path.join(ROOT, "include", h)).read(), re.M))
+    assert "tf_debug_shrink_y" in names
+    out = subprocess.check_output(["nm", "-D", "--defined-only", tf.SO_DEBUG]).decode()
+    exported = set(re.findall(r"\sT\s(tf_\w+)$", out, re.M))
+    assert names <= exported, names - exported
+    assert tf.debug_lib().tf_debug_shrink_y(17) == -3
+
+
 A = 4096  # a 16-byte aligned stand-in address; no call below reaches the device
 
 
