@@ -384,12 +384,14 @@ def item_launches(it) -> int:
     return it.get("launches", len(it["reps"][0]) if it.get("stack") else 1)
 
 
-def time_item(tf, it, stream, warmup, replays=7):
-    """Per-call device time (us): a CUDA graph of one call on every weight copy
-    (>= 4 L2 sizes of weights), replayed `replays` times, each replay timed with
-    CUDA events on the replay stream; the median over replays of time / calls."""
+def time_item(tf, it, stream, warmup, replays=7, min_calls=8):
+    """Per-call device time (us): a CUDA graph of calls cycling over every weight
+    copy (>= 4 L2 sizes of weights, and at least `min_calls` calls so that the
+    graph's own start is spread thin), replayed `replays` times, each replay
+    timed with CUDA events on the replay stream; the median over replays of
+    time / calls."""
     import torch
-    n = len(it["reps"])
+    n = max(len(it["reps"]), min_calls)
     with torch.cuda.stream(stream):
         for w in range(max(1, warmup)):
             launch_item(tf, it, w, stream)
@@ -682,7 +684,8 @@ def run_gpu(args, cases):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": sum(item_launches(it) for it in items) * args.steps,
             "timing": "exactly %d steps: a CUDA graph of %d steps replayed %d times%s; per-case time: the median "
-                      "over 7 replays of a graph of one call per weight copy (>= 4 L2 sizes of weights)"
+                      "over 7 replays of a graph of calls cycling over the weight copies (>= 4 L2 sizes of "
+                      "weights, >= 8 calls)"
                       % (args.steps, min(copies, args.steps), n_full,
                          " plus one of %d steps" % rem if rem else ""),
             "kernel_source_sha": kernel_source_sha(),
