@@ -178,6 +178,31 @@ int tf_qmm_ex(const uint16_t *x, int rows, int K,
               void *y, int64_t y_stride, int flags, void *stream);
 
 /*
+ * tf_qmm_prompt -- the product for many activation rows (a prompt), with the
+ * weights read once per 64-row window (PR #788, the 2-bit affine_mm commit: the
+ * prompt-side tiled product, checked row by row against windows of 1 to 65 rows).
+ *   Same arguments, layouts and output options (flags as tf_qmm_ex) as tf_qmm_ex,
+ *   rows 1..65536; K must be a multiple of 2048 (TF_EINVAL_SIZE otherwise) and
+ *   scales / biases 16-byte aligned (TF_EINVAL_PTR).
+ *   The group dot products run on the tcgen05 tensor cores (M = 128 output
+ *   columns, N = 64 rows, accumulators in tensor memory), so this entry point has
+ *   its own canonical order: per output, p = fma(scale, T, p); p = fma(bias',
+ *   sum_group(x), p) over the groups of each 2048-k chunk from 0 (T the tensor-core
+ *   group dot product; bias' = bias - 128 scale for 4-6-bit codes, which enter as
+ *   128 + c), y = C_0 + C_1 + ... over the chunks in order.  Every row's result is
+ *   the same bit for bit in any window of any size and position of this entry
+ *   point, and within the tolerance of tf_qmm; it is not bit-identical to
+ *   tf_qmm's (whose segment order and MMA instruction differ).
+ *   Allocates a per-(device, stream) workspace for the permuted activations and
+ *   their group sums (rows * K * 2 + (K / group) * ceil(rows / 64) * 256 bytes,
+ *   grown on demand).  Plain launches: one prepass and one launch per 64 rows.
+ */
+int tf_qmm_prompt(const uint16_t *x, int rows, int K,
+                  const uint32_t *W, const uint16_t *scales, const uint16_t *biases,
+                  int N, int bits, int group,
+                  void *y, int64_t y_stride, int flags, void *stream);
+
+/*
  * tf_qmm_gather -- indexed slots over a set of expert matrices (PR #788,
  * row-kernel commit: indexed slots in the bit-exact window gate; tf-affine-ref
  * commit: a one-expert gather equals the dense product).

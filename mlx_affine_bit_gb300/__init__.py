@@ -25,7 +25,7 @@ STATUS = {
     -9: "TF_ESTACK", -10: "TF_ECUDA", -11: "TF_EDEVICE", -12: "TF_EINVAL_FLAGS", -13: "TF_EGATHER",
     -14: "TF_EBOUNDS",
 }
-SYMBOLS = ("tf_qmm", "tf_qmm_ex", "tf_qmm_gather", "tf_qmm_noalloc", "tf_noalloc_status", "tf_qmm_stack", "tf_widen",
+SYMBOLS = ("tf_qmm", "tf_qmm_ex", "tf_qmm_prompt", "tf_qmm_gather", "tf_qmm_noalloc", "tf_noalloc_status", "tf_qmm_stack", "tf_widen",
            "tf_widen_host", "tf_common_width", "tf_qmm_bytes", "tf_device_status", "tf_set_launch_mode",
            "tf_inject_stall", "tf_last_error_string", "tf_version")
 TF_LAUNCH_PDL, TF_LAUNCH_EARLY_WEIGHTS, TF_LAUNCH_EARLY_X = 1, 2, 4
@@ -79,6 +79,7 @@ def _load(path):
     L.tf_qmm.argtypes = [P, i32, i32, P, P, P, i32, i32, i32, P, i64, P]
     L.tf_qmm_noalloc.argtypes = [P, i32, i32, P, P, P, i32, i32, i32, P, i64, P]
     L.tf_qmm_ex.argtypes = [P, i32, i32, P, P, P, i32, i32, i32, P, i64, i32, P]
+    L.tf_qmm_prompt.argtypes = [P, i32, i32, P, P, P, i32, i32, i32, P, i64, i32, P]
     L.tf_qmm_gather.argtypes = [P, i32, i32, ctypes.POINTER(TfRun), i32, ctypes.POINTER(ctypes.c_int),
                                 ctypes.POINTER(ctypes.c_int), i32, P, i64, i32, P]
     L.tf_qmm_stack.argtypes = [P, i32, i32, ctypes.POINTER(TfRun), i32,
@@ -93,7 +94,7 @@ def _load(path):
     L.tf_inject_stall.argtypes = []
     L.tf_last_error_string.restype = ctypes.c_char_p
     L.tf_version.restype = ctypes.c_char_p
-    for name in ("tf_qmm", "tf_qmm_ex", "tf_qmm_gather", "tf_qmm_noalloc", "tf_qmm_stack", "tf_widen",
+    for name in ("tf_qmm", "tf_qmm_ex", "tf_qmm_prompt", "tf_qmm_gather", "tf_qmm_noalloc", "tf_qmm_stack", "tf_widen",
                  "tf_widen_host", "tf_common_width", "tf_qmm_bytes", "tf_device_status", "tf_noalloc_status",
                  "tf_set_launch_mode", "tf_inject_stall"):
         getattr(L, name).restype = i32
@@ -137,6 +138,12 @@ def tf_qmm_ex(x, rows, K, W, scales, biases, N, bits, group, y, y_stride, flags,
     """tf_qmm with output flags (TF_OUT_BF16: y is bf16; TF_EPI_RELU2: squared ReLU)."""
     _check(lib().tf_qmm_ex(_ptr(x), rows, K, _ptr(W), _ptr(scales), _ptr(biases), N, bits, group,
                            _ptr(y), y_stride, flags, _stream(stream)))
+
+
+def tf_qmm_prompt(x, rows, K, W, scales, biases, N, bits, group, y, y_stride, flags=0, stream=None) -> None:
+    """Many-row product on the tcgen05 tensor cores, weights read once per 64 rows (see include/tfqmm.h)."""
+    _check(lib().tf_qmm_prompt(_ptr(x), rows, K, _ptr(W), _ptr(scales), _ptr(biases), N, bits, group,
+                               _ptr(y), y_stride, flags, _stream(stream)))
 
 
 def tf_qmm_gather(x, x_rows, K, experts, slot_expert, slot_row, y, y_stride, flags=0, stream=None) -> None:

@@ -618,6 +618,49 @@ int tfq::product_with_scratch(const uint16_t *x, int rows, int K, const uint32_t
 
 int tfq::fail_message(int code, const char *msg) { return fail(code, msg); }
 
+int tfq::cuda_error(cudaError_t e, const char *where) { return cuda_fail(e, where); }
+
+int tfq::check_product(const uint16_t *x, int rows, int K, const uint32_t *W, const uint16_t *s,
+                       const uint16_t *b, int N, int bits, int group, const float *y, int64_t y_stride) {
+    g_err.clear();
+    int rc = check_matrix(K, W, s, b, N, bits, group);
+    if (rc) return rc;
+    rc = check_io(x, rows, y, MAX_ROWS);
+    if (rc) return rc;
+    if (y_stride < N) return fail(TF_EINVAL_STRIDE, "y_stride below N is refused");
+    return TF_OK;
+}
+
+int tfq::tensor_map_2d(CUtensorMap *m, const void *base, int elem_bytes, long long cols, long long rows,
+                       int box_cols, int box_rows) {
+    const int rc = get_encoder();
+    if (rc) return rc;
+    const CUtensorMapDataType t = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
+                                  : elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32
+                                                    : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    return encode_2d(m, base, t, elem_bytes, cols, rows, box_cols, box_rows);
+}
+
+int tfq::tensor_map_3d(CUtensorMap *m, const void *base, int elem_bytes, long long d0, long long d1, long long d2,
+                       long long s1, long long s2, int b0, int b1, int b2) {
+    const int rc = get_encoder();
+    if (rc) return rc;
+    const CUtensorMapDataType t = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
+                                  : elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32
+                                                    : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    return encode_3d(m, base, t, d0, d1, d2, s1, s2, b0, b1, b2);
+}
+
+int tfq::device_info(int *nsm, int **status) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevState *d = nullptr;
+    const int rc = dev_state(&d);
+    if (rc) return rc;
+    *nsm = d->nsm;
+    *status = d->status;
+    return TF_OK;
+}
+
 // ============================================================== C ABI ====
 
 // A product of any row count: up to 16 rows in one launch; more as 16-row
