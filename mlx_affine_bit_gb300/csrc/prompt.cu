@@ -18,29 +18,36 @@ using namespace tfq;
 
 namespace {
 
-// x [rows][K] bf16 -> xp [rows][K] with every 8 values in the codes' pair order
-// (x0, x4, x1, x5, x2, x6, x3, x7), and sx [K/G][R64] fp32, the sequential sum of
-// each group's x in k order from 0 (rows past `rows` hold 0).  One thread per
-// (group, row).
-__global__ void prompt_prep(const uint16_t *x, int rows, int K, int G, int R64, uint16_t *xp, float *sx) {
+// x [rows][K] bf16 -> xt, the operand tiles of the prompt kernel: for each
+// 64-row window and 128-k stage, [16 k blocks][64 rows][8 values] (one
+// contiguous 16 KB block, copied with one bulk copy), every 8 values in the
+// codes' pair order (x0, x4, x1, x5, x2, x6, x3, x7) and rows past `rows` zero;
+// and sx [K/G][R64] fp32, the sequential sum of each group's x in k order from 0
+// (0 past `rows`).  One thread per (group, row).
+__global__ void prompt_prep(const uint16_t *x, int rows, int K, int G, int R64, uint16_t *xt, float *sx) {
     const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
     const int ng = K / G;
     if (t >= (long long)ng * R64) return;
     const int g = (int)(t / R64), r = (int)(t - (long long)g * R64);
+    const int nst = K / prompt::PSTAGE, win = r / prompt::PN, wr = r % prompt::PN;
     float acc = 0.f;
-    if (r < rows) {
-        const uint16_t *src = x + (long long)r * K + (long long)g * G;
-        uint16_t *dst = xp + (long long)r * K + (long long)g * G;
-        for (int j = 0; j < G / 8; ++j) {
-            const uint4 v = reinterpret_cast<const uint4 *>(src)[j];
-            reinterpret_cast<uint4 *>(dst)[j] = make_uint4(prmt(v.x, v.z, 0x5410u), prmt(v.x, v.z, 0x7632u),
-                                                           prmt(v.y, v.w, 0x5410u), prmt(v.y, v.w, 0x7632u));
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const uint16_t *src = x + (long long)r * K + (long long)g * G;
+    for (int j = 0; j < G / 8; ++j) {
+        const int k = g * G + 8 * j;
+        const long long blk = ((long long)win * nst + k / prompt::PSTAGE) * (prompt::PSTAGE / 8) + (k % prompt::PSTAGE) / 8;
+        uint4 *dst = reinterpret_cast<uint4 *>(xt + (blk * prompt::PN + wr) * 8);
+        if (r >= rows) {
+            *dst = make_uint4(0u, 0u, 0u, 0u);
+            continue;
+        }
+        const uint4 v = reinterpret_cast<const uint4 *>(src)[j];
+        *dst = make_uint4(prmt(v.x, v.z, 0x5410u), prmt(v.x, v.z, 0x7632u), prmt(v.y, v.w, 0x5410u),
+                          prmt(v.y, v.w, 0x7632u));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc += __uint_as_float(w[i] << 16);
-                acc += __uint_as_float(w[i] & 0xFFFF0000u);
-            }
+        for (int i = 0; i < 4; ++i) {
+            acc += __uint_as_float(w[i] << 16);
+            acc += __uint_as_float(w[i] & 0xFFFF0000u);
         }
     }
     sx[t] = acc;
@@ -130,9 +137,10 @@ extern "C" int tf_qmm_prompt(const uint16_t *x, int rows, int K, const uint32_t 
     int nsm = 0, *status = nullptr;
     rc = device_info(&nsm, &status);
     if (rc) return rc;
-    // Workspace: permuted x [rows][K] bf16, then the group sums [K/G][R64] fp32.
+    // Workspace: x operand tiles [R64 / 64 windows][K / 128 stages][16 KB], then the
+    // group sums [K/G][R64] fp32.
     const int R64 = (rows + prompt::PN - 1) / prompt::PN * prompt::PN;
-    const size_t xp_bytes = ((size_t)rows * K * 2 + 255) & ~(size_t)255;
+    const size_t xp_bytes = (size_t)R64 * K * 2;
     const size_t sx_bytes = (size_t)(K / group) * R64 * 4;
     void *ws = nullptr;
     rc = workspace(st, xp_bytes + sx_bytes, &ws);
@@ -149,8 +157,7 @@ extern "C" int tf_qmm_prompt(const uint16_t *x, int rows, int K, const uint32_t 
     const int sw = prompt::PSTAGE * bits / 32;                  // words of one stage row
     rc = tensor_map_3d(&P.tmW, W, 4, sw, N, K / prompt::PSTAGE, rowb, (long long)sw * 4,
                        sw + prompt::code_pad_words(bits), prompt::PM, 1);
-    if (!rc)
-        rc = tensor_map_3d(&P.tmX, xp, 2, 8, rows, K / 8, (long long)K * 2, 16, 8, prompt::PN, prompt::PSTAGE / 8);
+    P.xt = xp;
     if (!rc) {
         const int gps = prompt::PSTAGE / group >= 1 ? prompt::PSTAGE / group : 1;
         rc = tensor_map_2d(&P.tmSX, sx, 4, R64, K / group, prompt::PN, gps);

@@ -32,14 +32,18 @@ constexpr int PN = 64;                  // activation rows per window (MMA N)
 constexpr int PSTAGE = 128;             // k per pipeline stage
 constexpr int PIECE = 32;               // k per unpacked piece (two K = 16 MMAs)
 constexpr int NPIECE = PSTAGE / PIECE;  // pieces per stage
-constexpr int STAGES = 3;               // stage ring depth
-constexpr int MATH_WARPS = 4;
-constexpr int THREADS = (MATH_WARPS + 2) * 32;   // math warps, producer warp, MMA warp
-constexpr int PRODUCER = MATH_WARPS, MMA_WARP = MATH_WARPS + 1;
+constexpr int STAGES = 3;               // stage ring depth (codes and x)
+constexpr int SXR = 8;                  // ring depth of the per-group sums of x (one slot a stage)
+constexpr int ABUF = 4;                 // unpacked pieces in flight
+constexpr int DBUF = 4;                 // group accumulators in flight (tensor memory)
+constexpr int UNPACK_WARPS = 4;         // one column per thread
+constexpr int EPI_WARPS = 8;            // two per tensor-memory lane quarter: rows 0-31 and 32-63
+constexpr int PRODUCER = UNPACK_WARPS + EPI_WARPS, MMA_WARP = PRODUCER + 1;
+constexpr int THREADS = (MMA_WARP + 1) * 32;
 constexpr int A_BYTES = PM * PIECE * 2;          // one unpacked piece (bf16)
 constexpr int X_BYTES = PN * PSTAGE * 2;         // one stage of x (bf16)
 constexpr int SX_BYTES = 1024;                   // per-group sums of x of one stage (<= 4 groups x 64 rows)
-constexpr int TMEM_COLS = 2 * PN;                // two accumulator buffers
+constexpr int TMEM_COLS = DBUF * PN;             // accumulator buffers
 
 // Pad words after each stage row of codes: the TMA box row is a multiple of 16
 // bytes and row pitches of an odd number of 16-byte units keep the math warps'
@@ -50,25 +54,26 @@ __host__ __device__ constexpr int code_pitch(int bits) { return (PSTAGE * bits /
 __host__ __device__ constexpr int sb_pitch(int group) { return (CHUNK / group + 8) * 2; }
 
 struct Layout {
-    int w_off, x_off, sx_off, stage_bytes, sb_off, sb_bytes, a_off, smem;
+    int w_off, x_off, stage_bytes, sx_off, sb_off, sb_bytes, a_off, smem;
 };
 __host__ __device__ inline Layout layout(int bits, int group) {
     Layout L;
     const int wbytes = (PM * code_pitch(bits) + 1023) & ~1023;
     L.w_off = 0;
     L.x_off = wbytes;
-    L.sx_off = wbytes + X_BYTES;
-    L.stage_bytes = wbytes + X_BYTES + SX_BYTES;
+    L.stage_bytes = wbytes + X_BYTES;
     L.sb_bytes = (PM * sb_pitch(group) + 1023) & ~1023;   // scales (or biases) of one chunk
     const int base = 1024;                                // header: barriers, TMEM address, flags
-    L.sb_off = base + STAGES * L.stage_bytes;
+    L.sx_off = base + STAGES * L.stage_bytes;             // SXR slots of SX_BYTES
+    L.sb_off = L.sx_off + SXR * SX_BYTES;
     L.a_off = L.sb_off + 4 * L.sb_bytes;                  // two slots x (scales, biases)
-    L.smem = L.a_off + 2 * A_BYTES;
+    L.smem = L.a_off + ABUF * A_BYTES;
     return L;
 }
 
 struct Params {
-    CUtensorMap tmW, tmX, tmSX, tmS, tmB;
+    CUtensorMap tmW, tmSX, tmS, tmB;
+    const uint16_t *xt;    // x operand tiles: [window][stage][16 k blocks][64 rows][8] bf16
     float *y;
     long long y_stride;
     int *status;
@@ -94,6 +99,14 @@ __device__ __forceinline__ void mma_issue(uint32_t d_tmem, uint64_t ad, uint64_t
         "l"(ad), "l"(bd), "r"(IDESC), "r"((uint32_t)acc)
         : "memory");
 }
+// One contiguous global -> shared copy completing on an mbarrier (16-byte
+// aligned addresses, a multiple of 16 bytes).
+__device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
@@ -116,18 +129,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 // Barriers of the header, in order.
 struct Bars {
     uint64_t st_full[STAGES], st_empty[STAGES];
+    uint64_t sx_full[SXR], sx_empty[SXR];
     uint64_t sb_full[2], sb_empty[2];
-    uint64_t a_full[2], a_empty[2];
-    uint64_t d_full[2], d_empty[2];
+    uint64_t a_full[ABUF], a_empty[ABUF];
+    uint64_t d_full[DBUF], d_empty[DBUF];
     uint64_t mma_done;
     uint32_t tmem;
     int abort;
 };
 
 template <int BITS, int G>
-__global__ void __maxnreg__(232) prompt_kernel(const __grid_constant__ Params P) {
+__global__ void __maxnreg__(128) prompt_kernel(const __grid_constant__ Params P) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    constexpr int GPS = PSTAGE / G >= 1 ? PSTAGE / G : 1;     // groups per stage (G <= 128)
     constexpr int SBP = sb_pitch(G) / 2;                     // scale/bias row pitch (bf16 values)
     constexpr int CP = code_pitch(BITS) / 4;                 // code row pitch (words)
     constexpr bool OFF = offset_codes(BITS);
@@ -135,20 +148,29 @@ __global__ void __maxnreg__(232) prompt_kernel(const __grid_constant__ Params P)
     Bars &B = *reinterpret_cast<Bars *>(smem);
     volatile int *abort = &B.abort;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nstage_chunk = CHUNK / PSTAGE;
+    constexpr int SPC = CHUNK / PSTAGE;                      // stages per chunk
+    auto stage_ptr = [&](uint32_t slot) { return smem + 1024 + slot * L.stage_bytes; };
 
     if (tid == 0) {
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(&B.st_full[i], 1);
-            mbar_init(&B.st_empty[i], MATH_WARPS + 1);
+            mbar_init(&B.st_empty[i], UNPACK_WARPS + 1);
+        }
+        for (int i = 0; i < SXR; ++i) {
+            mbar_init(&B.sx_full[i], 1);
+            mbar_init(&B.sx_empty[i], EPI_WARPS);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&B.sb_full[i], 1);
-            mbar_init(&B.sb_empty[i], MATH_WARPS);
-            mbar_init(&B.a_full[i], MATH_WARPS);
+            mbar_init(&B.sb_empty[i], EPI_WARPS);
+        }
+        for (int i = 0; i < ABUF; ++i) {
+            mbar_init(&B.a_full[i], UNPACK_WARPS);
             mbar_init(&B.a_empty[i], 1);
+        }
+        for (int i = 0; i < DBUF; ++i) {
             mbar_init(&B.d_full[i], 1);
-            mbar_init(&B.d_empty[i], MATH_WARPS);
+            mbar_init(&B.d_empty[i], EPI_WARPS);
         }
         mbar_init(&B.mma_done, 1);
         B.abort = 0;
@@ -167,7 +189,7 @@ __global__ void __maxnreg__(232) prompt_kernel(const __grid_constant__ Params P)
     if (warp == PRODUCER) {
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(&P.tmW) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(&P.tmX) : "memory");
+            const uint16_t *xw = P.xt + (long long)(P.r0 / PN) * (P.K / PSTAGE) * (X_BYTES / 2);
             uint32_t sit = 0, cit = 0;
             for (int tile = blockIdx.x; tile < P.ntiles && !*abort; tile += gridDim.x) {
                 const int n0 = tile * PM;
@@ -177,28 +199,35 @@ __global__ void __maxnreg__(232) prompt_kernel(const __grid_constant__ Params P)
                     mbar_arrive_tx(&B.sb_full[cs], 2u * PM * sb_pitch(G));
                     tma_3d(smem + L.sb_off + (2 * cs) * L.sb_bytes, &P.tmS, 0, c, n0, &B.sb_full[cs]);
                     tma_3d(smem + L.sb_off + (2 * cs + 1) * L.sb_bytes, &P.tmB, 0, c, n0, &B.sb_full[cs]);
-                    for (int st = 0; st < nstage_chunk && !*abort; ++st, ++sit) {
-                        const int slot = (int)(sit % STAGES);
+                    for (int st = 0; st < SPC && !*abort; ++st, ++sit) {
+                        const uint32_t slot = sit % STAGES;
                         const int k0 = c * CHUNK + st * PSTAGE;
+                        const uint32_t xslot = sit % SXR;
+                        constexpr int GPS = PSTAGE / G >= 1 ? PSTAGE / G : 1;
+                        mbar_wait(&B.sx_empty[xslot], ((sit / SXR) & 1) ^ 1, abort, P.status);
+                        mbar_arrive_tx(&B.sx_full[xslot], (uint32_t)(GPS * PN * 4));
+                        tma_2d(smem + L.sx_off + xslot * SX_BYTES, &P.tmSX, P.r0, k0 / G, &B.sx_full[xslot]);
                         mbar_wait(&B.st_empty[slot], ((sit / STAGES) & 1) ^ 1, abort, P.status);
-                        uint8_t *sp = smem + 1024 + slot * L.stage_bytes;
-                        mbar_arrive_tx(&B.st_full[slot],
-                                       (uint32_t)(PM * code_pitch(BITS) + X_BYTES + GPS * PN * 4));
+                        uint8_t *sp = stage_ptr(slot);
+                        mbar_arrive_tx(&B.st_full[slot], (uint32_t)(PM * code_pitch(BITS) + X_BYTES));
                         tma_3d(sp + L.w_off, &P.tmW, 0, n0, k0 / PSTAGE, &B.st_full[slot]);
-                        tma_3d(sp + L.x_off, &P.tmX, 0, P.r0, k0 / 8, &B.st_full[slot]);
-                        tma_2d(sp + L.sx_off, &P.tmSX, P.r0, k0 / G, &B.st_full[slot]);
+                        bulk_copy(sp + L.x_off, xw + (long long)(k0 / PSTAGE) * (X_BYTES / 2), X_BYTES,
+                                  &B.st_full[slot]);
                     }
                 }
             }
-            // Drain: every issued stage has landed before the CTA may exit (the
-            // ring's last fills; an aborted launch waits only boundedly).
+            // Drain: every issued copy has landed before the CTA may exit.
             for (uint32_t j = 0; j < (sit < (uint32_t)STAGES ? sit : (uint32_t)STAGES); ++j) {
-                const uint32_t s = sit - 1 - j;
-                mbar_wait(&B.st_full[s % STAGES], (s / STAGES) & 1, abort, P.status, false);
+                const uint32_t q = sit - 1 - j;
+                mbar_wait(&B.st_full[q % STAGES], (q / STAGES) & 1, abort, P.status, false);
             }
             for (uint32_t j = 0; j < (cit < 2u ? cit : 2u); ++j) {
-                const uint32_t s = cit - 1 - j;
-                mbar_wait(&B.sb_full[s & 1], (s >> 1) & 1, abort, P.status, false);
+                const uint32_t q = cit - 1 - j;
+                mbar_wait(&B.sb_full[q & 1], (q >> 1) & 1, abort, P.status, false);
+            }
+            for (uint32_t j = 0; j < (sit < (uint32_t)SXR ? sit : (uint32_t)SXR); ++j) {
+                const uint32_t q = sit - 1 - j;
+                mbar_wait(&B.sx_full[q % SXR], (q / SXR) & 1, abort, P.status, false);
             }
         }
     } else if (warp == MMA_WARP) {
@@ -206,20 +235,19 @@ __global__ void __maxnreg__(232) prompt_kernel(const __grid_constant__ Params P)
             uint32_t sit = 0, pit = 0, git = 0;
             for (int tile = blockIdx.x; tile < P.ntiles && !*abort; tile += gridDim.x) {
                 for (int c = 0; c < P.nchunks && !*abort; ++c) {
-                    for (int st = 0; st < nstage_chunk && !*abort; ++st, ++sit) {
-                        const int slot = (int)(sit % STAGES);
+                    for (int st = 0; st < SPC && !*abort; ++st, ++sit) {
+                        const uint32_t slot = sit % STAGES;
                         mbar_wait(&B.st_full[slot], (sit / STAGES) & 1, abort, P.status);
-                        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                        const uint32_t xs = smem_u32(smem + 1024 + slot * L.stage_bytes + L.x_off);
+                        const uint32_t xs = smem_u32(stage_ptr(slot) + L.x_off);
                         for (int pc = 0; pc < NPIECE; ++pc, ++pit) {
                             const int kp = st * PSTAGE + pc * PIECE;            // piece's k within the chunk
                             const bool first = kp % G == 0, last = (kp + PIECE) % G == 0;
-                            const int a = (int)(pit & 1), d = (int)(git & 1);
-                            mbar_wait(&B.a_full[a], (pit >> 1) & 1, abort, P.status);
-                            if (first) mbar_wait(&B.d_empty[d], ((git >> 1) & 1) ^ 1, abort, P.status);
+                            const uint32_t a = pit % ABUF, d = git % DBUF;
+                            mbar_wait(&B.a_full[a], (pit / ABUF) & 1, abort, P.status);
+                            if (first) mbar_wait(&B.d_empty[d], ((git / DBUF) & 1) ^ 1, abort, P.status);
                             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                             const uint32_t as = smem_u32(smem + L.a_off + a * A_BYTES);
-                            const uint32_t dt = tmem + (uint32_t)(d * PN);
+                            const uint32_t dt = tmem + d * PN;
                             // A piece: [16 column blocks][4 k blocks][8][16 B]; x stage:
                             // [16 k blocks][64 rows][16 B].
                             mma_issue(dt, smem_desc(as, 128, 512), smem_desc(xs + (pc * 4) * 1024, 1024, 128), !first);
@@ -238,8 +266,8 @@ __global__ void __maxnreg__(232) prompt_kernel(const __grid_constant__ Params P)
             mma_commit(&B.mma_done);
             mbar_wait(&B.mma_done, 0, abort, P.status, false);
         }
-    } else {
-        // Math warps: thread m owns output column n0 + m (tensor-memory lane m).
+    } else if (warp < UNPACK_WARPS) {
+        // Unpack warps: thread m unpacks output column n0 + m into the A pieces.
         const int m = tid;
         const uint32_t mg = MAGIC, mq = QP<BITS>::value;
         uint32_t ua[4], ub[4], wo[4];
@@ -249,62 +277,19 @@ __global__ void __maxnreg__(232) prompt_kernel(const __grid_constant__ Params P)
             wo[kb] = bit >> 5;
             lane_args<BITS>(bit & 31u, ua[kb], ub[kb]);
         }
-        uint32_t sit = 0, pit = 0, git = 0, cit = 0;
-        float y[PN], p[PN];
-#pragma unroll
-        for (int r = 0; r < PN; ++r) y[r] = p[r] = 0.f;
-        // The epilogue of a group waits until the next piece is unpacked (the MMA
-        // of the group's last piece overlaps it): pending group state.
-        bool pend = false;
-        uint32_t pend_git = 0, pend_slot = 0;
-        int pend_lg = 0, pend_release = 0;
-        float pend_s = 0.f, pend_b = 0.f;
-
-        auto epilogue = [&]() {
-            const int d = (int)(pend_git & 1);
-            mbar_wait(&B.d_full[d], (pend_git >> 1) & 1, abort, P.status);
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const float *sxp = reinterpret_cast<const float *>(smem + 1024 + pend_slot * L.stage_bytes + L.sx_off) +
-                               pend_lg * PN;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float T[32];
-                tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(d * PN + h * 32), T);
-#pragma unroll
-                for (int r = 0; r < 32; ++r) {
-                    p[h * 32 + r] = fmaf(pend_s, T[r], p[h * 32 + r]);
-                    p[h * 32 + r] = fmaf(pend_b, sxp[h * 32 + r], p[h * 32 + r]);
-                }
-            }
-            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&B.d_empty[d]);
-                if (pend_release) mbar_arrive(&B.st_empty[pend_slot]);
-            }
-            pend = false;
-        };
-
+        uint32_t sit = 0, pit = 0;
         for (int tile = blockIdx.x; tile < P.ntiles && !*abort; tile += gridDim.x) {
-            const int n0 = tile * PM;
-            for (int c = 0; c < P.nchunks && !*abort; ++c, ++cit) {
-                const int cs = (int)(cit & 1);
-                mbar_wait(&B.sb_full[cs], (cit >> 1) & 1, abort, P.status);
-                const uint16_t *srow = reinterpret_cast<const uint16_t *>(smem + L.sb_off + (2 * cs) * L.sb_bytes) + m * SBP;
-                const uint16_t *brow =
-                    reinterpret_cast<const uint16_t *>(smem + L.sb_off + (2 * cs + 1) * L.sb_bytes) + m * SBP;
-                for (int st = 0; st < nstage_chunk && !*abort; ++st, ++sit) {
+            for (int c = 0; c < P.nchunks && !*abort; ++c) {
+                for (int st = 0; st < SPC && !*abort; ++st, ++sit) {
                     const uint32_t slot = sit % STAGES;
                     mbar_wait(&B.st_full[slot], (sit / STAGES) & 1, abort, P.status);
-                    const uint32_t *wrow =
-                        reinterpret_cast<const uint32_t *>(smem + 1024 + slot * L.stage_bytes + L.w_off) + m * CP;
+                    const uint32_t *wrow = reinterpret_cast<const uint32_t *>(stage_ptr(slot) + L.w_off) + m * CP;
 #pragma unroll 1
                     for (int pc = 0; pc < NPIECE; ++pc, ++pit) {
-                        const int kp = st * PSTAGE + pc * PIECE;
-                        const int a = (int)(pit & 1);
-                        // Unpack the piece's four runs of this column: pairs (c_i, c_i+4).
+                        const uint32_t a = pit % ABUF;
+                        // The piece's four runs of this column, as pairs (c_i, c_i+4).
                         uint32_t v[16];
-                        const uint32_t *pw = wrow + (pc * PIECE * BITS) / 32;
+                        const uint32_t *pw = wrow + pc * BITS;
 #pragma unroll
                         for (int kb = 0; kb < 4; ++kb) {
                             if constexpr (BITS == 6)
@@ -313,7 +298,7 @@ __global__ void __maxnreg__(232) prompt_kernel(const __grid_constant__ Params P)
                             else
                                 Unpack<BITS>::template run<1, OFF>(pw + wo[kb], ua[kb], ub[kb], mg, mq, v + 4 * kb);
                         }
-                        mbar_wait(&B.a_empty[a], ((pit >> 1) & 1) ^ 1, abort, P.status);
+                        mbar_wait(&B.a_empty[a], ((pit / ABUF) & 1) ^ 1, abort, P.status);
                         uint8_t *ap = smem + L.a_off + a * A_BYTES + (m >> 3) * 512 + (m & 7) * 16;
 #pragma unroll
                         for (int kb = 0; kb < 4; ++kb)
@@ -321,43 +306,84 @@ __global__ void __maxnreg__(232) prompt_kernel(const __grid_constant__ Params P)
                                 make_uint4(v[4 * kb], v[4 * kb + 1], v[4 * kb + 2], v[4 * kb + 3]);
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&B.a_full[a]);
-                        if (pend) epilogue();
-                        if ((kp + PIECE) % G == 0) {
-                            // This piece ends a group: its epilogue runs after the next piece.
-                            const int gl = kp / G;                       // group within the chunk
-                            pend = true;
-                            pend_git = git++;
-                            pend_slot = slot;
-                            pend_lg = (kp % PSTAGE) / G;
-                            pend_release = pc == NPIECE - 1;             // the stage's last group
-                            pend_s = bf16f(srow[gl]);
-                            pend_b = bias_term<BITS>(pend_s, bf16f(brow[gl]));
+                        if (lane == 0) {
+                            mbar_arrive(&B.a_full[a]);
+                            if (pc == NPIECE - 1) mbar_arrive(&B.st_empty[slot]);   // the stage's codes are read
                         }
                     }
                 }
-                if (pend) epilogue();
+            }
+        }
+    } else {
+        // Epilogue warps: column n0 + m (tensor-memory lane m), rows h*32 .. h*32 + 31.
+        const int e = warp - UNPACK_WARPS;
+        const int q = e & 3, h = e >> 2;
+        const int m = q * 32 + lane;
+        uint32_t sit = 0, git = 0, cit = 0;
+        float y[32], p[32];
+#pragma unroll
+        for (int r = 0; r < 32; ++r) y[r] = p[r] = 0.f;
+        for (int tile = blockIdx.x; tile < P.ntiles && !*abort; tile += gridDim.x) {
+            const int n0 = tile * PM;
+            for (int c = 0; c < P.nchunks && !*abort; ++c, ++cit) {
+                const int cs = (int)(cit & 1);
+                mbar_wait(&B.sb_full[cs], (cit >> 1) & 1, abort, P.status);
+                const uint16_t *srow = reinterpret_cast<const uint16_t *>(smem + L.sb_off + (2 * cs) * L.sb_bytes) + m * SBP;
+                const uint16_t *brow =
+                    reinterpret_cast<const uint16_t *>(smem + L.sb_off + (2 * cs + 1) * L.sb_bytes) + m * SBP;
+                for (int st = 0; st < SPC && !*abort; ++st, ++sit) {
+                    const uint32_t xslot = sit % SXR;
+                    mbar_wait(&B.sx_full[xslot], (sit / SXR) & 1, abort, P.status);
+                    const float *sxs = reinterpret_cast<const float *>(smem + L.sx_off + xslot * SX_BYTES) + h * 32;
+#pragma unroll 1
+                    for (int kp = st * PSTAGE; kp < (st + 1) * PSTAGE; kp += G, ++git) {
+                        const uint32_t d = git % DBUF;
+                        const int gl = kp / G;                       // group within the chunk
+                        const float s = bf16f(srow[gl]);
+                        const float bb = bias_term<BITS>(s, bf16f(brow[gl]));
+                        const float *sxp = sxs + ((kp % PSTAGE) / G) * PN;
+                        mbar_wait(&B.d_full[d], (git / DBUF) & 1, abort, P.status);
+                        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                        float T[32];
+                        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + d * PN + h * 32, T);
+                        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&B.d_empty[d]);
+#pragma unroll
+                        for (int r = 0; r < 32; r += 4) {
+                            const float4 sx4 = *reinterpret_cast<const float4 *>(sxp + r);
+                            const float sxv[4] = {sx4.x, sx4.y, sx4.z, sx4.w};
+#pragma unroll
+                            for (int i = 0; i < 4; i += 2) {
+                                fma2(p[r + i], p[r + i + 1], s, s, T[r + i], T[r + i + 1]);
+                                fma2(p[r + i], p[r + i + 1], bb, bb, sxv[i], sxv[i + 1]);
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&B.sx_empty[xslot]);  // the stage's group sums are read
+                }
                 // Chunk sums in chunk order.
 #pragma unroll
-                for (int r = 0; r < PN; ++r) {
+                for (int r = 0; r < 32; ++r) {
                     y[r] = c == 0 ? p[r] : y[r] + p[r];
                     p[r] = 0.f;
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&B.sb_empty[cs]);
             }
-            // Store the window's rows of this column.
+            // Store the window's rows h*32 .. h*32 + 31 of this column.
             const int n = n0 + m;
             if (n < P.N && !*abort) {
 #pragma unroll
-                for (int r = 0; r < PN; ++r) {
-                    if (r < P.rows) {
+                for (int r = 0; r < 32; ++r) {
+                    if (h * 32 + r < P.rows) {
                         float v = y[r];
                         if (P.out & OUT_RELU2) {
                             const float u = fmaxf(v, 0.f);
                             v = u * u;
                         }
-                        const long long at = (long long)(P.r0 + r) * P.y_stride + n;
+                        const long long at = (long long)(P.r0 + h * 32 + r) * P.y_stride + n;
                         if (P.out & OUT_BF16)
                             reinterpret_cast<__nv_bfloat16 *>(P.y)[at] = __float2bfloat16_rn(v);
                         else
