@@ -162,13 +162,15 @@ extern "C" int tf_qmm_prompt(const uint16_t *x, int rows, int K, const uint32_t 
         const int gps = prompt::PSTAGE / group >= 1 ? prompt::PSTAGE / group : 1;
         rc = tensor_map_2d(&P.tmSX, sx, 4, R64, K / group, prompt::PN, gps);
     }
-    const int gpc = CHUNK / group;
+    // Scales and biases as [N][K / unit][groups of a unit]: one box is a unit of
+    // 128 columns, each row padded by 8 zero values.
+    const int sbg = prompt::sb_groups(group);
     if (!rc)
-        rc = tensor_map_3d(&P.tmS, scales, 2, gpc, K / CHUNK, N, (long long)gpc * 2, (long long)(K / group) * 2,
-                           gpc + 8, 1, prompt::PM);
+        rc = tensor_map_3d(&P.tmS, scales, 2, sbg, K / prompt::sb_k(group), N, (long long)sbg * 2,
+                           (long long)(K / group) * 2, sbg + 8, 1, prompt::PM);
     if (!rc)
-        rc = tensor_map_3d(&P.tmB, biases, 2, gpc, K / CHUNK, N, (long long)gpc * 2, (long long)(K / group) * 2,
-                           gpc + 8, 1, prompt::PM);
+        rc = tensor_map_3d(&P.tmB, biases, 2, sbg, K / prompt::sb_k(group), N, (long long)sbg * 2,
+                           (long long)(K / group) * 2, sbg + 8, 1, prompt::PM);
     if (rc) return rc;
     P.y = static_cast<float *>(y);
     P.y_stride = y_stride;
