@@ -53,6 +53,26 @@ __global__ void prompt_prep(const uint16_t *x, int rows, int K, int G, int R64, 
     sx[t] = acc;
 }
 
+// y rows r0 .. r0 + rows - 1 = the chunk partials part[c][row][N] summed in chunk
+// order (C_0 + C_1 + ...), then the output options.  One thread per (row, column).
+__global__ void prompt_fold(const float *part, int nchunks, int N, int rows, int r0, void *y, long long y_stride,
+                            int out) {
+    const long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    if (t >= (long long)rows * N) return;
+    const int r = (int)(t / N), n = (int)(t - (long long)r * N);
+    float v = part[(long long)r * N + n];
+    for (int c = 1; c < nchunks; ++c) v += part[((long long)c * prompt::PN + r) * N + n];
+    if (out & OUT_RELU2) {
+        const float u = fmaxf(v, 0.f);
+        v = u * u;
+    }
+    const long long at = (long long)(r0 + r) * y_stride + n;
+    if (out & OUT_BF16)
+        static_cast<__nv_bfloat16 *>(y)[at] = __float2bfloat16_rn(v);
+    else
+        static_cast<float *>(y)[at] = v;
+}
+
 struct Ws {
     void *p = nullptr;
     size_t bytes = 0;
@@ -83,9 +103,9 @@ int workspace(cudaStream_t st, size_t bytes, void **out) {
     return TF_OK;
 }
 
-template <int BITS, int G>
-cudaError_t launch_one(const prompt::Params &P, int grid, int smem, cudaStream_t st) {
-    auto k = prompt::prompt_kernel<BITS, G>;
+template <int BITS, int G, bool MC>
+cudaError_t launch_mc(const prompt::Params &P, int grid, int smem, cudaStream_t st) {
+    auto k = prompt::prompt_kernel<BITS, G, MC>;
     static unsigned attr_set = 0;   // one bit per device: shared-memory limit raised
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -98,6 +118,13 @@ cudaError_t launch_one(const prompt::Params &P, int grid, int smem, cudaStream_t
     }
     k<<<grid, prompt::THREADS, smem, st>>>(P);
     return cudaGetLastError();
+}
+
+// Chunk sums in registers only for whole-K items of more than one chunk.
+template <int BITS, int G>
+cudaError_t launch_one(const prompt::Params &P, int grid, int smem, cudaStream_t st) {
+    return P.nchunks > 1 && !P.part ? launch_mc<BITS, G, true>(P, grid, smem, st)
+                                    : launch_mc<BITS, G, false>(P, grid, smem, st);
 }
 
 template <int BITS>
@@ -137,16 +164,29 @@ extern "C" int tf_qmm_prompt(const uint16_t *x, int rows, int K, const uint32_t 
     int nsm = 0, *status = nullptr;
     rc = device_info(&nsm, &status);
     if (rc) return rc;
-    // Workspace: x operand tiles [R64 / 64 windows][K / 128 stages][16 KB], then the
-    // group sums [K/G][R64] fp32.
+    // Work split: whole-K items over the column tiles, or, when the tiles leave SMs
+    // idle, each tile's chunks spread over up to nsm / ntiles items.
+    const int ntiles = (N + prompt::PM - 1) / prompt::PM, nchunks = K / CHUNK;
+    int nsplit = 1;
+    if (ntiles < nsm && nchunks > 1) {
+        nsplit = nsm / ntiles < nchunks ? nsm / ntiles : nchunks;
+        if (nsplit < 1) nsplit = 1;
+    }
+    const int cpi = (nchunks + nsplit - 1) / nsplit;
+    nsplit = (nchunks + cpi - 1) / cpi;
+    // Workspace: x operand tiles [R64 / 64 windows][K / 128 stages][16 KB], the
+    // group sums [K/G][R64] fp32, and with a split the chunk partials
+    // [nchunks][64][N] fp32 of one window.
     const int R64 = (rows + prompt::PN - 1) / prompt::PN * prompt::PN;
     const size_t xp_bytes = (size_t)R64 * K * 2;
     const size_t sx_bytes = (size_t)(K / group) * R64 * 4;
+    const size_t part_bytes = nsplit > 1 ? (size_t)nchunks * prompt::PN * N * 4 : 0;
     void *ws = nullptr;
-    rc = workspace(st, xp_bytes + sx_bytes, &ws);
+    rc = workspace(st, xp_bytes + sx_bytes + part_bytes, &ws);
     if (rc) return rc;
     uint16_t *xp = static_cast<uint16_t *>(ws);
     float *sx = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + xp_bytes);
+    float *part = nsplit > 1 ? reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + xp_bytes + sx_bytes) : nullptr;
     const long long nthreads = (long long)(K / group) * R64;
     prompt_prep<<<(unsigned)((nthreads + 255) / 256), 256, 0, st>>>(x, rows, K, group, R64, xp, sx);
     cudaError_t e = cudaGetLastError();
@@ -177,16 +217,26 @@ extern "C" int tf_qmm_prompt(const uint16_t *x, int rows, int K, const uint32_t 
     P.status = status;
     P.K = K;
     P.N = N;
-    P.ntiles = (N + prompt::PM - 1) / prompt::PM;
-    P.nchunks = K / CHUNK;
+    P.ntiles = ntiles;
+    P.nchunks = nchunks;
     P.out = flags;
+    P.nsplit = nsplit;
+    P.cpi = cpi;
+    P.nitems = ntiles * nsplit;
+    P.part = part;
     const prompt::Layout L = prompt::layout(bits, group);
-    const int grid = P.ntiles < nsm ? P.ntiles : nsm;
+    const int grid = P.nitems < nsm ? P.nitems : nsm;
     for (int r0 = 0; r0 < rows; r0 += prompt::PN) {
         P.r0 = r0;
         P.rows = rows - r0 < prompt::PN ? rows - r0 : prompt::PN;
         e = launch_prompt(bits, group, P, grid, L.smem, st);
         if (e != cudaSuccess) return cuda_error(e, "prompt kernel launch");
+        if (part) {
+            const long long nt = (long long)P.rows * N;
+            prompt_fold<<<(unsigned)((nt + 255) / 256), 256, 0, st>>>(part, nchunks, N, P.rows, r0, y, y_stride, flags);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) return cuda_error(e, "prompt fold launch");
+        }
     }
     return TF_OK;
 }

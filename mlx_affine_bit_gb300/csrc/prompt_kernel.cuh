@@ -88,6 +88,20 @@ struct Params {
     int K, N, ntiles, nchunks;
     int r0, rows;          // window: x rows r0 .. r0 + rows - 1 (rows <= 64) -> y rows r0 ..
     int out;               // OUT_* bits
+    // Work items: item w is column tile w / nsplit over chunks c0 = (w % nsplit) * cpi
+    // .. min(c0 + cpi, nchunks) - 1.  With nsplit > 1 every chunk's partial goes to
+    // part[c][window row][N] (fp32) and a fold sums them in chunk order.
+    int nitems, nsplit, cpi;
+    float *part;
+};
+
+struct Item {
+    int tile, c0, c1;
+    __device__ __forceinline__ Item(const Params &P, int w) {
+        tile = w / P.nsplit;
+        c0 = (w - tile * P.nsplit) * P.cpi;
+        c1 = c0 + P.cpi < P.nchunks ? c0 + P.cpi : P.nchunks;
+    }
 };
 
 // Shared-memory matrix descriptor (tcgen05): canonical K-major layout without
@@ -122,31 +136,21 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
 }
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
+// Tensor-memory load of 16 columns of this warp's lane quarter, completed by
+// tmem_wait16, which names the registers so that nothing reads them earlier.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait16(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
 }
 
 // Barriers of the header, in order.
@@ -166,7 +170,7 @@ struct Bars {
 // once, the MMA lane issues its eight MMAs into the groups' accumulator slots and
 // commits once, the epilogue warps take the stage's groups out of tensor memory
 // and release the slots once.
-template <int BITS, int G>
+template <int BITS, int G, bool MC>
 __global__ void __maxnreg__(80) prompt_kernel(const __grid_constant__ Params P) {
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr int SBP = sb_pitch(G) / 2;                     // scale/bias row pitch (bf16 values)
@@ -222,9 +226,10 @@ __global__ void __maxnreg__(80) prompt_kernel(const __grid_constant__ Params P) 
             asm volatile("prefetch.tensormap [%0];" ::"l"(&P.tmW) : "memory");
             const uint16_t *xw = P.xt + (long long)(P.r0 / PN) * (P.K / PSTAGE) * (X_BYTES / 2);
             uint32_t sit = 0, uit = 0;
-            for (int tile = blockIdx.x; tile < P.ntiles && !*abort; tile += gridDim.x) {
-                const int n0 = tile * PM;
-                for (int u = 0; u < P.nchunks * UPC && !*abort; ++u, ++uit) {
+            for (int w = blockIdx.x; w < P.nitems && !*abort; w += gridDim.x) {
+                const Item it(P, w);
+                const int n0 = it.tile * PM;
+                for (int u = it.c0 * UPC; u < it.c1 * UPC && !*abort; ++u, ++uit) {
                     const int us = uit & 1;
                     mbar_wait(&B.sb_empty[us], ((uit >> 1) & 1) ^ 1, abort, P.status);
                     mbar_arrive_tx(&B.sb_full[us], 2u * PM * sb_pitch(G));
@@ -270,8 +275,9 @@ __global__ void __maxnreg__(80) prompt_kernel(const __grid_constant__ Params P) 
             const uint64_t a0 = smem_desc(smem_u32(smem + L.a_off), 128, (PSTAGE / 8) * 128);
             const uint64_t x0 = smem_desc(smem_u32(stage_ptr(0) + L.x_off), PN * 16, 128);
             uint32_t sit = 0;
-            for (int tile = blockIdx.x; tile < P.ntiles && !*abort; tile += gridDim.x) {
-                for (int st = 0; st < P.nchunks * (CHUNK / PSTAGE) && !*abort; ++st, ++sit) {
+            for (int w = blockIdx.x; w < P.nitems && !*abort; w += gridDim.x) {
+                const Item it(P, w);
+                for (int st = it.c0 * (CHUNK / PSTAGE); st < it.c1 * (CHUNK / PSTAGE) && !*abort; ++st, ++sit) {
                     const uint32_t slot = sit % STAGES, a = sit % ABUF, ds = sit % DST;
                     mbar_wait(&B.st_full[slot], (sit / STAGES) & 1, abort, P.status);
                     mbar_wait(&B.a_full[a], (sit / ABUF) & 1, abort, P.status);
@@ -301,8 +307,9 @@ __global__ void __maxnreg__(80) prompt_kernel(const __grid_constant__ Params P) 
         const uint32_t mg = MAGIC, mq = QP<BITS>::value;
         constexpr int RW = PSTAGE * BITS / 32;                   // words of a stage row
         uint32_t sit = 0;
-        for (int tile = blockIdx.x; tile < P.ntiles && !*abort; tile += gridDim.x) {
-            for (int st = 0; st < P.nchunks * (CHUNK / PSTAGE) && !*abort; ++st, ++sit) {
+        for (int w = blockIdx.x; w < P.nitems && !*abort; w += gridDim.x) {
+            const Item it(P, w);
+            for (int st = it.c0 * (CHUNK / PSTAGE); st < it.c1 * (CHUNK / PSTAGE) && !*abort; ++st, ++sit) {
                 const uint32_t slot = sit % STAGES, a = sit % ABUF;
                 mbar_wait(&B.st_full[slot], (sit / STAGES) & 1, abort, P.status);
                 uint32_t wv[RW + 1];                             // + one zero word: a run's second word
@@ -346,12 +353,25 @@ __global__ void __maxnreg__(80) prompt_kernel(const __grid_constant__ Params P) 
         const int m = q * 32 + lane;
         const bool active = h * EPI_ROWS < P.rows;
         uint32_t sit = 0, uit = 0;
-        float y[EPI_ROWS], p[EPI_ROWS];
+        float p[EPI_ROWS], y[MC ? EPI_ROWS : 1];             // chunk partial; chunk sums (K > one chunk)
 #pragma unroll
-        for (int r = 0; r < EPI_ROWS; ++r) y[r] = p[r] = 0.f;
-        for (int tile = blockIdx.x; tile < P.ntiles && !*abort; tile += gridDim.x) {
-            const int n0 = tile * PM;
-            for (int c = 0; c < P.nchunks && !*abort; ++c) {
+        for (int r = 0; r < EPI_ROWS; ++r) p[r] = 0.f;
+        // One group's epilogue: p = fma(s, T, p); p = fma(b', sum_group(x), p) per row.
+        auto group_fma = [&](const uint32_t (&T)[16], float sg, float bg, const float *sxp) {
+#pragma unroll
+            for (int r = 0; r < EPI_ROWS; r += 4) {
+                const float4 sx4 = *reinterpret_cast<const float4 *>(sxp + r);
+                fma2(p[r], p[r + 1], sg, sg, __uint_as_float(T[r]), __uint_as_float(T[r + 1]));
+                fma2(p[r], p[r + 1], bg, bg, sx4.x, sx4.y);
+                fma2(p[r + 2], p[r + 3], sg, sg, __uint_as_float(T[r + 2]), __uint_as_float(T[r + 3]));
+                fma2(p[r + 2], p[r + 3], bg, bg, sx4.z, sx4.w);
+            }
+        };
+        for (int w = blockIdx.x; w < P.nitems && !*abort; w += gridDim.x) {
+            const Item it(P, w);
+            const int n0 = it.tile * PM;
+            const int n = n0 + m;
+            for (int c = it.c0; c < it.c1 && !*abort; ++c) {
                 for (int u = 0; u < UPC && !*abort; ++u, ++uit) {
                     const int us = (int)(uit & 1);
                     mbar_wait(&B.sb_full[us], (uit >> 1) & 1, abort, P.status);
@@ -364,32 +384,40 @@ __global__ void __maxnreg__(80) prompt_kernel(const __grid_constant__ Params P) 
                         mbar_wait(&B.d_full[ds], (sit / DST) & 1, abort, P.status);
                         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                         const float *sxs = reinterpret_cast<const float *>(smem + L.sx_off + xslot * SX_BYTES) + h * EPI_ROWS;
-#pragma unroll 1
+                        const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + ds * GPS * PN + h * EPI_ROWS;
+                        // Groups in order, the next group's accumulators and scale/bias
+                        // fetched while this group's products are issued.
+                        uint32_t TA[16], TB[16];
+                        float sA = bf16f(srow[st * GPS]), sB = 0.f;
+                        float bA = bias_term<BITS>(sA, bf16f(brow[st * GPS])), bB = 0.f;
+                        if (active) {
+                            tmem_ld16(tq, TA);
+                            tmem_wait16(TA);
+                        }
+#pragma unroll
                         for (int j = 0; j < GPS; ++j) {
-                            const float s = bf16f(srow[st * GPS + j]);
-                            const float bb = bias_term<BITS>(s, bf16f(brow[st * GPS + j]));
-                            float T[EPI_ROWS];
-                            if (active)
-                                tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (ds * GPS + j) * PN + h * EPI_ROWS, T);
-                            if (j == GPS - 1) {
-                                // The stage's accumulators are in registers: release the slots.
+                            uint32_t(&Tc)[16] = (j & 1) ? TB : TA;
+                            uint32_t(&Tn)[16] = (j & 1) ? TA : TB;
+                            const float sc = (j & 1) ? sB : sA, bc = (j & 1) ? bB : bA;
+                            if (j + 1 < GPS) {
+                                const float sn = bf16f(srow[st * GPS + j + 1]);
+                                const float bn = bias_term<BITS>(sn, bf16f(brow[st * GPS + j + 1]));
+                                if (j & 1) {
+                                    sA = sn;
+                                    bA = bn;
+                                } else {
+                                    sB = sn;
+                                    bB = bn;
+                                }
+                                if (active) tmem_ld16(tq + (j + 1) * PN, Tn);
+                            } else {
+                                // Every accumulator of the stage is in registers: release the slots.
                                 asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
                                 __syncwarp();
                                 if (lane == 0) mbar_arrive(&B.d_empty[ds]);
                             }
-                            if (active) {
-                                const float *sxp = sxs + j * PN;
-#pragma unroll
-                                for (int r = 0; r < EPI_ROWS; r += 4) {
-                                    const float4 sx4 = *reinterpret_cast<const float4 *>(sxp + r);
-                                    const float sxv[4] = {sx4.x, sx4.y, sx4.z, sx4.w};
-#pragma unroll
-                                    for (int i = 0; i < 4; i += 2) {
-                                        fma2(p[r + i], p[r + i + 1], s, s, T[r + i], T[r + i + 1]);
-                                        fma2(p[r + i], p[r + i + 1], bb, bb, sxv[i], sxv[i + 1]);
-                                    }
-                                }
-                            }
+                            if (active) group_fma(Tc, sc, bc, sxs + j * PN);
+                            if (j + 1 < GPS && active) tmem_wait16(Tn);
                         }
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&B.sx_empty[xslot]);  // the stage's group sums are read
@@ -397,20 +425,35 @@ __global__ void __maxnreg__(80) prompt_kernel(const __grid_constant__ Params P) 
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&B.sb_empty[us]);
                 }
-                // Chunk sums in chunk order.
+                if (P.part) {
+                    // This chunk's partial, summed with the others in chunk order by the fold.
+                    if (active && n < P.N && !*abort) {
 #pragma unroll
-                for (int r = 0; r < EPI_ROWS; ++r) {
-                    y[r] = c == 0 ? p[r] : y[r] + p[r];
-                    p[r] = 0.f;
+                        for (int r = 0; r < EPI_ROWS; ++r)
+                            P.part[((long long)c * PN + h * EPI_ROWS + r) * P.N + n] = p[r];
+                    }
+#pragma unroll
+                    for (int r = 0; r < EPI_ROWS; ++r) p[r] = 0.f;
+                } else if constexpr (MC) {
+                    // Chunk sums in chunk order.
+#pragma unroll
+                    for (int r = 0; r < EPI_ROWS; ++r) {
+                        y[r] = c == 0 ? p[r] : y[r] + p[r];
+                        p[r] = 0.f;
+                    }
                 }
             }
+            if (P.part) continue;
             // Store the window's rows h*16 .. h*16 + 15 of this column.
-            const int n = n0 + m;
             if (active && n < P.N && !*abort) {
 #pragma unroll
                 for (int r = 0; r < EPI_ROWS; ++r) {
                     if (h * EPI_ROWS + r < P.rows) {
-                        float v = y[r];
+                        float v;
+                        if constexpr (MC)
+                            v = y[r];
+                        else
+                            v = p[r];
                         if (P.out & OUT_RELU2) {
                             const float u = fmaxf(v, 0.f);
                             v = u * u;
@@ -422,6 +465,10 @@ __global__ void __maxnreg__(80) prompt_kernel(const __grid_constant__ Params P) 
                             P.y[at] = v;
                     }
                 }
+            }
+            if constexpr (!MC) {
+#pragma unroll
+                for (int r = 0; r < EPI_ROWS; ++r) p[r] = 0.f;
             }
         }
     }

@@ -111,3 +111,20 @@ def test_prompt_refusals():
     with pytest.raises(tf.TfError) as e:            # scales not 16-byte aligned
         tf.tf_qmm_prompt(xd2, 2, 2048, dm2.W, s_off, dm2.b, 64, 4, 64, y, 64, 0)
     assert e.value.rc == -5
+
+
+@pytest.mark.parametrize("bits,group", [(4, 64), (6, 32)])
+def test_prompt_chunk_split_bit_exact(bits, group):
+    # A matrix of more column tiles than SMs runs whole-K items (chunk sums in
+    # registers); its first 300 columns alone run as chunk-split items whose
+    # partials a fold sums.  Both follow C_0 + C_1 + ... and agree bit for bit.
+    N, K, rows = 160 * 128, 6144, 40
+    m = synth.make_matrix(N, K, bits, group, 880 + bits, 0.001, 0.03)
+    xd = dev(synth.make_x(rows, K, 881))
+    wide = prompt(DevMatrix(m), xd)
+    n = 300
+    sub = synth.Matrix(n, K, bits, group, np.ascontiguousarray(m.W[:n]), np.ascontiguousarray(m.scales[:n]),
+                       np.ascontiguousarray(m.biases[:n]), m.seed)
+    narrow = prompt(DevMatrix(sub), xd)
+    assert torch.equal(narrow.view(torch.int32), wide[:, :n].view(torch.int32))
+    oracle_check(sub, synth.make_x(rows, K, 881), narrow.cpu().numpy())
