@@ -63,6 +63,10 @@ def workload_cases(name: str):
     if name == "decode":
         return [("decode %dx%d r%d" % (N, K, r), N, K, 6, 32, s, r)
                 for (N, K, s) in synth.DECODE_SHAPES for r in synth.DECODE_ROWS]
+    if name == "prompt":   # tf_qmm_prompt: 64-row windows on the tensor cores
+        return ([("prompt lmhead %d/%d r64" % (b, g), synth.LMHEAD_N, synth.LMHEAD_K, b, g, s, 64)
+                 for (b, g, s) in synth.LMHEAD_CASES]
+                + [("prompt %dx%d r64" % (N, K), N, K, 6, 32, s, 64) for (N, K, s) in synth.DECODE_SHAPES])
     raise SystemExit("unknown workload " + name)
 
 
@@ -78,6 +82,8 @@ WORKLOAD_TEXT = {
     "options": "decode 12288 x 2048 6-bit g32, rows 1 and 16: fp32 output and bf16 output with the "
                "squared-ReLU epilogue (tf_qmm_ex)",
     "decode": "decode windows: 6-bit g32, 12288x2048 and 2048x12288, rows {1,2,3,8,16} (10 GEMVs a step)",
+    "prompt": "prompt windows (tf_qmm_prompt, 64 rows): the LM head 6-bit g32 and 4-bit g64, and 6-bit g32 "
+              "12288x2048 and 2048x12288 (4 products a step)",
 }
 
 
@@ -423,10 +429,32 @@ def case_row(label, nbytes, us, peak):
 
 
 # Target configurations timed in every default run beside the headline sweep.
-EXTRA_WORKLOADS = ("lmhead", "lmhead16", "decode", "stack")
+EXTRA_WORKLOADS = ("lmhead", "lmhead16", "decode", "stack", "prompt")
+
+
+def prompt_items(cases, dev, tf, min_bytes):
+    """tf_qmm_prompt calls: the product items, each call one x prepass, one launch
+    per 64-row window and, when the chunks are split over work items, one fold."""
+    import torch
+    items = product_items(cases, dev, min_bytes)
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    for it in items:
+        def call(c, st, it=it):
+            W, s, b = it["reps"][c % len(it["reps"])]
+            tf.tf_qmm_prompt(it["x"], it["rows"], it["K"], W, s, b, it["N"], it["bits"], it["group"], it["y"],
+                             it["N"], 0, st)
+        it["call"] = call
+        windows = -(-it["rows"] // 64)
+        ntiles, nchunks = -(-it["N"] // 128), it["K"] // 2048
+        split = ntiles < nsm and nchunks > 1
+        it["launches"] = 1 + windows * (2 if split else 1)
+    return items
 
 
 def build_items(workload, cases, dev, tf, min_bytes):
+    if workload == "prompt":
+        items = prompt_items(cases, dev, tf, min_bytes)
+        return items, sum(it["bytes"] for it in items)
     if workload == "gather":
         items, per_step = gather_items(cases, dev, tf)
     elif workload == "options":

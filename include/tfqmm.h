@@ -185,17 +185,22 @@ int tf_qmm_ex(const uint16_t *x, int rows, int K,
  *   rows 1..65536; K must be a multiple of 2048 (TF_EINVAL_SIZE otherwise) and
  *   scales / biases 16-byte aligned (TF_EINVAL_PTR).
  *   The group dot products run on the tcgen05 tensor cores (M = 128 output
- *   columns, N = 64 rows, accumulators in tensor memory), so this entry point has
- *   its own canonical order: per output, p = fma(scale, T, p); p = fma(bias',
- *   sum_group(x), p) over the groups of each 2048-k chunk from 0 (T the tensor-core
- *   group dot product; bias' = bias - 128 scale for 4-6-bit codes, which enter as
- *   128 + c), y = C_0 + C_1 + ... over the chunks in order.  Every row's result is
- *   the same bit for bit in any window of any size and position of this entry
- *   point, and within the tolerance of tf_qmm; it is not bit-identical to
- *   tf_qmm's (whose segment order and MMA instruction differ).
- *   Allocates a per-(device, stream) workspace for the permuted activations and
- *   their group sums (rows * K * 2 + (K / group) * ceil(rows / 64) * 256 bytes,
- *   grown on demand).  Plain launches: one prepass and one launch per 64 rows.
+ *   columns, N = the window's rows rounded up to 16, accumulators in tensor
+ *   memory), so this entry point has its own canonical order: per output,
+ *   p = fma(scale, T, p); p = fma(bias', sum_group(x), p) over the groups of each
+ *   2048-k chunk from 0 (T the tensor-core group dot product; bias' = bias - 128
+ *   scale for 4-6-bit codes, which enter as 128 + c), y = C_0 + C_1 + ... over the
+ *   chunks in order.  Every row's result is the same bit for bit in any window of
+ *   any size and position of this entry point, and whether or not the chunks are
+ *   split over work items; it is within the tolerance of tf_qmm but not
+ *   bit-identical to it (whose segment order and MMA instruction differ).
+ *   Allocates a per-(device, stream) workspace for the permuted activations,
+ *   their group sums and, when the column tiles are fewer than the SMs and K
+ *   holds more than one chunk, the chunk partials of one window (rows * K * 2 +
+ *   (K / group) * ceil(rows / 64) * 256 + [(K / 2048) * 64 * N * 4] bytes, grown
+ *   on demand; the first call on a stream must precede any graph capture on it).
+ *   Plain launches: one prepass, then per 64 rows one launch and, with split
+ *   chunks, one fold.
  */
 int tf_qmm_prompt(const uint16_t *x, int rows, int K,
                   const uint32_t *W, const uint16_t *scales, const uint16_t *biases,

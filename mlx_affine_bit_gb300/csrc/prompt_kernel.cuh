@@ -136,6 +136,29 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
 }
+// The scales (or biases) of the N <= 4 groups of one stage in one row: one
+// shared-memory load of 2N bytes (2N-byte aligned); get(j) with j known at
+// compile time.
+template <int N>
+struct SbRun {
+    uint32_t lo = 0, hi = 0;
+    __device__ __forceinline__ void load(const uint16_t *p) {
+        if constexpr (N == 4) {
+            const uint2 t = *reinterpret_cast<const uint2 *>(p);
+            lo = t.x;
+            hi = t.y;
+        } else if constexpr (N == 2) {
+            lo = *reinterpret_cast<const uint32_t *>(p);
+        } else {
+            lo = p[0];
+        }
+    }
+    __device__ __forceinline__ float get(int j) const {
+        const uint32_t w = (j & 2) ? hi : lo;
+        return __uint_as_float((j & 1) ? (w & 0xFFFF0000u) : (w << 16));
+    }
+};
+
 // Tensor-memory load of 16 columns of this warp's lane quarter, completed by
 // tmem_wait16, which names the registers so that nothing reads them earlier.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
@@ -388,8 +411,11 @@ __global__ void __maxnreg__(80) prompt_kernel(const __grid_constant__ Params P) 
                         // Groups in order, the next group's accumulators and scale/bias
                         // fetched while this group's products are issued.
                         uint32_t TA[16], TB[16];
-                        float sA = bf16f(srow[st * GPS]), sB = 0.f;
-                        float bA = bias_term<BITS>(sA, bf16f(brow[st * GPS])), bB = 0.f;
+                        SbRun<GPS> sr, br;
+                        sr.load(srow + st * GPS);
+                        br.load(brow + st * GPS);
+                        float sA = sr.get(0), sB = 0.f;
+                        float bA = bias_term<BITS>(sA, br.get(0)), bB = 0.f;
                         if (active) {
                             tmem_ld16(tq, TA);
                             tmem_wait16(TA);
@@ -400,8 +426,8 @@ __global__ void __maxnreg__(80) prompt_kernel(const __grid_constant__ Params P) 
                             uint32_t(&Tn)[16] = (j & 1) ? TA : TB;
                             const float sc = (j & 1) ? sB : sA, bc = (j & 1) ? bB : bA;
                             if (j + 1 < GPS) {
-                                const float sn = bf16f(srow[st * GPS + j + 1]);
-                                const float bn = bias_term<BITS>(sn, bf16f(brow[st * GPS + j + 1]));
+                                const float sn = sr.get(j + 1);
+                                const float bn = bias_term<BITS>(sn, br.get(j + 1));
                                 if (j & 1) {
                                     sA = sn;
                                     bA = bn;
