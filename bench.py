@@ -585,7 +585,8 @@ def run_gpu(args, cases):
     # The same calls when every product waits for the one before it before it
     # reads x (early weights only): the order a chain of dependent layers needs.
     dependent = None
-    if args.launch == "indep":
+    prompt_wl = args.workload == "prompt"      # tf_qmm_prompt: plain launches, no launch modes
+    if args.launch == "indep" and not prompt_wl:
         tf.tf_set_launch_mode(modes["early"])
         dep_us = [time_item(tf, it, cap, 2) for it in items]
         tf.tf_set_launch_mode(modes[args.launch])
@@ -691,7 +692,9 @@ def run_gpu(args, cases):
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOAD_TEXT[args.workload], "parallelism": "replicas" if world > 1 else "1 GPU",
-                       "launch": {"plain": "plain launches", "pdl": "programmatic dependent launch",
+                       "launch": "plain launches (x prepass, one kernel per 64-row window, a fold when chunks are "
+                                 "split); launch modes do not apply" if prompt_wl else
+                                 {"plain": "plain launches", "pdl": "programmatic dependent launch",
                                   "early": "programmatic dependent launch; weights streamed before the "
                                            "dependency wait (weights are never written in the step)",
                                   "indep": "programmatic dependent launch; the step's products are independent "
@@ -704,8 +707,10 @@ def run_gpu(args, cases):
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "frac_of_8tbs_nominal": achieved / 8000.0,
                          "traffic": traffic, "traffic_note": traffic_note,
-                         "traffic_unit": "bytes per step (all qmm launches of one step)",
-                         "kernel": "tfq::qmm_kernel (all products of the step, bytes / summed per-call time)"},
+                         "traffic_unit": "bytes per step (all %s launches of one step)"
+                                         % ("prompt" if prompt_wl else "qmm"),
+                         "kernel": ("tfq::prompt::prompt_kernel" if prompt_wl else "tfq::qmm_kernel")
+                                   + " (all products of the step, bytes / summed per-call time)"},
             "dependent_x": dependent,
             "cpu_baseline": cpu,
             "e2e": {"value": job_throughput(per_step * e2e_steps, world, e2e_ms), "unit": "GB/s",
