@@ -17,6 +17,7 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 SO = os.path.join(HERE, "_build", "libtfqmm.so")
 SO_DEBUG = os.path.join(HERE, "_build", "libtfqmm_debug.so")   # bounds-checking build (tfqmm_debug.h)
+SO_TRACE = os.path.join(HERE, "_build", "libtfqmm_trace.so")   # phase-trace build (tfqmm_trace.h)
 
 TF_OK = 0
 STATUS = {
@@ -50,6 +51,7 @@ class TfMember(ctypes.Structure):
 
 _lib = None
 _debug_lib = None
+_trace_lib = None
 
 
 def lib():
@@ -68,6 +70,36 @@ def debug_lib():
         _debug_lib.tf_debug_shrink_y.argtypes = [ctypes.c_int]
         _debug_lib.tf_debug_shrink_y.restype = ctypes.c_int
     return _debug_lib
+
+
+def trace_lib():
+    """The loaded phase-trace build, libtfqmm_trace.so (same entry points, plus tf_trace_reset / tf_trace_read)."""
+    global _trace_lib
+    if _trace_lib is None:
+        _trace_lib = _load(SO_TRACE)
+        _trace_lib.tf_trace_reset.argtypes = []
+        _trace_lib.tf_trace_reset.restype = ctypes.c_int
+        _trace_lib.tf_trace_read.argtypes = [ctypes.c_void_p, ctypes.c_int]
+        _trace_lib.tf_trace_read.restype = ctypes.c_int
+    return _trace_lib
+
+
+class using:
+    """Context manager: the calls of this module go to library L (a build from
+    debug_lib() or trace_lib()) inside the block."""
+
+    def __init__(self, L):
+        self.L = L
+
+    def __enter__(self):
+        global _lib
+        self.old, _lib = _lib, self.L
+        return self.L
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self.old
+        return False
 
 
 def _load(path):

@@ -15,6 +15,9 @@
 #include <utility>
 
 #include "../../include/tfqmm.h"
+#ifdef TF_TRACE
+#include "../../include/tfqmm_trace.h"
+#endif
 #include "internal.h"
 
 using namespace tfq;
@@ -620,6 +623,41 @@ int tfq::fail_message(int code, const char *msg) { return fail(code, msg); }
 
 int tfq::cuda_error(cudaError_t e, const char *where) { return cuda_fail(e, where); }
 
+#ifdef TF_TRACE
+// Per-device trace buffers (records, counter), allocated at the first traced
+// launch; a failed allocation leaves the launch untraced.
+namespace {
+std::mutex g_tmu;
+std::map<int, std::pair<unsigned long long *, unsigned *>> g_tbuf;
+std::atomic<unsigned> g_tseq{0};
+}  // namespace
+
+tfq::QmmParams tfq::trace_params(const QmmParams &P) {
+    QmmParams Q = P;
+    Q.trace = nullptr;
+    Q.trace_n = nullptr;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return Q;
+    std::lock_guard<std::mutex> lk(g_tmu);
+    auto &b = g_tbuf[dev];
+    if (!b.first) {
+        unsigned long long *rec = nullptr;
+        unsigned *cnt = nullptr;
+        if (cudaMalloc(&rec, (size_t)TRACE_MAX * TRACE_SLOTS * 8) != cudaSuccess) return Q;
+        if (cudaMalloc(&cnt, 4) != cudaSuccess || cudaMemset(cnt, 0, 4) != cudaSuccess) {
+            cudaFree(rec);
+            if (cnt) cudaFree(cnt);
+            return Q;
+        }
+        b = {rec, cnt};
+    }
+    Q.trace = b.first;
+    Q.trace_n = b.second;
+    Q.trace_seq = g_tseq.fetch_add(1);
+    return Q;
+}
+#endif
+
 int tfq::check_product(const uint16_t *x, int rows, int K, const uint32_t *W, const uint16_t *s,
                        const uint16_t *b, int N, int bits, int group, const float *y, int64_t y_stride) {
     g_err.clear();
@@ -941,6 +979,46 @@ int tf_inject_stall(void) {
     g_stall.store(1);
     return TF_OK;
 }
+
+#ifdef TF_TRACE
+int tf_trace_reset(void) {
+    g_err.clear();
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(g_tmu);
+    auto it = g_tbuf.find(dev);
+    if (it != g_tbuf.end()) {
+        e = cudaDeviceSynchronize();
+        if (e == cudaSuccess) e = cudaMemset(it->second.second, 0, 4);
+        if (e == cudaSuccess) e = cudaMemset(it->second.first, 0, (size_t)TRACE_MAX * TRACE_SLOTS * 8);
+        if (e != cudaSuccess) return cuda_fail(e, "trace reset");
+    }
+    g_tseq.store(0);
+    return TF_OK;
+}
+
+int tf_trace_read(uint64_t *buf, int max_records) {
+    g_err.clear();
+    if (!buf || max_records < 0) return fail(TF_EINVAL_PTR, "buf must be a host array of max_records records");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(g_tmu);
+    auto it = g_tbuf.find(dev);
+    if (it == g_tbuf.end()) return 0;
+    e = cudaDeviceSynchronize();
+    unsigned n = 0;
+    if (e == cudaSuccess) e = cudaMemcpy(&n, it->second.second, 4, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "trace read");
+    const int k = (int)std::min<unsigned>(std::min<unsigned>(n, (unsigned)TRACE_MAX), (unsigned)max_records);
+    if (k > 0) {
+        e = cudaMemcpy(buf, it->second.first, (size_t)k * TRACE_SLOTS * 8, cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return cuda_fail(e, "trace read");
+    }
+    return k;
+}
+#endif
 
 #ifdef TF_DEBUG_BOUNDS
 int tf_debug_shrink_y(int rows) {

@@ -3,11 +3,13 @@
 #pragma once
 #include <cuda.h>   // CUtensorMap (type only; the encoder is fetched at run time)
 
-// The bounds-checking debug build puts its internals in a namespace of its
-// own, so that its symbols (kernels, launchers) never meet the product's when
-// a process loads both libraries.
+// The bounds-checking debug build and the phase-trace build put their
+// internals in namespaces of their own, so that their symbols (kernels,
+// launchers) never meet the product's when a process loads several libraries.
 #ifdef TF_DEBUG_BOUNDS
 #define tfq tfq_debug
+#elif defined(TF_TRACE)
+#define tfq tfq_trace
 #endif
 #include <stdint.h>
 
@@ -36,6 +38,8 @@ constexpr int XS_MAX = 64 * 1024;          // bytes of permuted x a CTA keeps re
 constexpr int SMEM_MAX = 227 * 1024;       // dynamic shared memory per CTA on sm_103a
 constexpr int SMEM_PER_SM = 228 * 1024;    // shared memory per SM (each CTA reserves 1 KB)
 constexpr int HDR_BYTES = 256;             // mbarriers + flags at the start of smem
+// Phase-trace build: words a CTA record, records a buffer, header byte of the record index.
+constexpr int TRACE_SLOTS = 9, TRACE_MAX = 1 << 16, TRACE_HDR = 192;
 
 // Row bucket of a launch (a kernel template parameter): 1 (a single row),
 // 2, 4, 8 or 16; the B-fragment layout holds layout_rows(bucket) rows.
@@ -94,7 +98,18 @@ struct QmmParams {
     int x_rows, y_rows;
     long long ws_elems;
     int n_counters;
+    // Phase-trace build only (null otherwise): per-CTA records, their counter,
+    // and the launch's number.
+    unsigned long long *trace;
+    unsigned *trace_n;
+    unsigned trace_seq;
 };
+
+#ifdef TF_TRACE
+// Host (phase-trace build): the launch's parameters with the trace buffer and
+// the next launch number.
+QmmParams trace_params(const QmmParams &P);
+#endif
 
 // Bits of the device status word.
 constexpr int STATUS_WAIT = 1;      // a bounded wait ran out

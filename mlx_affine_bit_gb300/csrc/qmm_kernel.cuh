@@ -73,6 +73,46 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
+// Phase-trace build (TF_TRACE): each CTA takes a record of TRACE_SLOTS words
+// (its launch number, its SM and block, then %globaltimer at the phases below)
+// in a device buffer that tf_trace_read copies out; the record's index sits in
+// the shared header (byte TRACE_HDR).  In the product build the macros are empty.
+enum TracePhase {
+    TR_ENTER = 2,     // kernel entry
+    TR_TMA0 = 3,      // producer: the CTA's first stage issued
+    TR_LAND0 = 4,     // producer: the first stage landed
+    TR_RELEASE = 5,   // consumer thread 0 past the dependency wait
+    TR_XLOADED = 6,   // consumer thread 0: the first x slice placed and summed
+    TR_STAGE0 = 7,    // consumer thread 0: the first stage's group products done
+    TR_EXIT = 8,      // consumer thread 0: its last store issued
+};
+#ifdef TF_TRACE
+__device__ __forceinline__ void trace_begin(const QmmParams &P, uint8_t *smem) {
+    const unsigned s = P.trace ? atomicAdd(P.trace_n, 1u) : (unsigned)TRACE_MAX;
+    *reinterpret_cast<unsigned *>(smem + TRACE_HDR) = s;
+    if (s < (unsigned)TRACE_MAX) {
+        unsigned sm;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+        unsigned long long *r = P.trace + (unsigned long long)s * TRACE_SLOTS;
+        r[0] = P.trace_seq;
+        r[1] = ((unsigned long long)sm << 32) | blockIdx.x;
+        for (int i = 2; i < TRACE_SLOTS; ++i) r[i] = 0ull;
+        r[TR_ENTER] = global_ns();
+    }
+}
+__device__ __forceinline__ void trace_at(const QmmParams &P, const uint8_t *smem, int phase) {
+    const unsigned s = *reinterpret_cast<const volatile unsigned *>(smem + TRACE_HDR);
+    if (s < (unsigned)TRACE_MAX) P.trace[(unsigned long long)s * TRACE_SLOTS + phase] = global_ns();
+}
+#define TFQ_TRACE_BEGIN(P, smem) trace_begin(P, smem)
+#define TFQ_TRACE(smem, phase) trace_at(P, smem, phase)
+#define TFQ_LAUNCH_PARAMS(P) trace_params(P)
+#else
+#define TFQ_TRACE_BEGIN(P, smem) ((void)0)
+#define TFQ_TRACE(smem, phase) ((void)0)
+#define TFQ_LAUNCH_PARAMS(P) (P)
+#endif
+
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
                  : "memory");
@@ -288,7 +328,9 @@ __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                 }
                 // The CTA's first stage travels alone: every CTA's first stage
                 // lands before later stages compete with it for DRAM.
+                if (it == 0 && lane == 0) TFQ_TRACE(smem, TR_TMA0);
                 if (it == 0 && !withhold) mbar_wait(&full[slot], ring.phase, abort, P.status);
+                if (it == 0 && lane == 0) TFQ_TRACE(smem, TR_LAND0);
             } else {
                 // Odd shapes or alignments: plain copies by the warp into the same layout.
                 const int k1 = min(I.k_hi, k0 + CHUNK);
@@ -712,6 +754,7 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
     // that they too read x after its producer finished.
     const bool early_x = P.early_x && P.dep == 0;
     if (P.dep != 2 && !early_x) grid_dependency_wait();
+    if (tid == 0 && !early_x) TFQ_TRACE(smem, TR_RELEASE);
     if (P.dep == 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     bool waited = !early_x;                  // this thread has passed the dependency wait
     int cur_slice = -1;
@@ -728,6 +771,7 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
             else
                 load_x_groups<G, LR>(P, I, Bf, sx, tid, CG * GT);
             named_bar(1, CG * GT);
+            if (tid == 0 && cur_slice < 0) TFQ_TRACE(smem, TR_XLOADED);
             cur_slice = I.slice;
         }
         if (CG > 1 && (own % CG) != cg) {    // another group's item: skip its stages
@@ -854,11 +898,13 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                             *reinterpret_cast<float2 *>(pw + c * LR + r) = make_float2(p[t][nt][2 * h], p[t][nt][2 * h + 1]);
                     }
             named_bar(gbar, GT);
+            if (tid == 0 && it == 0) TFQ_TRACE(smem, TR_STAGE0);
             // Early x: every thread passes the dependency wait before the first
             // write of y or of split-K partials (the fold below).
             if (!waited && (P.nsl > 1 || k0 + CHUNK >= I.k_hi)) {
                 grid_dependency_wait();
                 waited = true;
+                if (tid == 0) TFQ_TRACE(smem, TR_RELEASE);
             }
             // Chunk sum C = P_0 + P_1 + ... in segment order, then the chunk fold.
             const int nseg = (k1 - k0 + SEG - 1) / SEG;
@@ -893,7 +939,10 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
     // Every thread passes the dependency wait before it exits, so that this
     // grid never completes before the one it depends on (a later kernel's
     // wait on this grid then covers every kernel before it).
-    if (!waited) grid_dependency_wait();
+    if (!waited) {
+        grid_dependency_wait();
+        if (tid == 0) TFQ_TRACE(smem, TR_RELEASE);
+    }
     if (CG == 1 && P.nsl > 1) {
         // Split K: once all of this CTA's chunk sums are out, one arrival ticket
         // per item, issued together; the last CTA to arrive at an item folds its
@@ -942,6 +991,7 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
             named_bar(gbar, GT);                             // before the flags are rewritten
         }
     }
+    if (tid == 0) TFQ_TRACE(smem, TR_EXIT);
 }
 
 // ------------------------------------------------------------------ kernel --
@@ -964,6 +1014,7 @@ __global__ void __maxnreg__((RegCap<MT, CG>::value)) qmm_kernel(const __grid_con
     volatile int *abort = reinterpret_cast<volatile int *>(empty + MAX_STAGES);
     volatile uint32_t *magic = reinterpret_cast<volatile uint32_t *>(abort + 2);
     if (threadIdx.x == 0) {
+        TFQ_TRACE_BEGIN(P, smem);
         for (int i = 0; i < P.stages; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], NCW);
@@ -1013,7 +1064,7 @@ cudaError_t launch_width(int group, int rb, int mt, int cg, const QmmParams &P, 
         attr[0].val.programmaticStreamSerializationAllowed = 1;                               \
         cfg.attrs = attr;                                                                     \
         cfg.numAttrs = pdl ? 1 : 0;                                                           \
-        return cudaLaunchKernelEx(&cfg, k, P);                                                \
+        return cudaLaunchKernelEx(&cfg, k, TFQ_LAUNCH_PARAMS(P));                             \
     }
 #define TFQ_ROWS(G_) TFQ_CASE(G_, 1, 1, 1) TFQ_CASE(G_, 2, 1, 1) TFQ_CASE(G_, 4, 1, 1) TFQ_CASE(G_, 8, 1, 1) \
     TFQ_CASE(G_, 16, 1, 1) TFQ_CASE(G_, 1, 2, 1) TFQ_CASE(G_, 2, 2, 1) TFQ_CASE(G_, 4, 2, 1)                \
