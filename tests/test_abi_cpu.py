@@ -44,6 +44,26 @@ def test_debug_build_exports(tf):
     assert tf.debug_lib().tf_debug_shrink_y(17) == -3
 
 
+def test_trace_build_exports(tf):
+    # The phase-trace build (made on request) exports every entry point of
+    # tfqmm.h and tfqmm_trace.h; the product library exports no trace entry.
+    from mlx_affine_bit_gb300 import build
+    so = build.build_trace()
+    names = set()
+    for h in ("tfqmm.h", "tfqmm_trace.h"):
+        names |= set(re.findall(r"^(?:int|const char \*)\s*(tf_\w+)\s*\(",
+                                open(os.path.join(ROOT, "include", h)).read(), re.M))
+    assert {"tf_trace_reset", "tf_trace_read"} <= names
+    out = subprocess.check_output(["nm", "-D", "--defined-only", so]).decode()
+    exported = set(re.findall(r"\sT\s(tf_\w+)$", out, re.M))
+    assert names <= exported, names - exported
+    L = tf.trace_lib()
+    for name in names:
+        getattr(L, name)
+    prod = subprocess.check_output(["nm", "-D", "--defined-only", tf.SO]).decode()
+    assert "tf_trace_" not in prod
+
+
 A = 4096  # a 16-byte aligned stand-in address; no call below reaches the device
 
 
