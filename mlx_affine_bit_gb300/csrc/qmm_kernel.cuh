@@ -757,6 +757,25 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
     if (tid == 0 && !early_x) TFQ_TRACE(smem, TR_RELEASE);
     if (P.dep == 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     bool waited = !early_x;                  // this thread has passed the dependency wait
+    // Early x: the outputs of an item finished before the dependency release wait
+    // in registers and are stored after it, with the group's next item, so that the
+    // group computes that item before the release.  One item is parked, in the one-
+    // and two-row single-group instances only (their CTAs hold few items; more
+    // parked items, or parking elsewhere, measured slower).
+    constexpr bool PARK = RB <= 2 && CG == 1;
+    float dv[OUTS];
+    int dn0 = 0;
+    bool parked = false;
+    auto flush = [&]() {
+        if (parked) {
+#pragma unroll
+            for (int i = 0; i < OUTS; ++i) {
+                const int o = gtid + i * GT;
+                if (o < NOUT) store_y(P, o - (o / LR) * LR, dn0 + o / LR, dv[i]);
+            }
+        }
+        parked = false;
+    };
     int cur_slice = -1;
     uint32_t it = 0;                         // stages this group has computed
     Ring ring;
@@ -900,11 +919,19 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
             named_bar(gbar, GT);
             if (tid == 0 && it == 0) TFQ_TRACE(smem, TR_STAGE0);
             // Early x: every thread passes the dependency wait before the first
-            // write of y or of split-K partials (the fold below).
+            // write of y or of split-K partials (the fold below); an item's final
+            // outputs are parked instead while the group has a later item and room.
+            bool park = false;
             if (!waited && (P.nsl > 1 || k0 + CHUNK >= I.k_hi)) {
-                grid_dependency_wait();
-                waited = true;
-                if (tid == 0) TFQ_TRACE(smem, TR_RELEASE);
+                const bool later = iw.mt + CG * iw.team < P.nmt;
+                if (PARK && P.nsl == 1 && later && !parked) {
+                    park = true;
+                } else {
+                    grid_dependency_wait();
+                    waited = true;
+                    if (tid == 0) TFQ_TRACE(smem, TR_RELEASE);
+                    flush();
+                }
             }
             // Chunk sum C = P_0 + P_1 + ... in segment order, then the chunk fold.
             const int nseg = (k1 - k0 + SEG - 1) / SEG;
@@ -927,12 +954,22 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                         if (j < nseg) C = C + v[j];
                     if (P.nsl == 1) {
                         yacc[i] = chunk == 0 ? C : yacc[i] + C;
-                        if (k0 + CHUNK >= I.k_hi) store_y(P, fr, n0 + fc, yacc[i]);
+                        if (k0 + CHUNK >= I.k_hi) {
+                            if (park) {
+                                dv[i] = yacc[i];
+                            } else {
+                                store_y(P, fr, n0 + fc, yacc[i]);
+                            }
+                        }
                     } else if (fr < rows && n0 + fc < P.N) {
                         const long long at = ((long long)chunk * rows + fr) * P.N + n0 + fc;
                         if (TFQ_IN(P, at < P.ws_elems)) P.ws[at] = C;
                     }
                 }
+            }
+            if (park) {
+                dn0 = n0;
+                parked = true;
             }
         }
     }
@@ -943,6 +980,7 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
         grid_dependency_wait();
         if (tid == 0) TFQ_TRACE(smem, TR_RELEASE);
     }
+    flush();
     if (CG == 1 && P.nsl > 1) {
         // Split K: once all of this CTA's chunk sums are out, one arrival ticket
         // per item, issued together; the last CTA to arrive at an item folds its
