@@ -189,6 +189,40 @@ __device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, int x,
         : "memory");
 }
 
+// The same copies with an L2 cache hint (a policy from createpolicy).  The
+// weights, scales and biases are read once a launch: streamed with an
+// evict-first policy they leave x, y and the split-K partials in L2.
+#define TFQ_L2_HINT 1
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void tma_3d_hint(void *dst, const CUtensorMap *map, int x, int y, int z, uint64_t *bar,
+                                            uint64_t pol) {
+#if TFQ_L2_HINT
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(
+            smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+#else
+    tma_3d(dst, map, x, y, z, bar);
+#endif
+}
+__device__ __forceinline__ void tma_2d_hint(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar,
+                                            uint64_t pol) {
+#if TFQ_L2_HINT
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(
+            smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+#else
+    tma_2d(dst, map, x, y, bar);
+#endif
+}
+
 __device__ __forceinline__ void mma_bf16(float c[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -317,13 +351,14 @@ __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                 // boxes count toward the transaction bytes.
                 if (lane == 0) {
                     mbar_arrive_tx(&full[slot], (uint32_t)P.stage_bytes);
-                    tma_3d(st, &P.tmW, 0, n0, k0 / SEG, &full[slot]);
+                    const uint64_t pol = l2_evict_first();
+                    tma_3d_hint(st, &P.tmW, 0, n0, k0 / SEG, &full[slot], pol);
                     if (P.sb3d) {
-                        tma_3d(sst, &P.tmS, 0, k0 / CHUNK, n0, &full[slot]);
-                        tma_3d(bst, &P.tmB, 0, k0 / CHUNK, n0, &full[slot]);
+                        tma_3d_hint(sst, &P.tmS, 0, k0 / CHUNK, n0, &full[slot], pol);
+                        tma_3d_hint(bst, &P.tmB, 0, k0 / CHUNK, n0, &full[slot], pol);
                     } else {
-                        tma_2d(sst, &P.tmS, k0 / G, n0, &full[slot]);
-                        tma_2d(bst, &P.tmB, k0 / G, n0, &full[slot]);
+                        tma_2d_hint(sst, &P.tmS, k0 / G, n0, &full[slot], pol);
+                        tma_2d_hint(bst, &P.tmB, k0 / G, n0, &full[slot], pol);
                     }
                 }
                 // The CTA's first stage travels alone: every CTA's first stage
