@@ -199,8 +199,8 @@ extern "C" int tf_qmm_prompt(const uint16_t *x, int rows, int K, const uint32_t 
                        sw + prompt::code_pad_words(bits), prompt::PM, 1);
     P.xt = xp;
     if (!rc) {
-        const int gps = prompt::PSTAGE / group >= 1 ? prompt::PSTAGE / group : 1;
-        rc = tensor_map_2d(&P.tmSX, sx, 4, R64, K / group, prompt::PN, gps);
+        // One box: a scale/bias unit's groups (<= 32) x the window's 64 rows.
+        rc = tensor_map_2d(&P.tmSX, sx, 4, R64, K / group, prompt::PN, prompt::sb_groups(group));
     }
     // Scales and biases as [N][K / unit][groups of a unit]: one box is a unit of
     // 128 columns, each row padded by 8 zero values.

@@ -13,10 +13,10 @@
 //            the group's codes (exact, or 128 + c at 4-6 bits) and x, K = 16 a step
 //   p      = fma(s, T, p); p = fma(b', sum_group(x), p)      (b' = b - 128 s for offset codes)
 // p runs over the groups of a 2048-k chunk from 0, and y = C_0 + C_1 + ... over the
-// chunks in order.  Roles: a producer warp streams, per 128-k stage, the tile's
-// codes, the window's x (permuted to the codes' pair order by a prepass) and the
-// per-group sums of x with TMA, and per unit of up to 32 groups the scales and
-// biases; four unpack warps write each stage's codes as bf16 into shared memory
+// chunks in order.  Roles: a producer warp streams with TMA, per 128-k stage, the
+// tile's codes and the window's x (permuted to the codes' pair order by a prepass),
+// and per unit of up to 32 groups the scales, the biases and the per-group sums of
+// x; four unpack warps write each stage's codes as bf16 into shared memory
 // (canonical K-major layout); one thread of an MMA warp issues the stage's eight
 // MMAs into the groups' accumulator slots; sixteen epilogue warps apply the group
 // epilogue out of tensor memory.  Every wait is bounded.
@@ -34,7 +34,6 @@ constexpr int PN = 64;                  // activation rows per window (largest M
 constexpr int PSTAGE = 128;             // k per pipeline stage (eight K = 16 MMAs)
 constexpr int KSTEP = 16;               // k per MMA
 constexpr int STAGES = 3;               // stage ring depth (codes and x)
-constexpr int SXR = 8;                  // ring depth of the per-group sums of x (one slot a stage)
 constexpr int ABUF = 2;                 // unpacked stages in flight
 constexpr int DSLOTS = 8;               // group accumulators in tensor memory (PN columns each)
 constexpr int UNPACK_WARPS = 4;         // one column per thread
@@ -44,7 +43,7 @@ constexpr int PRODUCER = UNPACK_WARPS + EPI_WARPS, MMA_WARP = PRODUCER + 1;
 constexpr int THREADS = (MMA_WARP + 1) * 32;
 constexpr int A_BYTES = PM * PSTAGE * 2;         // one unpacked stage (bf16)
 constexpr int X_BYTES = PN * PSTAGE * 2;         // one stage of x (bf16)
-constexpr int SX_BYTES = 1024;                   // per-group sums of x of one stage (<= 4 groups x 64 rows)
+constexpr int SX_BYTES = 32 * PN * 4;            // per-group sums of x of one scale/bias unit (<= 32 groups x 64 rows)
 constexpr int TMEM_COLS = DSLOTS * PN;           // accumulator slots
 
 // Groups of one stage, and stage-sized accumulator sets in tensor memory.
@@ -62,7 +61,7 @@ __host__ __device__ constexpr int code_pitch(int bits) { return (PSTAGE * bits /
 __host__ __device__ constexpr int sb_pitch(int group) { return (sb_groups(group) + 8) * 2; }
 
 struct Layout {
-    int w_off, x_off, stage_bytes, sx_off, sb_off, sb_bytes, a_off, smem;
+    int w_off, x_off, stage_bytes, sb_off, sb_bytes, sx_off, a_off, smem;
 };
 __host__ __device__ inline Layout layout(int bits, int group) {
     Layout L;
@@ -72,9 +71,9 @@ __host__ __device__ inline Layout layout(int bits, int group) {
     L.stage_bytes = wbytes + X_BYTES;
     L.sb_bytes = (PM * sb_pitch(group) + 1023) & ~1023;   // scales (or biases) of one unit
     const int base = 1024;                                // header: barriers, TMEM address, flags
-    L.sx_off = base + STAGES * L.stage_bytes;             // SXR slots of SX_BYTES
-    L.sb_off = L.sx_off + SXR * SX_BYTES;
-    L.a_off = L.sb_off + 4 * L.sb_bytes;                  // two slots x (scales, biases)
+    L.sb_off = base + STAGES * L.stage_bytes;
+    L.sx_off = L.sb_off + 4 * L.sb_bytes;                 // two slots x (scales, biases)
+    L.a_off = L.sx_off + 2 * SX_BYTES;                    // two slots of group sums
     L.smem = L.a_off + ABUF * A_BYTES;
     return L;
 }
@@ -179,7 +178,6 @@ __device__ __forceinline__ void tmem_wait16(uint32_t (&r)[16]) {
 // Barriers of the header, in order.
 struct Bars {
     uint64_t st_full[STAGES], st_empty[STAGES];
-    uint64_t sx_full[SXR], sx_empty[SXR];
     uint64_t sb_full[2], sb_empty[2];
     uint64_t a_full[ABUF], a_empty[ABUF];
     uint64_t d_full[DSLOTS], d_empty[DSLOTS];
@@ -213,10 +211,6 @@ __global__ void __maxnreg__(80) prompt_kernel(const __grid_constant__ Params P) 
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(&B.st_full[i], 1);
             mbar_init(&B.st_empty[i], UNPACK_WARPS + 1);
-        }
-        for (int i = 0; i < SXR; ++i) {
-            mbar_init(&B.sx_full[i], 1);
-            mbar_init(&B.sx_empty[i], EPI_WARPS);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&B.sb_full[i], 1);
@@ -255,16 +249,13 @@ __global__ void __maxnreg__(80) prompt_kernel(const __grid_constant__ Params P) 
                 for (int u = it.c0 * UPC; u < it.c1 * UPC && !*abort; ++u, ++uit) {
                     const int us = uit & 1;
                     mbar_wait(&B.sb_empty[us], ((uit >> 1) & 1) ^ 1, abort, P.status);
-                    mbar_arrive_tx(&B.sb_full[us], 2u * PM * sb_pitch(G));
+                    mbar_arrive_tx(&B.sb_full[us], 2u * PM * sb_pitch(G) + (uint32_t)(sb_groups(G) * PN * 4));
                     tma_3d(smem + L.sb_off + (2 * us) * L.sb_bytes, &P.tmS, 0, u, n0, &B.sb_full[us]);
                     tma_3d(smem + L.sb_off + (2 * us + 1) * L.sb_bytes, &P.tmB, 0, u, n0, &B.sb_full[us]);
+                    tma_2d(smem + L.sx_off + us * SX_BYTES, &P.tmSX, P.r0, u * sb_groups(G), &B.sb_full[us]);
                     for (int st = 0; st < SPU && !*abort; ++st, ++sit) {
                         const uint32_t slot = sit % STAGES;
                         const int k0 = u * sb_k(G) + st * PSTAGE;
-                        const uint32_t xslot = sit % SXR;
-                        mbar_wait(&B.sx_empty[xslot], ((sit / SXR) & 1) ^ 1, abort, P.status);
-                        mbar_arrive_tx(&B.sx_full[xslot], (uint32_t)(GPS * PN * 4));
-                        tma_2d(smem + L.sx_off + xslot * SX_BYTES, &P.tmSX, P.r0, k0 / G, &B.sx_full[xslot]);
                         mbar_wait(&B.st_empty[slot], ((sit / STAGES) & 1) ^ 1, abort, P.status);
                         uint8_t *sp = stage_ptr(slot);
                         mbar_arrive_tx(&B.st_full[slot], (uint32_t)(PM * code_pitch(BITS) + X_BYTES));
@@ -282,10 +273,6 @@ __global__ void __maxnreg__(80) prompt_kernel(const __grid_constant__ Params P) 
             for (uint32_t j = 0; j < (uit < 2u ? uit : 2u); ++j) {
                 const uint32_t q = uit - 1 - j;
                 mbar_wait(&B.sb_full[q & 1], (q >> 1) & 1, abort, P.status, false);
-            }
-            for (uint32_t j = 0; j < (sit < (uint32_t)SXR ? sit : (uint32_t)SXR); ++j) {
-                const uint32_t q = sit - 1 - j;
-                mbar_wait(&B.sx_full[q % SXR], (q / SXR) & 1, abort, P.status, false);
             }
         }
     } else if (warp == MMA_WARP) {
@@ -402,11 +389,11 @@ __global__ void __maxnreg__(80) prompt_kernel(const __grid_constant__ Params P) 
                     const uint16_t *brow =
                         reinterpret_cast<const uint16_t *>(smem + L.sb_off + (2 * us + 1) * L.sb_bytes) + m * SBP;
                     for (int st = 0; st < SPU && !*abort; ++st, ++sit) {
-                        const uint32_t xslot = sit % SXR, ds = sit % DST;
-                        mbar_wait(&B.sx_full[xslot], (sit / SXR) & 1, abort, P.status);
+                        const uint32_t ds = sit % DST;
                         mbar_wait(&B.d_full[ds], (sit / DST) & 1, abort, P.status);
                         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                        const float *sxs = reinterpret_cast<const float *>(smem + L.sx_off + xslot * SX_BYTES) + h * EPI_ROWS;
+                        const float *sxs = reinterpret_cast<const float *>(smem + L.sx_off + us * SX_BYTES) +
+                                           st * GPS * PN + h * EPI_ROWS;
                         const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + ds * GPS * PN + h * EPI_ROWS;
                         // Groups in order, the next group's accumulators and scale/bias
                         // fetched while this group's products are issued.
@@ -445,8 +432,6 @@ __global__ void __maxnreg__(80) prompt_kernel(const __grid_constant__ Params P) 
                             if (active) group_fma(Tc, sc, bc, sxs + j * PN);
                             if (j + 1 < GPS && active) tmem_wait16(Tn);
                         }
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&B.sx_empty[xslot]);  // the stage's group sums are read
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&B.sb_empty[us]);
