@@ -1,8 +1,9 @@
 // prompt.cu -- tf_qmm_prompt: the product for many activation rows, weights read
 // once per 64-row window, group dot products on the tcgen05 tensor cores
 // (kernel in prompt_kernel.cuh).  Host side: checks, a per-(device, stream)
-// workspace for the permuted activations and their per-group sums, the x
-// prepass kernel, tensor maps and one launch per 64-row window.
+// workspace for the permuted activations, their per-group sums and the chunk
+// partials of a split, the x prepass kernel, the work split, tensor maps, and per
+// 64-row window one launch (plus the fold of the partials when chunks are split).
 #include <cuda.h>
 #include <cuda_runtime.h>
 

@@ -53,8 +53,8 @@ __host__ __device__ constexpr int dsets(int group) { return DSLOTS / groups_per_
 __host__ __device__ constexpr int sb_groups(int group) { return CHUNK / group < 32 ? CHUNK / group : 32; }
 __host__ __device__ constexpr int sb_k(int group) { return sb_groups(group) * group; }
 // Pad words after each stage row of codes: the TMA box row is a multiple of 16
-// bytes and row pitches of an odd number of 16-byte units keep the math warps'
-// vector reads of their own rows apart in the banks.
+// bytes and row pitches of an odd number of 16-byte units keep the unpack warps'
+// 16-byte reads of their own rows apart in the banks.
 __host__ __device__ constexpr int code_pad_words(int bits) { return (bits & 1) ? 8 : 4; }
 __host__ __device__ constexpr int code_pitch(int bits) { return (PSTAGE * bits / 32 + code_pad_words(bits)) * 4; }
 // Scale/bias rows of a unit: its groups plus 8 padding values.
