@@ -76,9 +76,10 @@ def test_prompt_windows_bit_exact(bits, group):
     oracle_check(m, x, full.cpu().numpy())
 
 
+@pytest.mark.parametrize("K", [2048, 4096])   # 4096: two chunks over 3 column tiles, so split and folded
 @pytest.mark.parametrize("flags", [tf.TF_EPI_RELU2, tf.TF_OUT_BF16, tf.TF_OUT_BF16 | tf.TF_EPI_RELU2])
-def test_prompt_output_options_and_stride(flags):
-    N, K, rows = 300, 2048, 20
+def test_prompt_output_options_and_stride(flags, K):
+    N, rows = 300, 20
     m = synth.make_matrix(N, K, 4, 64, 860, 0.001, 0.03)
     dm = DevMatrix(m)
     xd = dev(synth.make_x(rows, K, 861))
