@@ -129,9 +129,9 @@ Plan layout(int N, int K, int bits, int group, int rows, int nsm, int ctas, bool
 
 // The launch plan, in order of preference (every choice gives the same bits):
 //  0. when consecutive products may overlap (early-x launches), 1-2 rows and at
-//     most eight column tiles per SM: one m-tile per item, one CTA per SM within
-//     half of the SM, so that the next product's CTA is resident beside it and
-//     computes while this one finishes (4096 x 4096 width sweep: 82 -> 69 us
+//     most eight column tiles per SM: one m-tile per item, at most one CTA per SM
+//     within half of the SM, so that the next product's CTA is resident beside it
+//     and computes while this one finishes (4096 x 4096 width sweep: 82 -> 69 us
 //     for the 18 products);
 //  1. up to 8 rows: two m-tiles (32 columns) per item, one CTA per SM, when two
 //     stages fit and the items fill the SMs (two per SM at 1-2 rows, one per two
@@ -149,6 +149,13 @@ Plan make_plan(int N, int K, int bits, int group, int rows, int nsm, bool sb3d, 
         Plan h = layout(N, K, bits, group, rows, nsm, 1, sb3d, 1, 1, true);
         if (h.nsl == 1 && h.stages >= 2 && (long long)h.nmt <= 8LL * nsm) {
             h.grid = std::min(h.grid, nsm);
+            // Up to two items a CTA: as few CTAs as give the busiest one its items
+            // (4096 columns: 128 CTAs of two items, not 152 of one or two); the
+            // critical CTA is the same and the SMs left over take a later product's
+            // CTAs early (width sweep 0.440 -> 0.449).  With more items a CTA the
+            // spread grid measured faster (12288 columns: 6.1 against 7.2 us).
+            const int per = (h.nmt + h.grid - 1) / h.grid;
+            if (per <= 2) h.grid = (h.nmt + per - 1) / per;
             return h;
         }
     }
