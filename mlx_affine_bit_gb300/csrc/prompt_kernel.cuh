@@ -41,6 +41,9 @@ constexpr int EPI_WARPS = 16;           // four per tensor-memory lane quarter: 
 constexpr int EPI_ROWS = PN / (EPI_WARPS / 4);   // window rows per epilogue warp
 constexpr int PRODUCER = UNPACK_WARPS + EPI_WARPS, MMA_WARP = PRODUCER + 1;
 constexpr int THREADS = (MMA_WARP + 1) * 32;
+// Registers a thread: an SM's four schedulers hold 16K registers each and the
+// CTA's 22 warps put six on two of them, so 6 x 32 x 80 <= 16384.
+constexpr int MAX_REGS = 80;
 constexpr int A_BYTES = PM * PSTAGE * 2;         // one unpacked stage (bf16)
 constexpr int X_BYTES = PN * PSTAGE * 2;         // one stage of x (bf16)
 constexpr int SX_BYTES = 32 * PN * 4;            // per-group sums of x of one scale/bias unit (<= 32 groups x 64 rows)
@@ -192,7 +195,7 @@ struct Bars {
 // commits once, the epilogue warps take the stage's groups out of tensor memory
 // and release the slots once.
 template <int BITS, int G, bool MC>
-__global__ void __maxnreg__(80) prompt_kernel(const __grid_constant__ Params P) {
+__global__ void __maxnreg__(MAX_REGS) prompt_kernel(const __grid_constant__ Params P) {
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr int SBP = sb_pitch(G) / 2;                     // scale/bias row pitch (bf16 values)
     constexpr int CP = code_pitch(BITS) / 4;                 // code row pitch (words)

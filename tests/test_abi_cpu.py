@@ -137,6 +137,23 @@ def test_planner_host(tmp_path):
     assert "PASS" in out, out
 
 
+def test_prompt_layout_host(tmp_path):
+    # The prompt kernel's static plan for every width and group: shared memory
+    # within a CTA's limit and above half an SM (one CTA and one tensor-memory
+    # allocation per SM), aligned regions and pitches, whole accumulator sets, and
+    # the register cap within the schedulers' files.  Host code only.
+    import shutil
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not available")
+    exe = str(tmp_path / "prompt_test")
+    subprocess.check_call([nvcc, "-std=c++17", "-O1", "-I" + os.path.join(ROOT, "mlx_affine_bit_gb300", "csrc"),
+                           "-gencode", "arch=compute_103a,code=sm_103a",
+                           os.path.join(ROOT, "tests", "prompt_host_test.cu"), "-o", exe])
+    out = subprocess.check_output([exe]).decode()
+    assert "PASS" in out, out
+
+
 def test_every_kernel_instantiated(tf):
     # 6 widths x 3 groups x row buckets {1, 2, 4, 8, 16} x one m-tile per item, and
     # buckets up to 8 rows with two m-tiles and one or two consumer groups, and
