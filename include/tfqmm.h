@@ -200,7 +200,9 @@ int tf_qmm_ex(const uint16_t *x, int rows, int K,
  *   (K / group) * ceil(rows / 64) * 256 + [(K / 2048) * 64 * N * 4] bytes, grown
  *   on demand; the first call on a stream must precede any graph capture on it).
  *   Plain launches: one prepass, then per 64 rows one launch and, with split
- *   chunks, one fold.
+ *   chunks, one fold.  Measured on GB300 it overtakes 16-row windows of tf_qmm
+ *   from about 24 rows (the 248320 x 2048 LM head; about 30 rows at 12288 x
+ *   2048) and is 2.3-2.4x faster at 64; below that, tf_qmm is faster.
  */
 int tf_qmm_prompt(const uint16_t *x, int rows, int K,
                   const uint32_t *W, const uint16_t *scales, const uint16_t *biases,
