@@ -818,8 +818,11 @@ __device__ void consumer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
     for (ItemWalk iw(P); iw.more(P); iw.next(P), ++own) {
         const Item I = iw.get(P);
         if (I.slice != cur_slice) {
-            // Every group walks every item, so all consumers meet here.
-            named_bar(1, CG * GT);
+            // Every group walks every item, so all consumers meet here before the
+            // x slice is overwritten (the first slice overwrites nothing: its
+            // warps start placing x at once; the barrier after the placement
+            // still orders it before every read).
+            if (cur_slice >= 0) named_bar(1, CG * GT);
             if (G >= 64 && (LR > 2 || I.k_hi - I.k_lo >= 4096))
                 load_x_pieces<G, LR>(P, I, Bf, sx, tid, CG * GT, 1);
             else
