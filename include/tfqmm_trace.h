@@ -7,7 +7,8 @@
  *   [0] the launch's number (0, 1, ... since the last tf_trace_reset, in launch
  *       order on the host), [1] (SM id << 32) | block index, then %globaltimer
  *   (ns) at [2] kernel entry, [3] the producer's first stage issued, [4] that
- *   stage landed, [5] consumer thread 0 past the dependency wait (programmatic
+ *   stage landed (0 in early-x launches of one or two rows, whose producer does
+ *   not wait for it), [5] consumer thread 0 past the dependency wait (programmatic
  *   dependent launch; a launch without it passes at once), [6] the first x
  *   slice placed and summed, [7] the first stage's group products done, [8]
  *   consumer thread 0's last store issued.  A phase the CTA did not reach is 0.

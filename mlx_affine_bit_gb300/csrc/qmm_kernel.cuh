@@ -80,7 +80,7 @@ __device__ __forceinline__ unsigned long long global_ns() {
 enum TracePhase {
     TR_ENTER = 2,     // kernel entry
     TR_TMA0 = 3,      // producer: the CTA's first stage issued
-    TR_LAND0 = 4,     // producer: the first stage landed
+    TR_LAND0 = 4,     // producer: the first stage landed (when the producer waits for it)
     TR_RELEASE = 5,   // consumer thread 0 past the dependency wait
     TR_XLOADED = 6,   // consumer thread 0: the first x slice placed and summed
     TR_STAGE0 = 7,    // consumer thread 0: the first stage's group products done
@@ -362,10 +362,15 @@ __device__ void producer(const QmmParams &P, uint8_t *smem, uint64_t *full, uint
                     }
                 }
                 // The CTA's first stage travels alone: every CTA's first stage
-                // lands before later stages compete with it for DRAM.
+                // lands before later stages compete with it for DRAM -- except in
+                // early-x launches of one or two rows, where the next stages follow
+                // at once (their CTAs overlap the products around them; width sweep
+                // 0.450 -> 0.454, while 3-16 rows measured slower without the rule).
                 if (it == 0 && lane == 0) TFQ_TRACE(smem, TR_TMA0);
-                if (it == 0 && !withhold) mbar_wait(&full[slot], ring.phase, abort, P.status);
-                if (it == 0 && lane == 0) TFQ_TRACE(smem, TR_LAND0);
+                if (it == 0 && !withhold && !(P.early_x && P.rows <= 2)) {
+                    mbar_wait(&full[slot], ring.phase, abort, P.status);
+                    if (lane == 0) TFQ_TRACE(smem, TR_LAND0);
+                }
             } else {
                 // Odd shapes or alignments: plain copies by the warp into the same layout.
                 const int k1 = min(I.k_hi, k0 + CHUNK);

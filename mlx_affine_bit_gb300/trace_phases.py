@@ -12,7 +12,8 @@ after the first `skip`, each CTA's record gives its phases; the script prints, p
 mode and width, the median over those CTAs of
 
     entry->issued   kernel entry to the producer's first stage issued
-    issued->landed  that stage's TMA flight
+    issued->landed  that stage's TMA flight (nan where the producer does not wait
+                    for it: early-x launches of one or two rows)
     entry->release  entry to consumer thread 0 past the dependency wait
     entry->x        entry to the first x slice placed and summed
     x->stage0       x placed to the first stage's group products done
@@ -47,7 +48,7 @@ def phase_table(rec: np.ndarray) -> dict:
     t = t[ok]
     d = {
         "entry->issued": t[:, TMA0] - t[:, ENTER],
-        "issued->landed": t[:, LAND0] - t[:, TMA0],
+        "issued->landed": np.where(t[:, LAND0] > 0, t[:, LAND0] - t[:, TMA0], np.nan),
         "entry->release": t[:, RELEASE] - t[:, ENTER],
         "entry->x": t[:, XLOADED] - t[:, ENTER],
         "x->stage0": t[:, STAGE0] - t[:, XLOADED],
@@ -113,7 +114,8 @@ def run(steps: int, skip: int) -> str:
                         per[k].extend(d[k].tolist())
                     if i > 0:
                         share.append(last_exit[i] - last_exit[i - 1])
-                rows.append((bits, group, {k: float(np.median(v)) for k, v in per.items()}, float(np.median(share))))
+                rows.append((bits, group, {k: float(np.nanmedian(v)) if np.any(np.isfinite(v)) else float("nan")
+                                           for k, v in per.items()}, float(np.median(share))))
             step = [last_exit[(s + 1) * len(mats) - 1] - last_exit[s * len(mats) - 1] for s in range(max(skip, 1), steps)]
             out.append("### %s (medians over steps %d..%d; step %.1f us from last exit to last exit)\n"
                        % (name, skip, steps - 1, float(np.median(step))))

@@ -55,6 +55,7 @@ def test_trace_records(trace_lib, mode):
         assert np.all(r[:, RELEASE] > 0) and np.all(r[:, RELEASE] <= r[:, EXIT])
         w = r[r[:, XLOADED] > 0]                        # CTAs that had an item
         assert len(w) > 0
-        assert np.all(w[:, LAND0] >= w[:, TMA0]) and np.all(w[:, TMA0] >= w[:, ENTER])
+        landed = w[w[:, LAND0] > 0]                     # the producer waited for its first stage
+        assert np.all(landed[:, LAND0] >= landed[:, TMA0]) and np.all(w[:, TMA0] >= w[:, ENTER])
         assert np.all(w[:, XLOADED] >= w[:, ENTER]) and np.all(w[:, STAGE0] >= w[:, XLOADED])
         assert np.all(w[:, EXIT] >= w[:, STAGE0])
